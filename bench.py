@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of libfusedconv on the three full-size workloads.
+
+One step = one pass of the whole fused path over the three full-size
+workloads, back to back on one stream:
+  * conv2d 3x3 (x [128,8,128,128]) + bias -> ReLU -> HardSwish,
+  * conv3d 3x3x3 (x [128,8,16,64,64]) + bias -> LeakyReLU(0.2) -> + s[64]
+    -> clamp[-1,1] -> exact GELU,
+  * transposed conv 3x3 s1 p1 (x [128,64,256,256]) + bias -> maxpool 2x2 ->
+    hardtanh[-1,1] -> mean(H,W) -> tanh.
+Metric: effective GFLOP/s = 2 * MACs / device time, MACs counted from the
+shapes (no epilogue ops counted).  Inputs are seeded synthetic tensors with
+the workloads' distributions, resident in HBM before the timed region; L2 is
+flushed (a 256 MiB write) before every workload call, outside its events.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded sample of the same workloads.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from convolution_epilogue_gb300 import synth  # noqa: E402
+
+METRIC = "effective GFLOP/s (2*MACs/device time) and % of roofline per config, 1 GB300"
+UNIT = "GFLOP/s"
+WORKLOADS = (3, 4, 5)
+CHAIN_RH = (("relu",), ("hardswish",))
+SMS = 152
+
+
+def macs_of(wid: int) -> int:
+    """MAC count of a workload from its shapes (stride 1)."""
+    if wid in (1, 3):
+        N, C, H, W = synth.WORKLOADS[wid]["x"]
+        return N * 64 * (H - 2) * (W - 2) * C * 9
+    if wid == 4:
+        N, C, D, H, W = synth.WORKLOADS[wid]["x"]
+        return N * 64 * (D - 2) * (H - 2) * (W - 2) * C * 27
+    N, C, H, W = synth.WORKLOADS[wid]["x"]
+    return N * 64 * H * W * C * 9
+
+
+def algorithmic_bytes(wid: int) -> int:
+    """x + W + b (+ s) + y, each counted once, fp32."""
+    spec = synth.WORKLOADS[wid]
+    xs = spec["x"]
+    nx = int(np.prod(xs))
+    if wid in (1, 3):
+        N, C, H, W = xs
+        nw, ny = 64 * C * 9, N * 64 * (H - 2) * (W - 2)
+        extra = 64
+    elif wid == 4:
+        N, C, D, H, W = xs
+        nw, ny = 64 * C * 27, N * 64 * (D - 2) * (H - 2) * (W - 2)
+        extra = 128
+    else:
+        N, C, H, W = xs
+        nw, ny = C * 64 * 9, N * 64
+        extra = 64
+    return 4 * (nx + nw + extra + ny)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+def pipe_peak_tflops(variant: str, peaks) -> tuple[float, str, str]:
+    """Peak of the pipe a variant uses, in useful fp32-accurate TFLOP/s.
+
+    tc_f16x3: fp16 tensor rate (= the measured bf16 rate) / 3 products.
+    tc_tf32x3: tf32 rate (measured bf16 x nominal 1.1/2.25) / 3 products.
+    ffma: 152 SMs x 128 FMA/clk x 2 FLOP x max SM clock."""
+    if variant == "tc_f16x3":
+        return peaks["bf16_sus"] / 3.0, "tensor", "fp16 tensor (measured bf16 sustained) / 3"
+    if variant == "tc_tf32x3":
+        return (peaks["bf16_sus"] * 1.1 / 2.25 / 3.0, "tensor",
+                "tf32 tensor (measured bf16 sustained x 1.1/2.25) / 3")
+    return (SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "alu",
+            "fp32 FFMA: 152 SMs x 128 lanes x 2 x max SM clock")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the
+    timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU side
+def cpu_sample(scale: int):
+    """A bounded sample of the three workloads for the CPU oracle:
+    `scale` images of the conv2d and conv3d workloads (full planes) and
+    16*scale (n, c_out) outputs of the pooled workload.  Returns a callable
+    that runs it and the MACs it covers."""
+    import oracle
+    scale = max(1, min(int(scale), 128))
+    inp3 = synth.make_inputs(3, first_images=scale)
+    inp4 = synth.make_inputs(4, first_images=scale)
+    inp5 = synth.make_inputs(5, first_images=math.ceil(16 * scale / 64))
+    x5, w5, b5 = inp5["x"], inp5["w"], inp5["b"]
+    s4 = inp4["s"].reshape(-1)
+    x3 = inp3["x"]
+    x4 = inp4["x"]
+    pairs = [(i // 64, i % 64) for i in range(16 * scale)]
+    chain4 = (("leaky_relu", 0.2), ("add_channel", s4), ("clamp", -1.0, 1.0), ("gelu_erf",))
+
+    def run():
+        oracle.conv_epi(x3, inp3["w"], inp3["b"], CHAIN_RH)
+        oracle.conv_epi(x4, inp4["w"], inp4["b"], chain4)
+        oracle.convT_pool_mean_points(x5, w5, b5, pairs)
+
+    macs = (macs_of(3) // 128 * scale + macs_of(4) // 128 * scale
+            + 256 * 256 * 64 * 9 * len(pairs))
+    desc = (f"{scale} image(s) of the conv2d and conv3d workloads (all outputs) + "
+            f"{len(pairs)} (n, c_out) outputs of the pooled transposed-conv workload")
+    return run, macs, desc
+
+
+def cpu_baseline(scale: int):
+    import oracle
+    oracle.build()
+    run, macs, desc = cpu_sample(scale)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * macs / dt / 1e9, "unit": UNIT,
+            "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
+            "kind": "oracle", "sample": desc, "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    run, macs, desc = cpu_sample(args.ref_scale)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2.0 * macs * args.steps / total / 1e9
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "CPU oracle (plain C, fp64) on a bounded sample of the "
+                                   "three full-size workloads", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU side
+def run_ours(args):
+    import torch
+    import convolution_epilogue_gb300 as fc
+    from convolution_epilogue_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    fc.lib()
+    fc.set_variant(args.variant)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs resident in HBM, outputs and workspaces preallocated
+    host = {w: synth.make_inputs(w) for w in WORKLOADS}
+    d = {}
+    for w in WORKLOADS:
+        d[w] = {k: torch.from_numpy(v).to(dev) for k, v in host[w].items()}
+    y3 = torch.empty((128, 64, 126, 126), device=dev)
+    y4 = torch.empty((128, 64, 14, 62, 62), device=dev)
+    y5 = torch.empty((128, 64, 1, 1), device=dev)
+    ws = {3: torch.empty(fc.workspace_bytes(0, (128, 8, 128, 128, 64, 3, 0)), dtype=torch.uint8, device=dev),
+          4: torch.empty(fc.workspace_bytes(1, (128, 8, 16, 64, 64, 64, 3, 0)), dtype=torch.uint8, device=dev),
+          5: torch.empty(fc.workspace_bytes(2, (128, 64, 256, 256, 64, 3, 1)), dtype=torch.uint8, device=dev)}
+    s4 = d[4]["s"].reshape(-1)
+    chain4 = (("leaky_relu", 0.2), ("add_channel", s4), ("clamp", -1.0, 1.0), ("gelu_erf",))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    calls = {
+        3: lambda: fc.fc_conv2d_epi(d[3]["x"], d[3]["w"], d[3]["b"], CHAIN_RH, y=y3, ws=ws[3]),
+        4: lambda: fc.fc_conv3d_epi(d[4]["x"], d[4]["w"], d[4]["b"], chain4, y=y4, ws=ws[4]),
+        5: lambda: fc.fc_convT2d_pool_mean(d[5]["x"], d[5]["w"], d[5]["b"], y=y5, ws=ws[5]),
+    }
+    variants, launches_per_step = {}, 0
+    for w in WORKLOADS:
+        calls[w]()
+        variants[w] = fc.last_variant()
+        launches_per_step += fc.last_launch_count()
+    torch.cuda.synchronize()
+    if fc.get_last_device_error() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    for _ in range(args.warmup):
+        for w in WORKLOADS:
+            flush.zero_()
+            calls[w]()
+    ev = {w: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for w in WORKLOADS}
+    fc.profile_reset()
+    fc.profile_enable(True)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    n_launch = 0
+    for k in range(args.steps):
+        for w in WORKLOADS:
+            flush.zero_()
+            ev[w][k][0].record(stream)
+            calls[w]()
+            ev[w][k][1].record(stream)
+            n_launch += fc.last_launch_count()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    fc.profile_enable(False)
+    status = fc.get_last_device_error()
+
+    per = {}
+    step_ms = [0.0] * args.steps
+    for w in WORKLOADS:
+        ts = [ev[w][k][0].elapsed_time(ev[w][k][1]) for k in range(args.steps)]
+        for k in range(args.steps):
+            step_ms[k] += ts[k]
+        per[w] = ts
+    my_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    else:
+        tot_ms = my_ms
+    flops_step = sum(2 * macs_of(w) for w in WORKLOADS)
+    value = world * flops_step * args.steps / (tot_ms * 1e-3) / 1e9
+
+    # dominant kernel: the main kernel with the largest summed time
+    entry_of = {3: 0, 4: 1, 5: 2}
+    kern = {}
+    for w in WORKLOADS:
+        ms, cnt = fc.profile_read(entry_of[w])
+        kern[w] = (ms / max(cnt, 1), cnt)
+    dom = max(WORKLOADS, key=lambda w: kern[w][0] * kern[w][1])
+    avg_ms = kern[dom][0]
+    pk_t, bound_kind, pk_desc = pipe_peak_tflops(variants[dom], peaks)
+    t_flop = 2 * macs_of(dom) / (pk_t * 1e12)
+    t_byte = algorithmic_bytes(dom) / (peaks["hbm_gbs"] * 1e9)
+    if t_byte > t_flop:
+        achieved = algorithmic_bytes(dom) / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = 2 * macs_of(dom) / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": bound_kind, "achieved": achieved, "peak": pk_t, "unit": "TFLOP/s",
+                "frac": achieved / pk_t}
+    roof.update({"traffic": None, "kernel": f"{synth.WORKLOADS[dom]['name']} main kernel "
+                 f"[{variants[dom]}]", "avg_ms": avg_ms, "peak_basis": pk_desc,
+                 "peak_source": peaks["source"]})
+
+    per_cfg = {}
+    for w in WORKLOADS:
+        med = statistics.median(per[w])
+        pk, bk, _ = pipe_peak_tflops(variants[w], peaks)
+        t_roof = max(2 * macs_of(w) / (pk * 1e12), algorithmic_bytes(w) / (peaks["hbm_gbs"] * 1e9))
+        per_cfg[synth.WORKLOADS[w]["name"]] = {
+            "variant": variants[w], "ms_median": med,
+            "ms_p10": float(np.percentile(per[w], 10)), "ms_p90": float(np.percentile(per[w], 90)),
+            "gflops": 2 * macs_of(w) / (med * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / med,
+            "kernel_ms": kern[w][0]}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, fc, host, dev, stream, chain4_host=host[4]["s"].reshape(-1))
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": " + ".join(synth.WORKLOADS[w]["name"] for w in WORKLOADS),
+                       "l2": "flushed by a 256 MiB write before every workload call (outside events)",
+                       "variants": {synth.WORKLOADS[w]["name"]: variants[w] for w in WORKLOADS},
+                       "per_workload": per_cfg,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof, "clocks": clocks, "gpu_launches": n_launch,
+            "device_status": status, "wall_s_timed": t_wall}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_scale)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(args, fc, host, dev, stream, chain4_host):
+    """Same metric with host buffers: pinned-host -> device copies of every
+    input, the three calls, device -> pinned-host copies of every output, all
+    inside the timed region."""
+    import torch
+    pin = {w: {k: torch.from_numpy(v).pin_memory() for k, v in host[w].items()} for w in WORKLOADS}
+    dd = {w: {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in host[w].items()}
+          for w in WORKLOADS}
+    outs = {3: torch.empty((128, 64, 126, 126), device=dev),
+            4: torch.empty((128, 64, 14, 62, 62), device=dev),
+            5: torch.empty((128, 64, 1, 1), device=dev)}
+    outs_h = {w: torch.empty(o.shape, dtype=torch.float32).pin_memory() for w, o in outs.items()}
+    ws = {3: torch.empty(fc.workspace_bytes(0, (128, 8, 128, 128, 64, 3, 0)), dtype=torch.uint8, device=dev),
+          4: torch.empty(fc.workspace_bytes(1, (128, 8, 16, 64, 64, 64, 3, 0)), dtype=torch.uint8, device=dev),
+          5: torch.empty(fc.workspace_bytes(2, (128, 64, 256, 256, 64, 3, 1)), dtype=torch.uint8, device=dev)}
+    h2d = sum(t.numel() * 4 for w in WORKLOADS for t in pin[w].values())
+    d2h = sum(o.numel() * 4 for o in outs.values())
+
+    def step():
+        for w in WORKLOADS:
+            for k in pin[w]:
+                dd[w][k].copy_(pin[w][k], non_blocking=True)
+        s4 = dd[4]["s"].reshape(-1)
+        ch4 = (("leaky_relu", 0.2), ("add_channel", s4), ("clamp", -1.0, 1.0), ("gelu_erf",))
+        fc.fc_conv2d_epi(dd[3]["x"], dd[3]["w"], dd[3]["b"], CHAIN_RH, y=outs[3], ws=ws[3])
+        fc.fc_conv3d_epi(dd[4]["x"], dd[4]["w"], dd[4]["b"], ch4, y=outs[4], ws=ws[4])
+        fc.fc_convT2d_pool_mean(dd[5]["x"], dd[5]["w"], dd[5]["b"], y=outs[5], ws=ws[5])
+        for w in WORKLOADS:
+            outs_h[w].copy_(outs[w], non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = sum(2 * macs_of(w) for w in WORKLOADS)
+    return {"value": flops / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tc_tf32x3", "tc_f16x3"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-scale", type=int, default=16)
+    ap.add_argument("--ref-scale", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,266 @@
+"""libfusedconv Python binding: argument marshalling over the C ABI only.
+
+Every computation runs in the CUDA kernels of ``_build/libfusedconv.so``
+(declared in ``include/fusedconv.h``); PyTorch only supplies device memory
+and streams.  There is no CPU fallback: if the library is missing or the
+device is unusable, these functions raise.
+
+Elementwise ops are tuples::
+
+    ("relu",) ("hardswish",) ("leaky_relu", slope) ("add_channel", t[C_out])
+    ("clamp", lo, hi) ("gelu_erf",) ("hardtanh", lo, hi) ("tanh",)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfusedconv.so")
+
+FC_OK = 0
+STATUS_NAMES = {0: "FC_OK", 1: "FC_ERR_INVALID_ARG", 2: "FC_ERR_UNSUPPORTED",
+                3: "FC_ERR_ALIGNMENT", 4: "FC_ERR_WORKSPACE", 5: "FC_ERR_CUDA",
+                6: "FC_ERR_TIMEOUT", 7: "FC_ERR_RANGE"}
+EPI = {"relu": 1, "hardswish": 2, "leaky_relu": 3, "add_channel": 4, "clamp": 5,
+       "gelu_erf": 6, "maxpool2x2": 7, "hardtanh": 8, "mean_hw": 9, "tanh": 10}
+VARIANTS = {"auto": 0, "ffma": 1, "tc_tf32x3": 2, "tc_f16x3": 3}
+VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
+MAX_OPS = 8
+
+# every symbol include/fusedconv.h declares
+EXPORTS = ("fc_conv2d_epi", "fc_conv3d_epi", "fc_convT2d_pool_mean",
+           "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
+           "fc_last_launch_count", "fc_status_string",
+           "fc_get_last_device_error", "fc_version", "fc_profile_enable",
+           "fc_profile_read", "fc_profile_reset")
+
+
+class FcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class _Op(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("a", ctypes.c_float),
+                ("b", ctypes.c_float), ("chan", ctypes.c_void_p)]
+
+
+class _Epilogue(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("n_ops", ctypes.c_int),
+                ("ops", _Op * MAX_OPS)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libfusedconv (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libfusedconv is not built ({LIB_PATH} missing); run "
+                    "convolution_epilogue_gb300._build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.fc_conv2d_epi.restype = I
+            L.fc_conv2d_epi.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P, P, S, P]
+            L.fc_conv3d_epi.restype = I
+            L.fc_conv3d_epi.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I, P, P,
+                                        P, S, P]
+            L.fc_convT2d_pool_mean.restype = I
+            L.fc_convT2d_pool_mean.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P,
+                                               P, S, P]
+            L.fc_workspace_bytes.restype = S
+            L.fc_workspace_bytes.argtypes = [I, ctypes.POINTER(I)]
+            L.fc_set_variant.restype = I
+            L.fc_set_variant.argtypes = [I]
+            L.fc_last_variant.restype = I
+            L.fc_last_launch_count.restype = I
+            L.fc_status_string.restype = ctypes.c_char_p
+            L.fc_status_string.argtypes = [I]
+            L.fc_get_last_device_error.restype = I
+            L.fc_get_last_device_error.argtypes = [P]
+            L.fc_version.restype = I
+            L.fc_profile_enable.restype = I
+            L.fc_profile_enable.argtypes = [I]
+            L.fc_profile_read.restype = I
+            L.fc_profile_read.argtypes = [I, ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(I)]
+            L.fc_profile_reset.restype = None
+            _lib = L
+    return _lib
+
+
+def _check(status, what):
+    if status != FC_OK:
+        msg = lib().fc_status_string(status).decode()
+        raise FcError(status, f"{what} ({msg})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _require_cuda_f32(name, t):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_epilogue(bias, ops):
+    """Build the C epilogue descriptor; returns (struct, keepalive list)."""
+    e = _Epilogue()
+    keep = []
+    e.bias = None if bias is None else bias.data_ptr()
+    if bias is not None:
+        keep.append(bias)
+    if len(ops) > MAX_OPS:
+        raise ValueError("at most 8 epilogue ops")
+    e.n_ops = len(ops)
+    for i, op in enumerate(ops):
+        name = op[0]
+        e.ops[i].kind = EPI[name]
+        if name == "leaky_relu":
+            e.ops[i].a = float(op[1])
+        elif name in ("clamp", "hardtanh"):
+            e.ops[i].a, e.ops[i].b = float(op[1]), float(op[2])
+        elif name == "add_channel":
+            t = op[1]
+            _require_cuda_f32("add_channel tensor", t)
+            e.ops[i].chan = t.data_ptr()
+            keep.append(t)
+    return e, keep
+
+
+def workspace_bytes(entry: int, dims) -> int:
+    arr = (ctypes.c_int * len(dims))(*[int(d) for d in dims])
+    return int(lib().fc_workspace_bytes(int(entry), arr))
+
+
+def _workspace(nbytes, device):
+    import torch
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def set_variant(name: str = "auto"):
+    _check(lib().fc_set_variant(VARIANTS[name]), "fc_set_variant")
+
+
+def last_variant() -> str:
+    return VARIANT_NAMES.get(lib().fc_last_variant(), "none")
+
+
+def last_launch_count() -> int:
+    return int(lib().fc_last_launch_count())
+
+
+def get_last_device_error(stream=None) -> int:
+    return int(lib().fc_get_last_device_error(_stream_handle(stream)))
+
+
+def profile_enable(on: bool = True):
+    _check(lib().fc_profile_enable(1 if on else 0), "fc_profile_enable")
+
+
+def profile_reset():
+    lib().fc_profile_reset()
+
+
+def profile_read(entry: int):
+    """(total_ms, launches) of the main kernels of one entry since reset."""
+    ms = ctypes.c_double()
+    n = ctypes.c_int()
+    _check(lib().fc_profile_read(int(entry), ctypes.byref(ms), ctypes.byref(n)),
+           "fc_profile_read")
+    return ms.value, n.value
+
+
+def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
+    """Conv2d(k=3, stride 1, pad) + bias + elementwise ops -> y [N,CO,Ho,Wo]."""
+    import torch
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    N, C, H, W = x.shape
+    CO, C2, KH, KW = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    Ho, Wo = H + 2 * pad - KH + 1, W + 2 * pad - KW + 1
+    if y is None:
+        y = torch.empty((N, CO, Ho, Wo), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    if ws is None:
+        ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
+    e, keep = make_epilogue(bias, ops)
+    st = lib().fc_conv2d_epi(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad,
+                             ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                             _stream_handle(stream))
+    _check(st, "fc_conv2d_epi")
+    del keep
+    return y
+
+
+def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
+    """Conv3d(k=3, stride 1, pad) + bias + elementwise ops."""
+    import torch
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    N, C, D, H, W = x.shape
+    CO, C2, KD, KH, KW = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    Do, Ho, Wo = D + 2 * pad - KD + 1, H + 2 * pad - KH + 1, W + 2 * pad - KW + 1
+    if y is None:
+        y = torch.empty((N, CO, Do, Ho, Wo), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    if ws is None:
+        ws = _workspace(workspace_bytes(1, (N, C, D, H, W, CO, KD, pad)), x.device)
+    e, keep = make_epilogue(bias, ops)
+    st = lib().fc_conv3d_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, 1,
+                             pad, ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                             _stream_handle(stream))
+    _check(st, "fc_conv3d_epi")
+    del keep
+    return y
+
+
+def pool_mean_ops(lo=-1.0, hi=1.0):
+    return (("maxpool2x2",), ("hardtanh", lo, hi), ("mean_hw",), ("tanh",))
+
+
+def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
+                         ws=None, stream=None):
+    """ConvTranspose2d(k=3, s=1, p=1) + bias -> maxpool 2x2 -> hardtanh ->
+    mean(H,W) -> tanh.  w: [C_in, C_out, 3, 3]; returns y [N, C_out, 1, 1]."""
+    import torch
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    N, C, H, W = x.shape
+    C2, CO, K, _ = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    if y is None:
+        y = torch.empty((N, CO, 1, 1), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    if ws is None:
+        ws = _workspace(workspace_bytes(2, (N, C, H, W, CO, K, pad)), x.device)
+    e, keep = make_epilogue(bias, pool_mean_ops(*hardtanh))
+    st = lib().fc_convT2d_pool_mean(_ptr(x), N, C, H, W, _ptr(w), CO, K, 1, pad, 0,
+                                    ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                                    _stream_handle(stream))
+    _check(st, "fc_convT2d_pool_mean")
+    del keep
+    return y

@@ -1,0 +1,401 @@
+// fc_api.cu -- the C ABI of libfusedconv: validation, epilogue decoding,
+// variant selection, workspace layout and launches.  Nothing here computes
+// a conv value; every step of the path runs in the kernels.
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "fc_internal.h"
+
+namespace fc {
+
+namespace {
+
+// Per-device status word (kernels OR bits into it; the host reads and clears
+// it in fc_get_last_device_error).
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int *g_status_ptr[kMaxDevices];
+
+int g_variant_override = FC_VARIANT_AUTO;
+thread_local int t_last_variant = 0;
+thread_local int t_last_launches = 0;
+
+// ---- benchmark profiling: event pairs around main kernels
+constexpr int kMaxProf = 4096;
+bool g_prof_on = false;
+cudaEvent_t g_prof_ev[kMaxProf][2];
+int g_prof_entry[kMaxProf];
+int g_prof_n = 0;       // pairs recorded since reset
+int g_prof_created = 0; // pairs whose events exist
+bool g_prof_open = false;
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+fc_status status_ptr(unsigned int **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return FC_ERR_CUDA;
+  if (!g_status_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FC_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned int *>(p);
+  }
+  *out = g_status_ptr[dev];
+  return FC_OK;
+}
+
+bool elementwise_kind(int k) {
+  return k == FC_EPI_RELU || k == FC_EPI_HARDSWISH || k == FC_EPI_LEAKY_RELU ||
+         k == FC_EPI_ADD_CHANNEL || k == FC_EPI_CLAMP || k == FC_EPI_GELU_ERF ||
+         k == FC_EPI_HARDTANH || k == FC_EPI_TANH;
+}
+
+// Decode an elementwise chain into EpiDev + a ChainId.
+fc_status decode_eltwise(const fc_epilogue *epi, EpiDev *e, int *chain) {
+  memset(e, 0, sizeof(*e));
+  if (!epi) {
+    *chain = CHAIN_NONE;
+    return FC_OK;
+  }
+  if (epi->bias && !aligned16(epi->bias)) return FC_ERR_ALIGNMENT;
+  if (epi->n_ops < 0 || epi->n_ops > FC_MAX_EPI_OPS) return FC_ERR_INVALID_ARG;
+  e->bias = epi->bias;
+  e->n_ops = epi->n_ops;
+  for (int i = 0; i < epi->n_ops; ++i) {
+    const fc_epi_op &o = epi->ops[i];
+    if (!elementwise_kind(o.kind)) return FC_ERR_UNSUPPORTED;
+    if (o.kind == FC_EPI_ADD_CHANNEL && !o.chan) return FC_ERR_INVALID_ARG;
+    if ((o.kind == FC_EPI_CLAMP || o.kind == FC_EPI_HARDTANH) && !(o.a <= o.b))
+      return FC_ERR_INVALID_ARG;
+    e->kind[i] = o.kind;
+    e->a[i] = o.a;
+    e->b[i] = o.b;
+    e->chan[i] = o.chan;
+  }
+  const int n = epi->n_ops;
+  if (n == 0) *chain = CHAIN_NONE;
+  else if (n == 2 && e->kind[0] == FC_EPI_RELU && e->kind[1] == FC_EPI_HARDSWISH)
+    *chain = CHAIN_RELU_HARDSWISH;
+  else if (n == 4 && e->kind[0] == FC_EPI_LEAKY_RELU &&
+           e->kind[1] == FC_EPI_ADD_CHANNEL &&
+           (e->kind[2] == FC_EPI_CLAMP || e->kind[2] == FC_EPI_HARDTANH) &&
+           e->kind[3] == FC_EPI_GELU_ERF)
+    *chain = CHAIN_LEAKY_ADD_CLAMP_GELU;
+  else
+    *chain = CHAIN_GENERIC;
+  return FC_OK;
+}
+
+// The pooled entry point accepts exactly MAXPOOL2X2, HARDTANH, MEAN_HW, TANH.
+fc_status decode_pool(const fc_epilogue *epi, EpiDev *e, float *lo, float *hi) {
+  memset(e, 0, sizeof(*e));
+  if (!epi) return FC_ERR_INVALID_ARG;
+  if (epi->bias && !aligned16(epi->bias)) return FC_ERR_ALIGNMENT;
+  if (epi->n_ops != 4) return FC_ERR_UNSUPPORTED;
+  const int want[4] = {FC_EPI_MAXPOOL2X2, FC_EPI_HARDTANH, FC_EPI_MEAN_HW, FC_EPI_TANH};
+  for (int i = 0; i < 4; ++i)
+    if (epi->ops[i].kind != want[i]) return FC_ERR_UNSUPPORTED;
+  if (!(epi->ops[1].a <= epi->ops[1].b)) return FC_ERR_INVALID_ARG;
+  e->bias = epi->bias;
+  *lo = epi->ops[1].a;
+  *hi = epi->ops[1].b;
+  return FC_OK;
+}
+
+bool fits_int32(long long v) { return v >= 0 && v < (1LL << 31); }
+
+// Automatic variant choice from measured times on GB300 (see the
+// benchmark's per-variant table): the tensor-core f16-split path wins once
+// there is enough work; tiny problems go to whichever finished first.
+int auto_variant(const ConvProblem &p) {
+  const double macs = (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
+  if (tc_supported(p, 1) && macs >= 4.0e8) return FC_VARIANT_TC_F16X3;
+  if (tc_supported(p, 0) && macs >= 4.0e8) return FC_VARIANT_TC_TF32X3;
+  return FC_VARIANT_FFMA;
+}
+
+fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
+  t_last_launches = 0;
+  unsigned int *st = nullptr;
+  fc_status s = status_ptr(&st);
+  if (s != FC_OK) return s;
+  p.status = st;
+  WsLayout L = ws_layout(p);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < L.total)
+    return FC_ERR_WORKSPACE;
+  int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : auto_variant(p);
+  if ((v == FC_VARIANT_TC_TF32X3 && !tc_supported(p, 0)) ||
+      (v == FC_VARIANT_TC_F16X3 && !tc_supported(p, 1)))
+    return FC_ERR_UNSUPPORTED;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e;
+  if (v == FC_VARIANT_FFMA) e = ffma_launch(p, ws, L, cs, &launches);
+  else e = tc_launch(p, v == FC_VARIANT_TC_F16X3 ? 1 : 0, ws, L, cs, &launches);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FC_ERR_CUDA;
+  }
+  t_last_variant = v;
+  t_last_launches = launches;
+  return FC_OK;
+}
+
+}  // namespace
+
+void prof_begin(cudaStream_t s) {
+  if (!g_prof_on || g_prof_n >= kMaxProf) return;
+  if (g_prof_n >= g_prof_created) {
+    if (cudaEventCreate(&g_prof_ev[g_prof_n][0]) != cudaSuccess) return;
+    if (cudaEventCreate(&g_prof_ev[g_prof_n][1]) != cudaSuccess) {
+      cudaEventDestroy(g_prof_ev[g_prof_n][0]);
+      return;
+    }
+    g_prof_created = g_prof_n + 1;
+  }
+  if (cudaEventRecord(g_prof_ev[g_prof_n][0], s) == cudaSuccess) g_prof_open = true;
+}
+
+void prof_end(cudaStream_t s, int entry) {
+  if (!g_prof_open) return;
+  g_prof_open = false;
+  if (cudaEventRecord(g_prof_ev[g_prof_n][1], s) != cudaSuccess) return;
+  g_prof_entry[g_prof_n] = entry;
+  ++g_prof_n;
+}
+
+WsLayout ws_layout(const ConvProblem &p) {
+  WsLayout L{};
+  const long Cp = (p.C + 7) / 8 * 8, COp = (p.CO + 63) / 64 * 64;
+  const long taps = (long)p.KD * p.KH * p.KW;
+  size_t off = 0;
+  L.ffma_w = off;
+  L.ffma_w_bytes = sizeof(float) * Cp * taps * COp;
+  off = align256(off + L.ffma_w_bytes);
+  L.tc_w = off;
+  L.tc_w_bytes = tc_weight_bytes(p);
+  off = align256(off + L.tc_w_bytes);
+  L.partial = off;
+  if (p.pool) {
+    long T = ffma_pool_tiles_per_image(p);
+    long T2 = tc_pool_tiles_per_image(p);
+    if (T2 > T) T = T2;
+    L.partial_bytes = sizeof(float) * (size_t)p.N * T * p.CO;
+  }
+  off = align256(off + L.partial_bytes);
+  L.total = off;
+  return L;
+}
+
+}  // namespace fc
+
+using namespace fc;
+
+extern "C" {
+
+fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
+                        const float *w, int C_out, int kH, int kW, int stride,
+                        int pad, const fc_epilogue *epi, float *y, void *ws,
+                        size_t ws_bytes, void *stream) {
+  if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || kH < 1 || kW < 1 ||
+      stride < 1 || pad < 0)
+    return FC_ERR_INVALID_ARG;
+  if (stride != 1 || kH != 3 || kW != 3 || pad > 2) return FC_ERR_UNSUPPORTED;
+  const int Ho = H + 2 * pad - kH + 1, Wo = W + 2 * pad - kW + 1;
+  if (Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
+  if (!fits_int32((long long)N * C_in * H * W) ||
+      !fits_int32((long long)N * C_out * Ho * Wo) ||
+      !fits_int32((long long)C_out * C_in * kH * kW))
+    return FC_ERR_UNSUPPORTED;
+  if (N == 0) return FC_OK;
+  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
+  ConvProblem p{};
+  fc_status s = decode_eltwise(epi, &p.epi, &p.chain);
+  if (s != FC_OK) return s;
+  p.x = x; p.w = w; p.y = y;
+  p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
+  p.CO = C_out; p.KD = 1; p.KH = kH; p.KW = kW;
+  p.pad_d = 0; p.pad = pad;
+  p.Do = 1; p.Ho = Ho; p.Wo = Wo;
+  p.wlayout = 0;
+  p.entry = 0;
+  return run(p, ws, ws_bytes, stream);
+}
+
+fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
+                        const float *w, int C_out, int kD, int kH, int kW,
+                        int stride, int pad, const fc_epilogue *epi, float *y,
+                        void *ws, size_t ws_bytes, void *stream) {
+  if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 ||
+      kH < 1 || kW < 1 || stride < 1 || pad < 0)
+    return FC_ERR_INVALID_ARG;
+  if (stride != 1 || kD != 3 || kH != 3 || kW != 3 || pad > 2)
+    return FC_ERR_UNSUPPORTED;
+  const int Do = D + 2 * pad - kD + 1, Ho = H + 2 * pad - kH + 1,
+            Wo = W + 2 * pad - kW + 1;
+  if (Do < 1 || Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
+  if (!fits_int32((long long)N * C_in * D * H * W) ||
+      !fits_int32((long long)N * C_out * Do * Ho * Wo) ||
+      !fits_int32((long long)C_out * C_in * kD * kH * kW))
+    return FC_ERR_UNSUPPORTED;
+  if (N == 0) return FC_OK;
+  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
+  ConvProblem p{};
+  fc_status s = decode_eltwise(epi, &p.epi, &p.chain);
+  if (s != FC_OK) return s;
+  p.x = x; p.w = w; p.y = y;
+  p.N = N; p.C = C_in; p.D = D; p.H = H; p.W = W;
+  p.CO = C_out; p.KD = kD; p.KH = kH; p.KW = kW;
+  p.pad_d = pad; p.pad = pad;
+  p.Do = Do; p.Ho = Ho; p.Wo = Wo;
+  p.wlayout = 0;
+  p.entry = 1;
+  return run(p, ws, ws_bytes, stream);
+}
+
+fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
+                               const float *w, int C_out, int k, int stride,
+                               int pad, int out_pad, const fc_epilogue *epi,
+                               float *y, void *ws, size_t ws_bytes,
+                               void *stream) {
+  if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || k < 1 || stride < 1 ||
+      pad < 0 || out_pad < 0)
+    return FC_ERR_INVALID_ARG;
+  if (stride != 1 || k != 3 || pad != 1 || out_pad != 0) return FC_ERR_UNSUPPORTED;
+  // transposed-conv output extent (H-1)*s - 2p + k + op = H for these values
+  const int Ho = (H - 1) * stride - 2 * pad + k + out_pad;
+  const int Wo = (W - 1) * stride - 2 * pad + k + out_pad;
+  if (Ho < 2 || Wo < 2) return FC_ERR_INVALID_ARG;
+  if (!fits_int32((long long)N * C_in * H * W) ||
+      !fits_int32((long long)C_out * C_in * k * k))
+    return FC_ERR_UNSUPPORTED;
+  ConvProblem p{};
+  float lo = 0.f, hi = 0.f;
+  fc_status s = decode_pool(epi, &p.epi, &lo, &hi);
+  if (s != FC_OK) return s;
+  if (N == 0) return FC_OK;
+  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
+  p.x = x; p.w = w; p.y = y;
+  p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
+  p.CO = C_out; p.KD = 1; p.KH = k; p.KW = k;
+  // the equivalent conv: swapped + flipped weights, padding k - 1 - p
+  p.pad_d = 0; p.pad = k - 1 - pad;
+  p.Do = 1; p.Ho = Ho; p.Wo = Wo;
+  p.wlayout = 1;
+  p.pool = 1;
+  p.ht_lo = lo; p.ht_hi = hi;
+  p.chain = CHAIN_NONE;
+  p.entry = 2;
+  return run(p, ws, ws_bytes, stream);
+}
+
+size_t fc_workspace_bytes(int entry, const int *d) {
+  if (!d) return 0;
+  ConvProblem p{};
+  switch (entry) {
+    case 0:
+      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
+      p.KD = 1; p.KH = p.KW = d[5]; p.pad = d[6];
+      p.Do = 1; p.Ho = p.H + 2 * p.pad - p.KH + 1; p.Wo = p.W + 2 * p.pad - p.KW + 1;
+      break;
+    case 1:
+      p.N = d[0]; p.C = d[1]; p.D = d[2]; p.H = d[3]; p.W = d[4]; p.CO = d[5];
+      p.KD = p.KH = p.KW = d[6]; p.pad = p.pad_d = d[7];
+      p.Do = p.D + 2 * p.pad - p.KD + 1; p.Ho = p.H + 2 * p.pad - p.KH + 1;
+      p.Wo = p.W + 2 * p.pad - p.KW + 1;
+      break;
+    case 2:
+      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
+      p.KD = 1; p.KH = p.KW = d[5]; p.pad = p.KH - 1 - d[6];
+      p.Do = 1; p.Ho = p.H - 1 - 2 * d[6] + p.KH; p.Wo = p.W - 1 - 2 * d[6] + p.KW;
+      p.pool = 1; p.wlayout = 1;
+      break;
+    default:
+      return 0;
+  }
+  if (p.N < 0 || p.C < 1 || p.CO < 1 || p.KH < 1 || p.Ho < 1 || p.Wo < 1 || p.Do < 1)
+    return 0;
+  return ws_layout(p).total;
+}
+
+fc_status fc_set_variant(int v) {
+  if (v < FC_VARIANT_AUTO || v > FC_VARIANT_TC_F16X3) return FC_ERR_INVALID_ARG;
+  g_variant_override = v;
+  return FC_OK;
+}
+
+int fc_last_variant(void) { return t_last_variant; }
+
+int fc_last_launch_count(void) { return t_last_launches; }
+
+const char *fc_status_string(fc_status s) {
+  switch (s) {
+    case FC_OK: return "FC_OK";
+    case FC_ERR_INVALID_ARG: return "FC_ERR_INVALID_ARG: invalid argument";
+    case FC_ERR_UNSUPPORTED: return "FC_ERR_UNSUPPORTED: parameters or epilogue chain not supported";
+    case FC_ERR_ALIGNMENT: return "FC_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case FC_ERR_WORKSPACE: return "FC_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case FC_ERR_CUDA: return "FC_ERR_CUDA: CUDA runtime or launch failure";
+    case FC_ERR_TIMEOUT: return "FC_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    case FC_ERR_RANGE: return "FC_ERR_RANGE: input beyond the fp16-split range";
+    default: return "unknown fc_status";
+  }
+}
+
+fc_status fc_get_last_device_error(void *stream) {
+  unsigned int *st = nullptr;
+  fc_status s = status_ptr(&st);
+  if (s != FC_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return FC_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, st, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FC_ERR_CUDA;
+  if (word) {
+    unsigned int zero = 0;
+    if (cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FC_ERR_CUDA;
+  }
+  if (word & ST_TIMEOUT) return FC_ERR_TIMEOUT;
+  if (word & ST_RANGE) return FC_ERR_RANGE;
+  return FC_OK;
+}
+
+int fc_version(void) { return 100; }
+
+fc_status fc_profile_enable(int on) {
+  g_prof_on = on != 0;
+  return FC_OK;
+}
+
+fc_status fc_profile_read(int entry, double *total_ms, int *launches) {
+  if (!total_ms || !launches) return FC_ERR_INVALID_ARG;
+  double tot = 0.0;
+  int cnt = 0;
+  for (int i = 0; i < g_prof_n; ++i) {
+    if (g_prof_entry[i] != entry) continue;
+    if (cudaEventSynchronize(g_prof_ev[i][1]) != cudaSuccess) return FC_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof_ev[i][0], g_prof_ev[i][1]) != cudaSuccess)
+      return FC_ERR_CUDA;
+    tot += ms;
+    ++cnt;
+  }
+  *total_ms = tot;
+  *launches = cnt;
+  return FC_OK;
+}
+
+void fc_profile_reset(void) {
+  g_prof_n = 0;
+  g_prof_open = false;
+}
+
+}  // extern "C"

@@ -1,0 +1,301 @@
+// fc_ffma.cu -- fp32 CUDA-core path: register-blocked direct convolution
+// with the epilogue applied from registers, plus the fixed-order second
+// stage of the pooled mean (shared by every variant).
+//
+// Design (the GB300 form of the smem-tiled direct conv that the
+// Kimi-K2.6__l2_p57 trace sketches: an input halo tile plus the weights in
+// shared memory, one output tile per block):
+//   * block = 256 threads = 8 channel groups (one warp each, 8 output
+//     channels per thread) x 32 pixel groups (one lane each, PR x PC output
+//     pixels per thread), so a warp reads one weight vector by broadcast;
+//   * C_in is consumed in chunks of 8 channels: the chunk's input halo
+//     [8][KD][TH+2][TW+2] and its weights [8][taps][64] are staged in smem;
+//   * eltwise mode (PR=1, PC=4): 32 x 4 output tile; pool mode (PR=PC=2):
+//     each thread owns one 2x2 pooling window of a 16 x 8 tile, so the
+//     window max, hardtanh and the per-tile partial sum need no exchange.
+#include <cuda_runtime.h>
+
+#include "fc_epi.cuh"
+#include "fc_internal.h"
+
+namespace fc {
+
+namespace {
+
+constexpr int kCiT = 8;   // input channels per staged chunk
+constexpr int kCoT = 64;  // output channels per block
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Packed FFMA weights: wp[ci][tap][co] with ci padded to a multiple of 8
+// and co to a multiple of 64 (zeros).  tap = (kd * KH + kh) * KW + kw.
+// Transposed-conv weights W[ci][co][kh][kw] enter as the equivalent conv:
+// wp[ci][kh'][kw'][co] = W[ci][co][KH-1-kh'][KW-1-kw'].
+__global__ void ffma_pack_weights(const float *__restrict__ w, int C, int CO,
+                                  int KD, int KH, int KW, int wlayout,
+                                  int Cp, int COp, float *__restrict__ wp) {
+  int taps = KD * KH * KW;
+  long total = (long)Cp * taps * COp;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
+       i += (long)gridDim.x * blockDim.x) {
+    int co = (int)(i % COp);
+    int tap = (int)((i / COp) % taps);
+    int ci = (int)(i / ((long)COp * taps));
+    float v = 0.0f;
+    if (ci < C && co < CO) {
+      if (wlayout == 0) {
+        v = w[((long)co * C + ci) * taps + tap];
+      } else {
+        int kh = tap / KW, kw = tap % KW;
+        v = w[(((long)ci * CO + co) * KH + (KH - 1 - kh)) * KW + (KW - 1 - kw)];
+      }
+    }
+    wp[i] = v;
+  }
+}
+
+template <int KD, int PR, int PC, bool POOL, int CHAIN>
+__global__ void __launch_bounds__(256)
+ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
+                 float *__restrict__ partial, int n_th, int n_tw) {
+  constexpr int K = 3;
+  constexpr int TAPS = KD * K * K;
+  constexpr int TW = 8 * PC, TH = 4 * PR;
+  constexpr int SW = TW + K - 1, SH = TH + K - 1;
+  extern __shared__ __align__(16) float smem_f[];
+  float (*s_w)[TAPS][kCoT] = reinterpret_cast<float (*)[TAPS][kCoT]>(smem_f);
+  float (*s_in)[KD][SH][SW] =
+      reinterpret_cast<float (*)[KD][SH][SW]>(smem_f + kCiT * TAPS * kCoT);
+
+  const int tid = threadIdx.x;
+  const int cg = tid >> 5;   // channel group (warp)
+  const int pg = tid & 31;   // pixel group (lane)
+  const int gr = pg >> 3, gc = pg & 7;
+
+  long b = blockIdx.x;
+  const int tw = (int)(b % n_tw); b /= n_tw;
+  const int th = (int)(b % n_th); b /= n_th;
+  const int od = (int)(b % p.Do); b /= p.Do;
+  const int n = (int)(b % p.N); b /= p.N;
+  const int cb = (int)b;
+
+  const int oh0 = th * TH, ow0 = tw * TW;
+  const int HW = p.H * p.W;
+  const long x_n = (long)n * p.C * p.D * HW;
+
+  float acc[PR][PC][8];
+#pragma unroll
+  for (int a = 0; a < PR; ++a)
+#pragma unroll
+    for (int c = 0; c < PC; ++c)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[a][c][j] = 0.0f;
+
+  for (int ci0 = 0; ci0 < Cp; ci0 += kCiT) {
+    __syncthreads();
+    // stage the input halo of this channel chunk (zero padded)
+    constexpr int NIN = kCiT * KD * SH * SW;
+    for (int i = tid; i < NIN; i += 256) {
+      int c = i % SW, r = (i / SW) % SH, kd = (i / (SW * SH)) % KD;
+      int ci = i / (SW * SH * KD);
+      int gci = ci0 + ci;
+      int id = od + kd - p.pad_d, ih = oh0 + r - p.pad, iw = ow0 + c - p.pad;
+      float v = 0.0f;
+      if (gci < p.C && id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 &&
+          iw < p.W)
+        v = __ldg(p.x + x_n + ((long)gci * p.D + id) * HW + (long)ih * p.W + iw);
+      s_in[ci][kd][r][c] = v;
+    }
+    // stage the chunk's weights for this block's 64 output channels
+    constexpr int NW4 = kCiT * TAPS * (kCoT / 4);
+    for (int i = tid; i < NW4; i += 256) {
+      int c4 = i % (kCoT / 4), t = (i / (kCoT / 4)) % TAPS, ci = i / (TAPS * (kCoT / 4));
+      const float4 *src = reinterpret_cast<const float4 *>(
+          wp + ((long)(ci0 + ci) * TAPS + t) * COp + cb * kCoT);
+      reinterpret_cast<float4 *>(&s_w[ci][t][0])[c4] = __ldg(src + c4);
+    }
+    __syncthreads();
+
+#pragma unroll 1
+    for (int ci = 0; ci < kCiT; ++ci) {
+#pragma unroll
+      for (int kd = 0; kd < KD; ++kd) {
+#pragma unroll
+        for (int kh = 0; kh < K; ++kh) {
+          float4 wv[K][2];
+#pragma unroll
+          for (int kw = 0; kw < K; ++kw) {
+            const float4 *ws4 =
+                reinterpret_cast<const float4 *>(&s_w[ci][(kd * K + kh) * K + kw][cg * 8]);
+            wv[kw][0] = ws4[0];
+            wv[kw][1] = ws4[1];
+          }
+#pragma unroll
+          for (int a = 0; a < PR; ++a) {
+            float xin[PC + K - 1];
+#pragma unroll
+            for (int q = 0; q < PC + K - 1; ++q)
+              xin[q] = s_in[ci][kd][gr * PR + a + kh][gc * PC + q];
+#pragma unroll
+            for (int kw = 0; kw < K; ++kw)
+#pragma unroll
+              for (int c = 0; c < PC; ++c) {
+                float xv = xin[c + kw];
+                acc[a][c][0] = fmaf(xv, wv[kw][0].x, acc[a][c][0]);
+                acc[a][c][1] = fmaf(xv, wv[kw][0].y, acc[a][c][1]);
+                acc[a][c][2] = fmaf(xv, wv[kw][0].z, acc[a][c][2]);
+                acc[a][c][3] = fmaf(xv, wv[kw][0].w, acc[a][c][3]);
+                acc[a][c][4] = fmaf(xv, wv[kw][1].x, acc[a][c][4]);
+                acc[a][c][5] = fmaf(xv, wv[kw][1].y, acc[a][c][5]);
+                acc[a][c][6] = fmaf(xv, wv[kw][1].z, acc[a][c][6]);
+                acc[a][c][7] = fmaf(xv, wv[kw][1].w, acc[a][c][7]);
+              }
+          }
+        }
+      }
+    }
+  }
+
+  const int co0 = cb * kCoT + cg * 8;
+  if constexpr (!POOL) {
+    const long plane = (long)p.Do * p.Ho * p.Wo;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int co = co0 + j;
+      if (co >= p.CO) break;
+      const float bias = p.epi.bias ? __ldg(p.epi.bias + co) : 0.0f;
+      const float add = chain_addend<CHAIN>(p.epi, co);
+      float *yc = p.y + ((long)n * p.CO + co) * plane + (long)od * p.Ho * p.Wo;
+#pragma unroll
+      for (int a = 0; a < PR; ++a) {
+        const int oh = oh0 + gr * PR + a;
+        if (oh >= p.Ho) continue;
+#pragma unroll
+        for (int c = 0; c < PC; ++c) {
+          const int ow = ow0 + gc * PC + c;
+          if (ow < p.Wo)
+            yc[(long)oh * p.Wo + ow] = apply_chain<CHAIN>(p.epi, co, acc[a][c][j] + bias, add);
+        }
+      }
+    }
+  } else {
+    // one 2x2 window per thread: window (wi, wj) of the pooled plane
+    const int wi = (oh0 >> 1) + gr, wj = (ow0 >> 1) + gc;
+    const bool valid = (wi < p.Ho / 2) && (wj < p.Wo / 2);
+    float part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int co = co0 + j;
+      const float bias = (co < p.CO && p.epi.bias) ? __ldg(p.epi.bias + co) : 0.0f;
+      float m = fmaxf(fmaxf(acc[0][0][j] + bias, acc[0][1][j] + bias),
+                      fmaxf(acc[1][0][j] + bias, acc[1][1][j] + bias));
+      m = fminf(fmaxf(m, p.ht_lo), p.ht_hi);
+      part[j] = valid ? m : 0.0f;
+    }
+    // fixed-order butterfly over the 32 windows of this tile
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
+    if (pg == 0) {
+      const int T = n_th * n_tw;
+      const int t = th * n_tw + tw;
+      float *dst = partial + ((long)n * T + t) * p.CO;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (co0 + j < p.CO) dst[co0 + j] = part[j];
+    }
+  }
+}
+
+// Second stage of the pooled mean: y[n][co] = tanh(sum_t partial[n][t][co] /
+// count), summed in double in index order.
+__global__ void pool_finish_kernel(const float *__restrict__ partial, int N,
+                                   int CO, int T, double inv_count,
+                                   float *__restrict__ y) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N * CO) return;
+  int n = i / CO, co = i % CO;
+  const float *src = partial + (long)n * T * CO + co;
+  double s = 0.0;
+  for (int t = 0; t < T; ++t) s += (double)src[(long)t * CO];
+  y[i] = (float)tanh(s * inv_count);
+}
+
+template <int KD, int PR, int PC, bool POOL, int CHAIN>
+cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
+                       float *partial, cudaStream_t s) {
+  constexpr int TW = 8 * PC, TH = 4 * PR;
+  int n_tw = ceil_div(p.Wo, TW), n_th = ceil_div(p.Ho, TH);
+  long blocks = (long)(COp / kCoT) * p.N * p.Do * n_th * n_tw;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+  constexpr size_t smem = sizeof(float) * (kCiT * KD * 9 * kCoT +
+                                           kCiT * KD * (TH + 2) * (TW + 2));
+  auto kern = ffma_conv_kernel<KD, PR, PC, POOL, CHAIN>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_begin(s);
+  kern<<<(unsigned)blocks, 256, smem, s>>>(p, wp, Cp, COp, partial, n_th, n_tw);
+  prof_end(s, p.entry);
+  return cudaGetLastError();
+}
+
+template <int KD>
+cudaError_t launch_eltwise(const ConvProblem &p, const float *wp, int Cp, int COp,
+                           cudaStream_t s) {
+  switch (p.chain) {
+    case CHAIN_NONE: return launch_one<KD, 1, 4, false, CHAIN_NONE>(p, wp, Cp, COp, nullptr, s);
+    case CHAIN_RELU_HARDSWISH:
+      return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH>(p, wp, Cp, COp, nullptr, s);
+    case CHAIN_LEAKY_ADD_CLAMP_GELU:
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU>(p, wp, Cp, COp, nullptr, s);
+    default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC>(p, wp, Cp, COp, nullptr, s);
+  }
+}
+
+}  // namespace
+
+int ffma_pool_tiles_per_image(const ConvProblem &p) {
+  return ceil_div(p.Ho, 8) * ceil_div(p.Wo, 16);
+}
+
+cudaError_t pool_finish_launch(const ConvProblem &p, const float *partials,
+                               int tiles_per_image, cudaStream_t s) {
+  int total = p.N * p.CO;
+  int count = (p.Ho / 2) * (p.Wo / 2);
+  pool_finish_kernel<<<ceil_div(total, 128), 128, 0, s>>>(
+      partials, p.N, p.CO, tiles_per_image, 1.0 / (double)count, p.y);
+  return cudaGetLastError();
+}
+
+cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
+                        cudaStream_t s, int *launches) {
+  const int Cp = ceil_div(p.C, kCiT) * kCiT;
+  const int COp = ceil_div(p.CO, kCoT) * kCoT;
+  float *wp = reinterpret_cast<float *>(static_cast<char *>(ws) + L.ffma_w);
+  const int taps = p.KD * p.KH * p.KW;
+  long total = (long)Cp * taps * COp;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 1024) blocks = 1024;
+  ffma_pack_weights<<<blocks, 256, 0, s>>>(p.w, p.C, p.CO, p.KD, p.KH, p.KW,
+                                           p.wlayout, Cp, COp, wp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launches = 1;
+  if (p.pool) {
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
+    e = launch_one<1, 2, 2, true, CHAIN_NONE>(p, wp, Cp, COp, partial, s);
+    if (e != cudaSuccess) return e;
+    e = pool_finish_launch(p, partial, ffma_pool_tiles_per_image(p), s);
+    *launches += 2;
+    return e;
+  }
+  e = (p.KD == 1) ? launch_eltwise<1>(p, wp, Cp, COp, s)
+                  : launch_eltwise<3>(p, wp, Cp, COp, s);
+  *launches += 1;
+  return e;
+}
+
+}  // namespace fc

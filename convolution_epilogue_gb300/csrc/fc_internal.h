@@ -1,0 +1,82 @@
+// fc_internal.h -- host/device shared declarations of libfusedconv (not part
+// of the public ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fusedconv.h"
+
+namespace fc {
+
+// Elementwise chains with a specialised fast path; anything else runs the
+// generic op interpreter.
+enum ChainId : int {
+  CHAIN_GENERIC = 0,
+  CHAIN_NONE = 1,             // no op after the bias
+  CHAIN_RELU_HARDSWISH = 2,   // relu -> hardswish
+  CHAIN_LEAKY_ADD_CLAMP_GELU = 3  // leaky(a) -> + chan -> clamp[a,b] -> gelu
+};
+
+// Epilogue as the kernels see it (passed by value).
+struct EpiDev {
+  const float *bias;
+  int n_ops;
+  int kind[FC_MAX_EPI_OPS];
+  float a[FC_MAX_EPI_OPS];
+  float b[FC_MAX_EPI_OPS];
+  const float *chan[FC_MAX_EPI_OPS];
+};
+
+// One conv problem after the host has validated it.  2-D problems have
+// D = Do = KD = 1 and pad_d = 0.  Transposed convs arrive here already
+// rewritten as a conv (swapped + flipped weights, pad k - 1 - p).
+struct ConvProblem {
+  const float *x;
+  const float *w;  // caller layout (see wlayout)
+  float *y;        // eltwise: [N][CO][Do][Ho][Wo]; pool: [N][CO]
+  int N, C, D, H, W;
+  int CO, KD, KH, KW;
+  int pad_d, pad;  // zero padding on D and on H/W
+  int Do, Ho, Wo;
+  int wlayout;     // 0: conv [CO][C][KD][KH][KW]; 1: convT [C][CO][KH][KW]
+  int pool;        // 1: 2x2 maxpool -> hardtanh -> mean -> tanh
+  float ht_lo, ht_hi;
+  int chain;       // ChainId
+  int entry;       // 0 conv2d, 1 conv3d, 2 convT-pool-mean (for profiling)
+  EpiDev epi;
+  unsigned int *status;  // device status word
+};
+
+// Status bits written by kernels.
+enum : unsigned int { ST_TIMEOUT = 1u, ST_RANGE = 2u };
+
+// Workspace regions (byte offsets, all 256-aligned).
+struct WsLayout {
+  size_t ffma_w, ffma_w_bytes;
+  size_t tc_w, tc_w_bytes;
+  size_t partial, partial_bytes;
+  size_t total;
+};
+
+WsLayout ws_layout(const ConvProblem &p);
+
+// Event pair around a main kernel (no-ops unless fc_profile_enable(1)).
+void prof_begin(cudaStream_t s);
+void prof_end(cudaStream_t s, int entry);
+
+// Launchers (each returns cudaSuccess or the launch error) and the number of
+// kernels they launched through *launches.
+cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
+                        cudaStream_t s, int *launches);
+cudaError_t pool_finish_launch(const ConvProblem &p, const float *partials,
+                               int tiles_per_image, cudaStream_t s);
+int ffma_pool_tiles_per_image(const ConvProblem &p);
+
+// Tensor-core path.  prec: 0 = tf32x3, 1 = f16x3.
+bool tc_supported(const ConvProblem &p, int prec);
+cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws,
+                      const WsLayout &L, cudaStream_t s, int *launches);
+int tc_pool_tiles_per_image(const ConvProblem &p);
+size_t tc_weight_bytes(const ConvProblem &p);
+
+}  // namespace fc

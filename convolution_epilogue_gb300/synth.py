@@ -122,17 +122,25 @@ WORKLOADS = {
 }
 
 
-def make_inputs(wid: int, x_shape=None):
+def make_inputs(wid: int, x_shape=None, first_images=None):
     """Seeded inputs of workload `wid` (optionally with another x shape of
     the same kind, for the small edge-case sweeps).  Returns a dict with
-    x, w, b and (conv3d only) s, all fp32 numpy arrays."""
+    x, w, b and (conv3d only) s, all fp32 numpy arrays.  With
+    `first_images=n` only the first n images of x are drawn (the same bytes
+    as the full draw) and W, b, s are the full workload's."""
     spec = WORKLOADS[wid]
     xs = tuple(x_shape) if x_shape is not None else spec["x"]
     st = Stream(wid)
     k = spec["k"]
     cin = xs[1]
     cout = spec["cout"]
-    out = {"x": st.normal(xs)}
+    if first_images is None:
+        out = {"x": st.normal(xs)}
+    else:
+        n = int(np.prod(xs))
+        part = (int(first_images),) + tuple(xs[1:])
+        out = {"x": st.normal(part)}
+        st.pos = 2 * ((n + 1) // 2)
     if spec["kind"] == "conv2d":
         wshape = (cout, cin, k, k)
         fan_in = cin * k * k

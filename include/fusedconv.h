@@ -1,0 +1,193 @@
+/*
+ * fusedconv.h -- C ABI of libfusedconv: dense 2-D / 3-D convolutions and a
+ * stride-1 transposed convolution with their elementwise and reduction
+ * epilogues fused into the same kernel, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (three POPCORNBENCH reasoning traces):
+ *  - fc_conv2d_epi: trace "Kimi-K2.6__l2_p57", problem statement and
+ *    "simplest kernel" paragraph: Conv2d (bias, stride 1, padding 0) ->
+ *    ReLU -> HardSwish x * clamp((x + 3) / 6, 0, 1).
+ *  - fc_conv3d_epi: trace "Kimi-K2.6__l2_p90", problem statement: Conv3d
+ *    (bias) -> LeakyReLU(0.2) -> + sum_tensor[C_out,1,1,1] -> clamp[-1, 1]
+ *    -> GELU 0.5 x (1 + erf(x / sqrt 2)) (exact form, GELU accuracy
+ *    paragraph).
+ *  - fc_convT2d_pool_mean: trace "Kimi-K2.6__l2_p10", problem statement:
+ *    ConvTranspose2d(k 3, stride 1, padding 1) (bias) -> MaxPool2d(2, 2) ->
+ *    Hardtanh[-1, 1] -> mean over (H, W) keepdim -> tanh.  Computed as a
+ *    plain convolution with swapped channel axes, both taps flipped and
+ *    padding k - 1 - p (the trace's transposed-conv equivalence paragraph).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers to contiguous fp32 arrays in
+ *    PyTorch's default layouts: x NCHW / NCDHW; conv weights
+ *    [C_out][C_in][kD][kH][kW]; transposed-conv weights [C_in][C_out][k][k];
+ *    bias [C_out]; per-channel tensors of epilogue ops [C_out].  The caller
+ *    owns every buffer; the library allocates nothing.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they enqueue kernels and return.
+ *  - `ws` is a caller-owned device workspace of at least
+ *    fc_workspace_bytes(...) bytes, 256-byte aligned, that must not be used
+ *    by another call in flight on another stream.  It holds the packed
+ *    weights and (for the pooled entry point) the per-tile partial sums.
+ *  - Invalid shapes, NULL or misaligned pointers, unsupported parameters or
+ *    epilogue chains and a too-small workspace are rejected on the host
+ *    before anything is launched, and the call returns a non-zero
+ *    fc_status.  No exception ever crosses this boundary.  There is no CPU
+ *    fallback: without a usable sm_103a device the calls return
+ *    FC_ERR_CUDA.
+ *  - Kernel-side failures (a bounded wait that ran out, an input value
+ *    outside the range of the fp16-split variant) are recorded in a
+ *    per-device status word that fc_get_last_device_error() reads.
+ */
+#ifndef FUSEDCONV_H
+#define FUSEDCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FC_API __attribute__((visibility("default")))
+#else
+#define FC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FC_OK = 0,
+  FC_ERR_INVALID_ARG = 1, /* bad shape, NULL pointer, bad op parameter */
+  FC_ERR_UNSUPPORTED = 2, /* valid but not implemented (stride, pad, chain) */
+  FC_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  FC_ERR_WORKSPACE = 4,   /* ws is NULL/misaligned or ws_bytes too small */
+  FC_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  FC_ERR_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device) */
+  FC_ERR_RANGE = 7        /* |x| or |w| beyond the fp16-split range (device) */
+} fc_status;
+
+/* Epilogue ops, applied in order to the conv output (bias already added). */
+typedef enum {
+  FC_EPI_RELU = 1,        /* max(x, 0) */
+  FC_EPI_HARDSWISH = 2,   /* x * clamp((x + 3) / 6, 0, 1) */
+  FC_EPI_LEAKY_RELU = 3,  /* x > 0 ? x : a * x */
+  FC_EPI_ADD_CHANNEL = 4, /* x + chan[c_out] (device pointer, C_out floats) */
+  FC_EPI_CLAMP = 5,       /* min(max(x, a), b) */
+  FC_EPI_GELU_ERF = 6,    /* 0.5 x (1 + erf(x / sqrt 2)) */
+  FC_EPI_MAXPOOL2X2 = 7,  /* 2x2 window, stride 2, floor extent */
+  FC_EPI_HARDTANH = 8,    /* min(max(x, a), b) */
+  FC_EPI_MEAN_HW = 9,     /* mean over the (pooled) H x W plane */
+  FC_EPI_TANH = 10        /* tanh(x) */
+} fc_epi_kind;
+
+typedef struct {
+  int kind;          /* fc_epi_kind */
+  float a, b;        /* parameters, see fc_epi_kind */
+  const float *chan; /* FC_EPI_ADD_CHANNEL only: device pointer [C_out] */
+} fc_epi_op;
+
+#define FC_MAX_EPI_OPS 8
+
+typedef struct {
+  const float *bias; /* device pointer [C_out] or NULL (no bias) */
+  int n_ops;         /* 0 .. FC_MAX_EPI_OPS */
+  fc_epi_op ops[FC_MAX_EPI_OPS];
+} fc_epilogue;
+
+/* How the contraction is computed.  AUTO picks per shape from a table of
+ * measured times.  FFMA: fp32 CUDA-core register-blocked direct conv.
+ * TC_TF32X3: tcgen05 tensor cores, each fp32 operand split into a tf32
+ * high part and a tf32 remainder, three products (hi*hi + hi*lo + lo*hi)
+ * accumulated in fp32 in tensor memory.  TC_F16X3: the same split with fp16
+ * parts (the remainder scaled by 2^11): same accuracy as TC_TF32X3 for
+ * |x|, |w| < 65504, twice the tensor rate; values outside that range set
+ * FC_ERR_RANGE in the device status word. */
+typedef enum {
+  FC_VARIANT_AUTO = 0,
+  FC_VARIANT_FFMA = 1,
+  FC_VARIANT_TC_TF32X3 = 2,
+  FC_VARIANT_TC_F16X3 = 3
+} fc_variant;
+
+/* Conv2d + bias + elementwise epilogue chain (any sequence of RELU,
+ * HARDSWISH, LEAKY_RELU, ADD_CHANNEL, CLAMP, GELU_ERF, HARDTANH, TANH).
+ * x [N][C_in][H][W]; w [C_out][C_in][kH][kW]; y [N][C_out][Ho][Wo] with
+ * Ho = H + 2 pad - kH + 1, Wo = W + 2 pad - kW + 1.
+ * Supported: stride 1, kH = kW = 3, 0 <= pad <= 2, 1 <= C_in, 1 <= C_out,
+ * Ho, Wo >= 1, and every tensor below 2^31 elements.  N = 0 is a valid
+ * empty call (nothing is launched). */
+FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
+                        const float *w, int C_out, int kH, int kW, int stride,
+                        int pad, const fc_epilogue *epi, float *y, void *ws,
+                        size_t ws_bytes, void *stream);
+
+/* Conv3d + bias + elementwise epilogue chain; same ops as fc_conv2d_epi.
+ * x [N][C_in][D][H][W]; w [C_out][C_in][kD][kH][kW];
+ * y [N][C_out][Do][Ho][Wo], each extent in + 2 pad - k + 1.
+ * Supported: stride 1, kD = kH = kW = 3, 0 <= pad <= 2. */
+FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
+                        const float *w, int C_out, int kD, int kH, int kW,
+                        int stride, int pad, const fc_epilogue *epi, float *y,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/* ConvTranspose2d + bias -> MaxPool2d(2,2) -> Hardtanh[a,b] -> mean(H,W)
+ * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];
+ * y [N][C_out][1][1].  The epilogue chain must be exactly
+ * MAXPOOL2X2, HARDTANH(a, b), MEAN_HW, TANH.  Supported: stride 1,
+ * k = 3, pad 1, out_pad 0 (conv output extent Ho = H, Wo = W; H, W >= 2).
+ * The mean is reduced in a fixed order (per-tile partials, then a second
+ * kernel sums them in index order), so results are bitwise reproducible. */
+FC_API fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
+                               const float *w, int C_out, int k, int stride,
+                               int pad, int out_pad, const fc_epilogue *epi,
+                               float *y, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/* Workspace bytes needed by one call.  entry: 0 = fc_conv2d_epi,
+ * 1 = fc_conv3d_epi, 2 = fc_convT2d_pool_mean.  dims:
+ *   entry 0: {N, C_in, H, W, C_out, k, pad}
+ *   entry 1: {N, C_in, D, H, W, C_out, k, pad}
+ *   entry 2: {N, C_in, H, W, C_out, k, pad}
+ * The size covers every variant, so it does not depend on the selection.
+ * Returns 0 for an invalid entry or NULL dims. */
+FC_API size_t fc_workspace_bytes(int entry, const int *dims);
+
+/* Process-wide variant override (FC_VARIANT_AUTO restores the automatic
+ * choice).  Returns FC_ERR_INVALID_ARG for an unknown value.  Not
+ * synchronised with calls running on other host threads. */
+FC_API fc_status fc_set_variant(int variant);
+
+/* The variant the calling thread's last successful entry-point call used. */
+FC_API int fc_last_variant(void);
+
+/* Number of kernels the calling thread's last successful entry-point call
+ * launched. */
+FC_API int fc_last_launch_count(void);
+
+/* Human-readable name of a status code (static string). */
+FC_API const char *fc_status_string(fc_status s);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns FC_OK, FC_ERR_TIMEOUT, FC_ERR_RANGE or FC_ERR_CUDA. */
+FC_API fc_status fc_get_last_device_error(void *stream);
+
+/* Kernel timing for benchmarks.  While enabled, every entry-point call
+ * records a pair of CUDA events on its stream around its main (contraction
+ * + epilogue) kernel; pack and finishing kernels are outside the pair.
+ * fc_profile_read synchronises on the recorded events and returns, for one
+ * entry (0 conv2d, 1 conv3d, 2 convT-pool-mean), the summed milliseconds and
+ * the number of timed launches since the last fc_profile_reset.  At most
+ * 4096 pairs are kept; later launches are not timed.  Host-thread safe only
+ * when one thread uses it at a time. */
+FC_API fc_status fc_profile_enable(int on);
+FC_API fc_status fc_profile_read(int entry, double *total_ms, int *launches);
+FC_API void fc_profile_reset(void);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+FC_API int fc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEDCONV_H */

@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/fusedconv.h declares, and rejects bad arguments on the host
+before it touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import convolution_epilogue_gb300 as fc
+from convolution_epilogue_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "fusedconv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fc.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"FC_API\s+[\w\s\*]+?\b(fc_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("fc_conv2d_epi", "fc_conv3d_epi", "fc_convT2d_pool_mean"):
+        assert n in names
+    assert sorted(fc.EXPORTS) == names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in fc.STATUS_NAMES.items():
+        assert L.fc_status_string(code).decode().startswith(name)
+    assert L.fc_version() >= 100
+
+
+def test_workspace_sizes(L):
+    w0 = fc.workspace_bytes(0, (128, 8, 128, 128, 64, 3, 0))
+    w1 = fc.workspace_bytes(1, (128, 8, 16, 64, 64, 64, 3, 0))
+    w2 = fc.workspace_bytes(2, (128, 64, 256, 256, 64, 3, 1))
+    assert w0 >= 8 * 9 * 64 * 4 and w0 % 256 == 0
+    assert w1 >= 8 * 27 * 64 * 4 and w1 % 256 == 0
+    # w2 holds the packed weights and one fp32 partial per (n, tile, c_out)
+    assert w2 >= 64 * 9 * 64 * 4 + 128 * 64 * 4
+    assert fc.workspace_bytes(7, (1, 1, 1, 1, 1, 3, 0)) == 0
+
+
+def _epi(ops=()):
+    e, keep = fc.make_epilogue(None, ops)
+    return e, keep
+
+
+def _conv2d(L, N=1, C=8, H=8, W=8, CO=64, k=3, stride=1, pad=0, x=16, w=16,
+            y=16, ops=(), ws=256, ws_bytes=1 << 20):
+    e, _ = _epi(ops)
+    return L.fc_conv2d_epi(ctypes.c_void_p(x), N, C, H, W, ctypes.c_void_p(w), CO,
+                           k, k, stride, pad, ctypes.byref(e), ctypes.c_void_p(y),
+                           ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_host_validation_rejects_before_launch(L):
+    INVALID, UNSUP, ALIGN = 1, 2, 3
+    assert _conv2d(L, N=-1) == INVALID
+    assert _conv2d(L, C=0) == INVALID
+    assert _conv2d(L, stride=0) == INVALID
+    assert _conv2d(L, stride=2) == UNSUP
+    assert _conv2d(L, k=5) == UNSUP
+    assert _conv2d(L, pad=3) == UNSUP
+    assert _conv2d(L, H=2) == INVALID  # Ho = 0
+    assert _conv2d(L, x=0) == INVALID  # NULL x
+    assert _conv2d(L, x=18) == ALIGN
+    assert _conv2d(L, ops=(("maxpool2x2",),)) == UNSUP
+    assert _conv2d(L, ops=(("clamp", 1.0, -1.0),)) == INVALID
+    assert _conv2d(L, N=0) == 0  # empty batch: nothing to launch
+
+
+def test_pool_entry_requires_exact_chain(L):
+    e, _ = _epi((("maxpool2x2",), ("hardtanh", -1, 1), ("tanh",)))
+    st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
+                                4, 3, 1, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
+                                ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 2
+    e, _ = _epi(fc.pool_mean_ops())
+    st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
+                                4, 3, 2, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
+                                ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 2  # stride 2 is not supported
+
+
+def test_no_cpu_fallback_without_gpu(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # a fully valid call cannot run anywhere but the GPU
+    assert _conv2d(L) == 5  # FC_ERR_CUDA
+
+
+def test_set_variant(L):
+    assert L.fc_set_variant(9) == 1
+    for v in range(4):
+        assert L.fc_set_variant(v) == 0
+    assert L.fc_set_variant(0) == 0
