@@ -1,12 +1,731 @@
-// fc_tc.cu -- tcgen05 tensor-core path (placeholder until the kernel lands).
+// fc_tc.cu -- tcgen05 tensor-core path: implicit-GEMM convolution with the
+// epilogue fused, persistent and warp-specialised, for sm_103a.
+//
+// GEMM view (the implicit-GEMM reading of the Kimi-K2.6__l2_p57 and
+// Kimi-K2.6__l2_p90 traces, GEMM-shape paragraphs):
+//   M = output pixels (128 per MMA, one TMEM lane each), N = output channels
+//   (64), K = C_in x taps.
+// fp32 accuracy from 11-bit-significand tensor formats: every operand v is
+// split into v_hi (rounded to the tensor format) and a remainder v_lo; the
+// sum x_hi w_hi + x_hi w_lo + x_lo w_hi is exact up to the x_lo w_lo term
+// (~2^-22 relative).  The B operand is stored as [W_hi | W_lo] (N = 128), so
+// the three products take two MMAs per K step:
+//   D[:, 0:128]  += A_hi * [W_hi | W_lo]     (N = 128)
+//   D[:, 64:128] += A_lo * W_hi              (N = 64)
+//   y = D[:, c] + scale * D[:, 64 + c]
+// tf32 mode (kind::tf32): scale 1.  f16 mode (kind::f16, twice the rate):
+// the remainders are stored multiplied by 2^11 so they stay normal in fp16,
+// and scale = 2^-11; |x|, |w| must stay within 65504 (checked, status bit).
+//
+// Operand layout (no swizzle, K-major): a "slice" is 16 bytes per row (4
+// tf32 or 8 fp16 values of consecutive input channels).  Staged input
+// pixels sit 16 bytes apart in each slice plane, in the same raster order
+// (rows RS pixels apart) as the M tile's output pixels, so the A operand of
+// tap (kd, kh, kw) is the stage shifted by ((kd*RIN + kh)*RS + kw) pixels:
+// a different descriptor start address, no data movement per tap.  This is
+// the GB300 form of the traces' shared-memory halo tile.
+//
+// Roles (416 threads): warps 0-3 epilogue (TMEM lanes 32w..32w+31), warp 4
+// TMEM allocation + MMA issue (the warp runs converged; one fixed leader
+// lane issues each burst of MMAs), warps 5-12 producers (global loads of
+// the input halo, hi/lo split, st.shared into the stage ring; one producer
+// lane also streams packed weights with bulk copies).  All waits are
+// bounded (4 s on %globaltimer) and warp-uniform; a timeout sets a status
+// bit, every role drains, and the CTA frees its tensor memory and exits.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "fc_epi.cuh"
 #include "fc_internal.h"
+#include "fc_tc_ptx.cuh"
 
 namespace fc {
-bool tc_supported(const ConvProblem &, int) { return false; }
-cudaError_t tc_launch(const ConvProblem &, int, void *, const WsLayout &,
-                      cudaStream_t, int *) {
-  return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int kThreads = 416;
+constexpr int kEpiWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kProdWarp0 = 5;
+constexpr int kProdThreads = 256;
+constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
+constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
+constexpr uint64_t kWaitNs = 4000000000ull;
+
+struct TcPlan {
+  int ok;
+  int prec;       // 0 tf32, 1 f16
+  int E;          // values per 16-byte slice
+  int chunk_ci;   // input channels per stage
+  int P;          // slice planes per stage
+  int NCH;        // stages per unit (chunks of C_in)
+  int KS;         // K steps per chunk
+  int TAPS;
+  int pairtaps;   // f16 with one plane per chunk: a K step spans two taps
+  int U, R, RS, WT, RIN;
+  int NPIX;
+  int plane_bytes;
+  int a_stage_bytes;
+  int S;
+  int COB;
+  int b_chunk_bytes;
+  int b_resident;
+  int SB;
+  int NACC;
+  int tmem_cols;
+  int n_rt, n_ct;
+  long units;
+  int smem_bytes;
+  int off_b, off_bar, off_misc;
+};
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+TcPlan make_plan(const ConvProblem &p, int prec) {
+  TcPlan q{};
+  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
+  if (p.pool && p.KD != 1) return q;
+  q.prec = prec;
+  q.E = prec ? 8 : 4;
+  const int Cp8 = cdiv(p.C, 8) * 8;
+  q.chunk_ci = (prec && Cp8 > 8) ? 16 : 8;
+  const int Cp = cdiv(p.C, q.chunk_ci) * q.chunk_ci;
+  q.P = q.chunk_ci / q.E;
+  q.NCH = Cp / q.chunk_ci;
+  q.TAPS = p.KD * 9;
+  q.pairtaps = (q.P == 1);
+  q.KS = q.pairtaps ? cdiv(q.TAPS, 2) : q.TAPS;
+  q.U = p.pool ? 2 : 1;
+  const bool rowpack = (p.Wo + 2 <= 128);
+  if (rowpack) {
+    q.RS = p.Wo + 2;
+    q.WT = p.Wo;
+    q.n_ct = 1;
+    q.R = p.pool ? 1 : 128 / q.RS;
+  } else {
+    q.RS = 130;
+    q.WT = 128;
+    q.n_ct = cdiv(p.Wo, 128);
+    q.R = 1;
+  }
+  q.RIN = q.U * q.R + 2;
+  // last staged pixel any MMA can touch (+1 for the paired-tap slice)
+  const int maxread = ((p.KD - 1) * q.RIN + 2) * q.RS + 2 + (q.U - 1) * q.R * q.RS + 127 + 1;
+  int npix = maxread + 1;
+  if (npix < p.KD * q.RIN * q.RS) npix = p.KD * q.RIN * q.RS;
+  q.NPIX = cdiv(npix, 8) * 8;
+  q.plane_bytes = q.NPIX * 16;
+  q.a_stage_bytes = 2 * q.P * q.plane_bytes;
+  q.COB = cdiv(p.CO, 64);
+  q.b_chunk_bytes = q.KS * kBStep;
+  q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.R);
+  q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
+  q.NACC = p.pool ? 2 : 4;
+  q.tmem_cols = q.NACC * q.U * 128;
+  if (q.tmem_cols > 512) return q;
+  // shared memory: A stages + B (resident or a ring) + barriers/misc
+  const int misc = 2048;
+  const long b_all = (long)q.COB * q.NCH * q.b_chunk_bytes;
+  int S = 0, resident = 0, SB = 0;
+  for (int s = 4; s >= 2 && !S; --s)
+    if ((long)s * q.a_stage_bytes + b_all + misc <= kMaxSmem) { S = s; resident = 1; }
+  if (!S)
+    for (int s = 4; s >= 1 && !S; --s)
+      if ((long)s * q.a_stage_bytes + 2L * q.b_chunk_bytes + misc <= kMaxSmem) { S = s; SB = 2; }
+  if (!S)
+    for (int s = 2; s >= 1 && !S; --s)
+      if ((long)s * q.a_stage_bytes + 1L * q.b_chunk_bytes + misc <= kMaxSmem) { S = s; SB = 1; }
+  if (!S) return q;
+  q.S = S;
+  q.b_resident = resident;
+  q.SB = resident ? 1 : SB;
+  q.off_b = S * q.a_stage_bytes;
+  q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
+  q.off_misc = q.off_bar + 512;
+  q.smem_bytes = q.off_misc + misc - 512;
+  if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
+  q.ok = 1;
+  return q;
 }
-int tc_pool_tiles_per_image(const ConvProblem &) { return 0; }
-size_t tc_weight_bytes(const ConvProblem &) { return 0; }
+
+// --------------------------------------------------------------- device
+struct SmemCtl {
+  uint32_t tmem_base;
+  int abort;
+  int shift[27];     // staged-pixel offset of each tap
+  float red[4][64];  // pool: per-warp partial sums
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         unsigned int *status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 127u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitNs) {
+        atomicOr(status, ST_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so a
+// warp never splits around .sync.aligned instructions or named barriers.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort, unsigned int *status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// AND of a predicate over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+struct UnitPos {
+  int cb, n, od, rt, ct;
+};
+
+__device__ __forceinline__ UnitPos decode_unit(long u, const TcPlan &q, const ConvProblem &p) {
+  UnitPos r;
+  r.ct = (int)(u % q.n_ct); u /= q.n_ct;
+  r.rt = (int)(u % q.n_rt); u /= q.n_rt;
+  r.od = (int)(u % p.Do); u /= p.Do;
+  r.n = (int)(u % p.N); u /= p.N;
+  r.cb = (int)u;
+  return r;
+}
+
+__device__ __forceinline__ uint32_t tf32_rna(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ bool f16_out_of_range(float v) {
+  return !(fabsf(v) <= 65504.0f) && v == v;  // NaN propagates, not flagged
+}
+
+// Packs the B image: for each (channel block, chunk, K step) a 4 KB block
+// of 2 slices x 128 rows x 16 bytes; rows 0-63 hold W_hi of the block's
+// output channels, rows 64-127 W_lo (zero rows past C_out).
+__global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ out) {
+  const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nelem;
+       i += (long)gridDim.x * blockDim.x) {
+    const int e = (int)(i % q.E);
+    long t = i / q.E;
+    const int row = (int)(t % 128); t /= 128;
+    const int k = (int)(t % 2); t /= 2;
+    const int ks = (int)(t % q.KS); t /= q.KS;
+    const int c = (int)(t % q.NCH);
+    const int cb = (int)(t / q.NCH);
+    int tap, ci;
+    if (q.pairtaps) {
+      tap = 2 * ks + k;
+      ci = c * q.chunk_ci + e;
+    } else {
+      tap = ks;
+      ci = c * q.chunk_ci + k * q.E + e;
+    }
+    const int co = cb * 64 + (row & 63);
+    float w = 0.0f;
+    if (tap < q.TAPS && ci < p.C && co < p.CO) {
+      if (p.wlayout == 0) {
+        w = p.w[((long)co * p.C + ci) * q.TAPS + tap];
+      } else {  // transposed conv: swap channel axes, flip both taps
+        const int kh = tap / 3, kw = tap % 3;
+        w = p.w[(((long)ci * p.CO + co) * 3 + (2 - kh)) * 3 + (2 - kw)];
+      }
+    }
+    const bool lo = row >= 64;
+    const long base = ((((long)cb * q.NCH + c) * q.KS + ks) * kBStep) + k * 2048 + row * 16;
+    if (q.prec == 0) {
+      const uint32_t hi = tf32_rna(w);
+      const uint32_t v = lo ? tf32_rna(w - __uint_as_float(hi)) : hi;
+      reinterpret_cast<uint32_t *>(out + base)[e] = v;
+    } else {
+      if (f16_out_of_range(w)) atomicOr(p.status, ST_RANGE);
+      const __half hi = __float2half_rn(w);
+      const __half v = lo ? __float2half_rn((w - __half2float(hi)) * 2048.0f) : hi;
+      reinterpret_cast<__half *>(out + base)[e] = v;
+    }
+  }
+}
+
+template <int PREC, int E>
+__device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, const float (&v)[E],
+                                            bool &range_bad) {
+  if constexpr (PREC == 0) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      h[e] = tf32_rna(v[e]);
+      l[e] = tf32_rna(v[e] - __uint_as_float(h[e]));
+    }
+    *reinterpret_cast<uint4 *>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
+  } else {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = v[2 * e], b = v[2 * e + 1];
+      range_bad |= f16_out_of_range(a) || f16_out_of_range(b);
+      const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+      const __half la = __float2half_rn((a - __half2float(ha)) * 2048.0f);
+      const __half lb = __float2half_rn((b - __half2float(hb)) * 2048.0f);
+      h[e] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+      l[e] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+    }
+    *reinterpret_cast<uint4 *>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+template <int PREC, int CHAIN, bool POOL>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
+               float *__restrict__ partial) {
+  constexpr int E = PREC ? 8 : 4;
+  constexpr int U = POOL ? 2 : 1;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + q.off_bar);
+  uint64_t *a_full = bars;
+  uint64_t *a_empty = bars + 4;
+  uint64_t *b_full = bars + 8;
+  uint64_t *b_empty = bars + 10;
+  uint64_t *acc_full = bars + 12;
+  uint64_t *acc_empty = bars + 16;
+  uint64_t *drain = bars + 20;
+  SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + q.off_misc);
+  volatile int *abort_flag = &ctl->abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < q.S; ++s) {
+      ptx::mbar_init(&a_full[s], kProdThreads / 32);
+      ptx::mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&b_full[s], 1);
+      ptx::mbar_init(&b_empty[s], 1);
+    }
+    for (int a = 0; a < 4; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    ptx::mbar_init(drain, 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (tid < q.TAPS) {
+    const int kd = tid / 9, kh = (tid / 3) % 3, kw = tid % 3;
+    ctl->shift[tid] = (kd * q.RIN + kh) * q.RS + kw;
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(&ctl->tmem_base, (uint32_t)q.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  const long units = q.units;
+  const int HW = p.H * p.W;
+
+  if (warp >= kProdWarp0) {
+    // ------------------------------------------------------------ producers
+    const int pt = tid - kProdWarp0 * 32;
+    bool range_bad = false;
+    uint32_t g = 0, gb = 0;
+    bool ok = true;
+    if (q.b_resident && pt == 0) {
+      const long total = (long)q.COB * q.NCH * q.b_chunk_bytes;
+      ptx::mbar_arrive_expect_tx(&b_full[0], (uint32_t)total);
+      for (long off = 0; off < total; off += 16384) {
+        const uint32_t nb = (uint32_t)((total - off) < 16384 ? (total - off) : 16384);
+        ptx::bulk_g2s(smem + q.off_b + off, bimg + off, nb, &b_full[0]);
+      }
+    }
+    const int items = q.P * q.NPIX;
+    const int rinrs = q.RIN * q.RS;
+    const long cstride = (long)p.D * HW;
+    for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const UnitPos up = decode_unit(u, q, p);
+      const int oh0 = up.rt * U * q.R;  // first output row of the unit
+      const int ow0 = up.ct * q.WT;
+      const long xn = (long)up.n * p.C * p.D * HW;
+      for (int c = 0; c < q.NCH; ++c, ++g) {
+        const int s = (int)(g % q.S);
+        if (!wait_bar_warp(&a_empty[s], ((g / q.S) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (!q.b_resident && warp == kProdWarp0) {
+          const int sb = (int)(gb % q.SB);
+          if (!wait_bar_warp(&b_empty[sb], ((gb / q.SB) & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&b_full[sb], (uint32_t)q.b_chunk_bytes);
+            const uint8_t *src = bimg + ((long)up.cb * q.NCH + c) * q.b_chunk_bytes;
+            uint8_t *dst = smem + q.off_b + (long)sb * q.b_chunk_bytes;
+            for (int off = 0; off < q.b_chunk_bytes; off += 16384) {
+              const int nb = (q.b_chunk_bytes - off) < 16384 ? (q.b_chunk_bytes - off) : 16384;
+              ptx::bulk_g2s(dst + off, src + off, (uint32_t)nb, &b_full[sb]);
+            }
+          }
+          ++gb;
+        }
+        uint8_t *stage = smem + (long)s * q.a_stage_bytes;
+        uint8_t *stage_lo = stage + q.P * q.plane_bytes;
+        const int ci0 = c * q.chunk_ci;
+        for (int it0 = pt; it0 < items; it0 += 4 * kProdThreads) {
+          float v[4][E];
+          int dst_off[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * kProdThreads;
+            dst_off[k] = -1;
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[k][e] = 0.0f;
+            if (it < items) {
+              const int plane = it / q.NPIX;
+              const int pix = it - plane * q.NPIX;
+              dst_off[k] = plane * q.plane_bytes + pix * 16;
+              const int kdp = pix / rinrs;
+              const int rem = pix - kdp * rinrs;
+              const int r = rem / q.RS;
+              const int cc = rem - r * q.RS;
+              const int id = up.od + kdp - p.pad_d;
+              const int ih = oh0 + r - p.pad;
+              const int iw = ow0 + cc - p.pad;
+              if (kdp < p.KD && id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 &&
+                  iw < p.W) {
+                const long base = xn + (long)id * HW + (long)ih * p.W + iw;
+                const int cbase = ci0 + plane * E;
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                  if (cbase + e < p.C) v[k][e] = __ldg(p.x + base + (long)(cbase + e) * cstride);
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (dst_off[k] >= 0)
+              store_slice<PREC, E>(stage + dst_off[k], stage_lo + dst_off[k], v[k], range_bad);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&a_full[s]);
+      }
+    }
+    if (range_bad) atomicOr(p.status, ST_RANGE);
+    // drain outstanding weight copies before the CTA can exit
+    if (pt == 0) {
+      if (q.b_resident) {
+        wait_bar(&b_full[0], 0, abort_flag, p.status);
+      } else if (gb > 0) {
+        for (uint32_t k = (gb > (uint32_t)q.SB ? gb - q.SB : 0); k < gb; ++k)
+          wait_bar(&b_full[k % q.SB], (k / q.SB) & 1, abort_flag, p.status);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issue
+    // The warp stays converged; one leader lane (fixed for the whole kernel,
+    // so every commit tracks every MMA) issues each short burst.
+    const bool leader = ptx::elect_one();
+    constexpr uint32_t fmt = PREC ? 0u : 2u;
+    constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+    constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    uint32_t g = 0, gb = 0, it = 0;
+    bool ok = true;
+    if (q.b_resident) ok = wait_bar_warp(&b_full[0], 0, abort_flag, p.status);
+    for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
+      const int cb = (int)(u / ((long)p.N * p.Do * q.n_rt * q.n_ct));
+      const int acc = (int)(it % q.NACC);
+      if (!wait_bar_warp(&acc_empty[acc], ((it / q.NACC) & 1) ^ 1, abort_flag, p.status)) break;
+      ptx::tc_fence_after();
+      for (int c = 0; c < q.NCH; ++c, ++g) {
+        const int s = (int)(g % q.S);
+        if (!wait_bar_warp(&a_full[s], (g / q.S) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        uint32_t bbase;
+        int sb = 0;
+        if (q.b_resident) {
+          bbase = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
+        } else {
+          sb = (int)(gb % q.SB);
+          if (!wait_bar_warp(&b_full[sb], (gb / q.SB) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          bbase = sbase + q.off_b + (uint32_t)(sb * q.b_chunk_bytes);
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_hi = sbase + (uint32_t)(s * q.a_stage_bytes);
+        const uint32_t a_lo = a_hi + (uint32_t)(q.P * q.plane_bytes);
+        const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
+        for (int ks = 0; ks < q.KS; ++ks) {
+          uint32_t off0, lbo;
+          if (q.pairtaps) {
+            const int t0 = 2 * ks;
+            off0 = (uint32_t)ctl->shift[t0] * 16u;
+            lbo = (t0 + 1 < q.TAPS) ? (uint32_t)(ctl->shift[t0 + 1] - ctl->shift[t0]) * 16u : 16u;
+          } else {
+            off0 = (uint32_t)ctl->shift[ks] * 16u;
+            lbo = (uint32_t)q.plane_bytes;
+          }
+          const uint64_t bdesc = ptx::smem_desc(bbase + (uint32_t)ks * kBStep, 2048, 128);
+          const uint32_t accum = (c | ks) != 0;
+          uint64_t ah[U], al[U];
+#pragma unroll
+          for (int t = 0; t < U; ++t) {
+            const uint32_t moff = (uint32_t)(t * q.R * q.RS * 16);
+            ah[t] = ptx::smem_desc(a_hi + off0 + moff, lbo, 128);
+            al[t] = ptx::smem_desc(a_lo + off0 + moff, lbo, 128);
+          }
+          if (leader) {
+#pragma unroll
+            for (int t = 0; t < U; ++t) {
+              const uint32_t d = dacc + (uint32_t)(t * 128);
+              if constexpr (PREC == 0) {
+                ptx::mma_tf32(d, ah[t], bdesc, idesc1, accum);
+                ptx::mma_tf32(d + 64, al[t], bdesc, idesc2, 1u);
+              } else {
+                ptx::mma_f16(d, ah[t], bdesc, idesc1, accum);
+                ptx::mma_f16(d + 64, al[t], bdesc, idesc2, 1u);
+              }
+            }
+          }
+          __syncwarp();
+        }
+        if (leader) {
+          ptx::tc_commit(&a_empty[s]);
+          if (!q.b_resident) ptx::tc_commit(&b_empty[sb]);
+        }
+        __syncwarp();
+        if (!q.b_resident) ++gb;
+      }
+      if (!ok) break;
+      if (leader) ptx::tc_commit(&acc_full[acc]);
+      __syncwarp();
+    }
+    // wait until every MMA this warp issued has completed
+    if (leader) ptx::tc_commit(drain);
+    __syncwarp();
+    wait_bar_warp(drain, 0, abort_flag, p.status);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int m = warp * 32 + lane;  // TMEM lane = M row = output pixel
+    const float scale = PREC ? (1.0f / 2048.0f) : 1.0f;
+    uint32_t it = 0;
+    for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+      const UnitPos up = decode_unit(u, q, p);
+      const int acc = (int)(it % q.NACC);
+      bool okw = wait_bar_warp(&acc_full[acc], (it / q.NACC) & 1, abort_flag, p.status);
+      if constexpr (POOL) okw = epi_all(okw);
+      if (!okw) break;
+      ptx::tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+      const int co_base = up.cb * 64;
+      if constexpr (!POOL) {
+        const int r = m / q.RS, c = m - r * q.RS;
+        const int oh = up.rt * q.R + r, ow = up.ct * q.WT + c;
+        const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
+        const long plane = (long)p.Ho * p.Wo;
+        const long cstride = (long)p.Do * plane;
+        float *ybase = p.y + ((long)up.n * p.CO * p.Do + up.od) * plane;
+        const long yoff = (long)oh * p.Wo + ow;
+        const uint32_t col0 = (uint32_t)(acc * 128);
+#pragma unroll 1
+        for (int cc = 0; cc < 64; cc += 16) {
+          uint32_t hi[16], lo[16];
+          ptx::tmem_ld16(tl + col0 + cc, hi);
+          ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
+          ptx::tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int co = co_base + cc + j;
+              if (co < p.CO) {
+                const float bias = p.epi.bias ? __ldg(p.epi.bias + co) : 0.0f;
+                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bias;
+                v = apply_chain<CHAIN>(p.epi, co, v, chain_addend<CHAIN>(p.epi, co));
+                ybase[(long)co * cstride + yoff] = v;
+              }
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+      } else {
+        const int c = m;  // one output row per M tile
+        const int ow = up.ct * q.WT + c;
+        const bool valid = ((c & 1) == 0) && (c + 1 < q.WT) && (ow + 1 < p.Wo);
+        const uint32_t col0 = (uint32_t)(acc * 256);
+#pragma unroll 1
+        for (int cc = 0; cc < 64; cc += 16) {
+          uint32_t h0[16], l0[16], h1[16], l1[16];
+          ptx::tmem_ld16(tl + col0 + cc, h0);
+          ptx::tmem_ld16(tl + col0 + 64 + cc, l0);
+          ptx::tmem_ld16(tl + col0 + 128 + cc, h1);
+          ptx::tmem_ld16(tl + col0 + 192 + cc, l1);
+          ptx::tmem_wait_ld();
+          float part[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int co = co_base + cc + j;
+            const float bias = (co < p.CO && p.epi.bias) ? __ldg(p.epi.bias + co) : 0.0f;
+            const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
+            const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
+            float mx = fmaxf(v0, v1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fminf(fmaxf(mx, p.ht_lo), p.ht_hi);
+            part[j] = valid ? mx : 0.0f;
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
+          if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ctl->red[warp][cc + j] = part[j];
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+        epi_sync();
+        if (warp == 0) {
+          const int T = q.n_rt * q.n_ct;
+          const int t = up.rt * q.n_ct + up.ct;
+          float *dst = partial + ((long)up.n * T + t) * p.CO;
+          for (int j = lane; j < 64; j += 32) {
+            const int co = co_base + j;
+            if (co < p.CO)
+              dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
+          }
+        }
+        epi_sync();
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
+}
+
+int g_num_sms = 0;
+
+template <int PREC, int CHAIN, bool POOL>
+cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
+                          float *partial, cudaStream_t s) {
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL>;
+  const int smem = q.smem_bytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (!g_num_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  const long grid = q.units < g_num_sms ? q.units : g_num_sms;
+  prof_begin(s);
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(p, q, bimg, partial);
+  prof_end(s, p.entry);
+  return cudaGetLastError();
+}
+
+template <int PREC>
+cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
+                        float *partial, cudaStream_t s) {
+  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true>(p, q, bimg, partial, s);
+  switch (p.chain) {
+    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false>(p, q, bimg, partial, s);
+    case CHAIN_RELU_HARDSWISH:
+      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false>(p, q, bimg, partial, s);
+    case CHAIN_LEAKY_ADD_CLAMP_GELU:
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false>(p, q, bimg, partial, s);
+    default: return launch_kernel<PREC, CHAIN_GENERIC, false>(p, q, bimg, partial, s);
+  }
+}
+
+}  // namespace
+
+bool tc_supported(const ConvProblem &p, int prec) { return make_plan(p, prec).ok != 0; }
+
+size_t tc_weight_bytes(const ConvProblem &p) {
+  size_t m = 0;
+  for (int prec = 0; prec < 2; ++prec) {
+    TcPlan q = make_plan(p, prec);
+    if (q.ok) {
+      size_t b = (size_t)q.COB * q.NCH * q.b_chunk_bytes;
+      if (b > m) m = b;
+    }
+  }
+  return m;
+}
+
+int tc_pool_tiles_per_image(const ConvProblem &p) {
+  if (!p.pool) return 0;
+  int m = 0;
+  for (int prec = 0; prec < 2; ++prec) {
+    TcPlan q = make_plan(p, prec);
+    if (q.ok && q.n_rt * q.n_ct > m) m = q.n_rt * q.n_ct;
+  }
+  return m;
+}
+
+cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &L,
+                      cudaStream_t s, int *launches) {
+  TcPlan q = make_plan(p, prec);
+  if (!q.ok) return cudaErrorNotSupported;
+  uint8_t *bimg = static_cast<uint8_t *>(ws) + L.tc_w;
+  float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
+  const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
+  int blocks = (int)((nelem + 255) / 256);
+  if (blocks > 2048) blocks = 2048;
+  tc_pack_weights<<<blocks, 256, 0, s>>>(p, q, bimg);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launches = 1;
+  e = prec ? launch_prec<1>(p, q, bimg, partial, s) : launch_prec<0>(p, q, bimg, partial, s);
+  if (e != cudaSuccess) return e;
+  *launches += 1;
+  if (p.pool) {
+    e = pool_finish_launch(p, partial, q.n_rt * q.n_ct, s);
+    *launches += 1;
+  }
+  return e;
+}
+
 }  // namespace fc

@@ -19,7 +19,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 ATOL = RTOL = 1e-4
-VARIANTS = ["ffma"]
+VARIANTS = ["ffma", "tc_tf32x3", "tc_f16x3"]
 
 
 def fc():
