@@ -34,7 +34,7 @@ EXPORTS = ("fc_conv2d_epi", "fc_conv3d_epi", "fc_convT2d_pool_mean",
            "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
-           "fc_profile_read", "fc_profile_reset")
+           "fc_profile_read", "fc_profile_reset", "fc_wait_report")
 
 
 class FcError(RuntimeError):
@@ -93,6 +93,8 @@ def lib():
             L.fc_profile_read.argtypes = [I, ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(I)]
             L.fc_profile_reset.restype = None
+            L.fc_wait_report.restype = I
+            L.fc_wait_report.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I]
             _lib = L
     return _lib
 
@@ -170,6 +172,21 @@ def last_launch_count() -> int:
 
 def get_last_device_error(stream=None) -> int:
     return int(lib().fc_get_last_device_error(_stream_handle(stream)))
+
+
+def wait_report(stream=None):
+    """Records of timed-out kernel waits since the last call (diagnostics
+    for FC_ERR_TIMEOUT): a list of dicts, cleared on read."""
+    buf = (ctypes.c_uint * (1 + 32 * 8))()
+    n = lib().fc_wait_report(_stream_handle(stream), buf, len(buf))
+    if n < 0:
+        raise FcError(5, "fc_wait_report")
+    recs = []
+    for i in range(min(n, 32)):
+        r = buf[1 + 8 * i:1 + 8 * i + 8]
+        recs.append({"block": r[0], "thread": r[1], "barrier": r[2], "parity": r[3],
+                     "tag": hex(r[4]), "word": hex(r[5] | (r[6] << 32))})
+    return n, recs
 
 
 def profile_enable(on: bool = True):

@@ -11,9 +11,12 @@ namespace fc {
 
 namespace {
 
-// Per-device status word (kernels OR bits into it; the host reads and clears
-// it in fc_get_last_device_error).
-__device__ unsigned int g_status_word;
+// Per-device status area: word 0 is the status word (kernels OR bits into
+// it; fc_get_last_device_error reads and clears it); word 1 counts
+// timed-out waits and words 2.. hold up to 32 records of 8 words each
+// describing where those waits gave up (read by fc_wait_report).
+constexpr int kStatusWords = 2 + 32 * 8;
+__device__ unsigned int g_status_word[kStatusWords];
 
 constexpr int kMaxDevices = 64;
 unsigned int *g_status_ptr[kMaxDevices];
@@ -369,6 +372,22 @@ fc_status fc_get_last_device_error(void *stream) {
 }
 
 int fc_version(void) { return 100; }
+
+int fc_wait_report(void *stream, unsigned int *out, int max_words) {
+  unsigned int *st = nullptr;
+  if (status_ptr(&st) != FC_OK || !out || max_words < 1) return -1;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  unsigned int buf[kStatusWords];
+  if (cudaMemcpy(buf, st, sizeof(buf), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  const int n = (int)(buf[1] < 32u ? buf[1] : 32u);
+  const int words = 1 + 8 * n;
+  for (int i = 0; i < words && i < max_words; ++i) out[i] = buf[1 + i];
+  if (buf[1]) {
+    unsigned int zero[kStatusWords - 1] = {0};
+    if (cudaMemcpy(st + 1, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+  }
+  return (int)buf[1];
+}
 
 fc_status fc_profile_enable(int on) {
   g_prof_on = on != 0;

@@ -34,10 +34,27 @@
 // bit, every role drains, and the CTA frees its tensor memory and exits.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stdlib.h>
 
 #include "fc_epi.cuh"
 #include "fc_internal.h"
 #include "fc_tc_ptx.cuh"
+
+// Optional per-role cycle accounting for performance experiments (off in
+// the library build): each role's first thread accumulates clock64 deltas
+// into named buckets, written per CTA to fc_tc_role_cycles at exit.
+#ifdef FC_ROLE_TIMING
+#define RT_DECL unsigned long long rt_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; \
+  unsigned long long rt_t0 = clock64();
+#define RT_MARK(i) do { const unsigned long long t_ = clock64(); rt_[i] += t_ - rt_t0; rt_t0 = t_; } while (0)
+#define RT_STORE(role) do { if ((threadIdx.x & 31) == 0 && (role) >= 0) for (int i_ = 0; i_ < 8; ++i_) \
+  fc_tc_role_cycles[(blockIdx.x * 3 + (role)) * 8 + i_] = rt_[i_]; } while (0)
+__device__ unsigned long long fc_tc_role_cycles[1024 * 3 * 8];
+#else
+#define RT_DECL
+#define RT_MARK(i) do {} while (0)
+#define RT_STORE(role) do {} while (0)
+#endif
 
 namespace fc {
 
@@ -51,6 +68,7 @@ constexpr int kProdThreads = 256;
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
+constexpr unsigned int kWaitRecords = 32;  // diagnostic records kept after the status word
 
 struct TcPlan {
   int ok;
@@ -77,6 +95,7 @@ struct TcPlan {
   long units;
   int smem_bytes;
   int off_b, off_bar, off_misc;
+  int dbg;  // diagnostics: bit 0 MMA issue from lane 0, bit 1 every lane polls
 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -156,16 +175,44 @@ struct SmemCtl {
   float red[4][64];  // pool: per-warp partial sums
 };
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                         unsigned int *status) {
+// Bounded wait on phase `parity` of `bar`.  On timeout: sets the status
+// bit, records where it gave up (block, thread, barrier index, parity, the
+// caller's tag and the raw barrier word) in the diagnostic area that
+// follows the status word, raises the CTA's abort flag and returns false.
+__device__ __noinline__ void record_timeout(unsigned int *status, const uint64_t *bar,
+                                            int bar_idx, uint32_t parity, uint32_t tag) {
+  if (!(tag & 0x08000000u)) atomicOr(status, ST_TIMEOUT);
+  const unsigned int i = atomicAdd(status + 1, 1u);
+  if (i < kWaitRecords) {
+    unsigned int *r = status + 2 + i * 8;
+    uint64_t word;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(word) : "r"(ptx::smem_u32(bar)));
+    r[0] = blockIdx.x;
+    r[1] = threadIdx.x;
+    r[2] = (unsigned)bar_idx;
+    r[3] = parity;
+    r[4] = tag;
+    r[5] = (unsigned)word;
+    r[6] = (unsigned)(word >> 32);
+    r[7] = 0x5afeu;
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parity,
+                                         volatile int *abort, unsigned int *status,
+                                         uint32_t tag) {
+  uint64_t *bar = bars + idx;
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((i & 127u) == 0) {
-      if (*abort) return false;
+      if (*abort) {
+        record_timeout(status, bar, idx, parity, tag | 0x08000000u);
+        return false;
+      }
       if (ptx::globaltimer_ns() - t0 > kWaitNs) {
-        atomicOr(status, ST_TIMEOUT);
+        record_timeout(status, bar, idx, parity, tag);
         *abort = 1;
         return false;
       }
@@ -175,10 +222,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so a
 // warp never splits around .sync.aligned instructions or named barriers.
-__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity,
-                                              volatile int *abort, unsigned int *status) {
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t parity,
+                                              volatile int *abort, unsigned int *status,
+                                              uint32_t tag, int dbg = 0) {
+  if (dbg & 2) {
+    const int okl = wait_bar(bars, idx, parity, abort, status, tag) ? 1 : 0;
+    return __all_sync(0xffffffffu, okl) != 0;
+  }
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bars, idx, parity, abort, status, tag) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -308,13 +360,15 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + q.off_bar);
-  uint64_t *a_full = bars;
-  uint64_t *a_empty = bars + 4;
-  uint64_t *b_full = bars + 8;
-  uint64_t *b_empty = bars + 10;
-  uint64_t *acc_full = bars + 12;
-  uint64_t *acc_empty = bars + 16;
-  uint64_t *drain = bars + 20;
+  constexpr int A_FULL = 0, A_EMPTY = 4, B_FULL = 8, B_EMPTY = 10, ACC_FULL = 12,
+                ACC_EMPTY = 16, DRAIN = 20;
+  uint64_t *a_full = bars + A_FULL;
+  uint64_t *a_empty = bars + A_EMPTY;
+  uint64_t *b_full = bars + B_FULL;
+  uint64_t *b_empty = bars + B_EMPTY;
+  uint64_t *acc_full = bars + ACC_FULL;
+  uint64_t *acc_empty = bars + ACC_EMPTY;
+  uint64_t *drain = bars + DRAIN;
   SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + q.off_misc);
   volatile int *abort_flag = &ctl->abort;
 
@@ -371,6 +425,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const int items = q.P * q.NPIX;
     const int rinrs = q.RIN * q.RS;
     const long cstride = (long)p.D * HW;
+    RT_DECL
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q, p);
       const int oh0 = up.rt * U * q.R;  // first output row of the unit
@@ -378,13 +433,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       const long xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = (int)(g % q.S);
-        if (!wait_bar_warp(&a_empty[s], ((g / q.S) & 1) ^ 1, abort_flag, p.status)) {
+        RT_MARK(0);
+        if (!wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag, p.status, 0x10000000u | g, q.dbg)) {
           ok = false;
           break;
         }
         if (!q.b_resident && warp == kProdWarp0) {
           const int sb = (int)(gb % q.SB);
-          if (!wait_bar_warp(&b_empty[sb], ((gb / q.SB) & 1) ^ 1, abort_flag, p.status)) {
+          if (!wait_bar_warp(bars, B_EMPTY + sb, ((gb / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | gb, q.dbg)) {
             ok = false;
             break;
           }
@@ -399,6 +455,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           }
           ++gb;
         }
+        RT_MARK(1);  // waiting for a free stage
         uint8_t *stage = smem + (long)s * q.a_stage_bytes;
         uint8_t *stage_lo = stage + q.P * q.plane_bytes;
         const int ci0 = c * q.chunk_ci;
@@ -440,38 +497,44 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&a_full[s]);
+        RT_MARK(2);  // filling the stage
       }
     }
+    RT_STORE(warp == kProdWarp0 ? 2 : -1);
     if (range_bad) atomicOr(p.status, ST_RANGE);
     // drain outstanding weight copies before the CTA can exit
     if (pt == 0) {
       if (q.b_resident) {
-        wait_bar(&b_full[0], 0, abort_flag, p.status);
+        wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
       } else if (gb > 0) {
         for (uint32_t k = (gb > (uint32_t)q.SB ? gb - q.SB : 0); k < gb; ++k)
-          wait_bar(&b_full[k % q.SB], (k / q.SB) & 1, abort_flag, p.status);
+          wait_bar(bars, B_FULL + (int)(k % q.SB), (k / q.SB) & 1, abort_flag, p.status, 0x13000000u | k);
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
     // The warp stays converged; one leader lane (fixed for the whole kernel,
     // so every commit tracks every MMA) issues each short burst.
-    const bool leader = ptx::elect_one();
+    const bool leader = (q.dbg & 1) ? (lane == 0) : ptx::elect_one();
     constexpr uint32_t fmt = PREC ? 0u : 2u;
     constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
     constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
     const uint32_t sbase = ptx::smem_u32(smem);
     uint32_t g = 0, gb = 0, it = 0;
     bool ok = true;
-    if (q.b_resident) ok = wait_bar_warp(&b_full[0], 0, abort_flag, p.status);
+    RT_DECL
+    if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u, q.dbg);
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)(u / ((long)p.N * p.Do * q.n_rt * q.n_ct));
       const int acc = (int)(it % q.NACC);
-      if (!wait_bar_warp(&acc_empty[acc], ((it / q.NACC) & 1) ^ 1, abort_flag, p.status)) break;
+      RT_MARK(0);
+      if (!wait_bar_warp(bars, ACC_EMPTY + acc, ((it / q.NACC) & 1) ^ 1, abort_flag, p.status, 0x21000000u | it, q.dbg)) break;
       ptx::tc_fence_after();
+      RT_MARK(1);  // waiting for a free accumulator
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = (int)(g % q.S);
-        if (!wait_bar_warp(&a_full[s], (g / q.S) & 1, abort_flag, p.status)) {
+        RT_MARK(0);
+        if (!wait_bar_warp(bars, A_FULL + s, (g / q.S) & 1, abort_flag, p.status, 0x22000000u | g, q.dbg)) {
           ok = false;
           break;
         }
@@ -481,13 +544,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           bbase = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
         } else {
           sb = (int)(gb % q.SB);
-          if (!wait_bar_warp(&b_full[sb], (gb / q.SB) & 1, abort_flag, p.status)) {
+          if (!wait_bar_warp(bars, B_FULL + sb, (gb / q.SB) & 1, abort_flag, p.status, 0x23000000u | gb, q.dbg)) {
             ok = false;
             break;
           }
           bbase = sbase + q.off_b + (uint32_t)(sb * q.b_chunk_bytes);
         }
         ptx::tc_fence_after();
+        RT_MARK(2);  // waiting for a filled stage
         const uint32_t a_hi = sbase + (uint32_t)(s * q.a_stage_bytes);
         const uint32_t a_lo = a_hi + (uint32_t)(q.P * q.plane_bytes);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
@@ -531,6 +595,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
         __syncwarp();
         if (!q.b_resident) ++gb;
+        RT_MARK(3);  // issuing MMAs
       }
       if (!ok) break;
       if (leader) ptx::tc_commit(&acc_full[acc]);
@@ -539,19 +604,24 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // wait until every MMA this warp issued has completed
     if (leader) ptx::tc_commit(drain);
     __syncwarp();
-    wait_bar_warp(drain, 0, abort_flag, p.status);
+    wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u, q.dbg);
+    RT_MARK(4);
+    RT_STORE(1);
   } else {
     // ------------------------------------------------------------ epilogue
     const int m = warp * 32 + lane;  // TMEM lane = M row = output pixel
     const float scale = PREC ? (1.0f / 2048.0f) : 1.0f;
     uint32_t it = 0;
+    RT_DECL
     for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const UnitPos up = decode_unit(u, q, p);
       const int acc = (int)(it % q.NACC);
-      bool okw = wait_bar_warp(&acc_full[acc], (it / q.NACC) & 1, abort_flag, p.status);
+      RT_MARK(0);
+      bool okw = wait_bar_warp(bars, ACC_FULL + acc, (it / q.NACC) & 1, abort_flag, p.status, 0x30000000u | it, q.dbg);
       if constexpr (POOL) okw = epi_all(okw);
       if (!okw) break;
       ptx::tc_fence_after();
+      RT_MARK(1);  // waiting for a finished accumulator
       const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
       const int co_base = up.cb * 64;
       if constexpr (!POOL) {
@@ -566,9 +636,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 #pragma unroll 1
         for (int cc = 0; cc < 64; cc += 16) {
           uint32_t hi[16], lo[16];
+          RT_MARK(0);
           ptx::tmem_ld16(tl + col0 + cc, hi);
           ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
           ptx::tmem_wait_ld();
+          RT_MARK(2);  // tensor-memory loads
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -581,6 +653,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               }
             }
           }
+          RT_MARK(3);  // epilogue math + stores
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -635,6 +708,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         epi_sync();
       }
     }
+    RT_STORE(warp == 0 ? 0 : -1);
   }
 
   ptx::tc_fence_before();
@@ -709,6 +783,7 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
                       cudaStream_t s, int *launches) {
   TcPlan q = make_plan(p, prec);
   if (!q.ok) return cudaErrorNotSupported;
+  if (const char *e = getenv("FC_TC_DEBUG")) q.dbg = atoi(e);
   uint8_t *bimg = static_cast<uint8_t *>(ws) + L.tc_w;
   float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
   const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
@@ -729,3 +804,13 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
 }
 
 }  // namespace fc
+
+#ifdef FC_ROLE_TIMING
+extern "C" __attribute__((visibility("default"))) int fc_debug_role_cycles(unsigned long long *out,
+                                                                            int n) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (n > 1024 * 3 * 8) n = 1024 * 3 * 8;
+  return cudaMemcpyFromSymbol(out, fc_tc_role_cycles, sizeof(unsigned long long) * n) == cudaSuccess
+             ? n : -1;
+}
+#endif

@@ -183,6 +183,16 @@ FC_API fc_status fc_profile_enable(int on);
 FC_API fc_status fc_profile_read(int entry, double *total_ms, int *launches);
 FC_API void fc_profile_reset(void);
 
+/* Diagnostics for FC_ERR_TIMEOUT.  Synchronises `stream`, copies the
+ * current device's record of timed-out kernel waits into `out` (word 0:
+ * number of timeouts since the last call; then 8 words per record, at most
+ * 32 records: block, thread, barrier index, phase parity, the waiting
+ * role's tag, the raw 64-bit barrier word (low, high), and the marker
+ * 0x5afe), clears it, and returns the number of timeouts (-1 on error).
+ * No counterpart on the pages: this is the failure-detection side of the
+ * bounded waits. */
+FC_API int fc_wait_report(void *stream, unsigned int *out, int max_words);
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 FC_API int fc_version(void);
 
