@@ -26,10 +26,12 @@
 // the GB300 form of the traces' shared-memory halo tile.
 //
 // Roles (416 threads): warps 0-3 epilogue (TMEM lanes 32w..32w+31), warp 4
-// TMEM allocation + MMA issue (the warp runs converged; one fixed leader
-// lane issues each burst of MMAs), warps 5-12 producers (global loads of
-// the input halo, hi/lo split, st.shared into the stage ring; one producer
-// lane also streams packed weights with bulk copies).  All waits are
+// TMEM allocation + MMA issue (the warp runs converged; each burst of MMAs
+// and each commit is issued by the lane elect.sync picks, the same lowest
+// lane every time), warps 5-12 producers (one staged input row per warp
+// pass, lanes across its pixels: global loads, hi/lo split, st.shared into
+// the stage ring; one producer lane also streams packed weights with bulk
+// copies).  All waits are
 // bounded (4 s on %globaltimer) and warp-uniform; a timeout sets a status
 // bit, every role drains, and the CTA frees its tensor memory and exits.
 #include <cuda_fp16.h>
@@ -100,6 +102,18 @@ struct TcPlan {
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in smem
+
+struct SmemCtl {
+  uint32_t tmem_base;
+  int abort;
+  uint32_t koff[27];          // byte offset of K step ks's first slice in a stage
+  uint32_t klbo[27];          // byte distance to its second slice
+  float red[4][64];           // pool: per-warp partial sums
+  float bias[kMaxCoTc];       // bias per output channel (0 without bias)
+  float addend[kMaxCoTc];     // per-channel addend of the fused GELU chain
+};
+
 TcPlan make_plan(const ConvProblem &p, int prec) {
   TcPlan q{};
   if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
@@ -136,6 +150,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.plane_bytes = q.NPIX * 16;
   q.a_stage_bytes = 2 * q.P * q.plane_bytes;
   q.COB = cdiv(p.CO, 64);
+  if (q.COB * 64 > kMaxCoTc) return q;
   q.b_chunk_bytes = q.KS * kBStep;
   q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
@@ -143,7 +158,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.tmem_cols = q.NACC * q.U * 128;
   if (q.tmem_cols > 512) return q;
   // shared memory: A stages + B (resident or a ring) + barriers/misc
-  const int misc = 2048;
+  const int misc = 512 + (int)sizeof(SmemCtl) + 256;
   const long b_all = (long)q.COB * q.NCH * q.b_chunk_bytes;
   int S = 0, resident = 0, SB = 0;
   for (int s = 4; s >= 2 && !S; --s)
@@ -161,19 +176,14 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.off_b = S * q.a_stage_bytes;
   q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
   q.off_misc = q.off_bar + 512;
-  q.smem_bytes = q.off_misc + misc - 512;
+  q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
   q.ok = 1;
   return q;
 }
 
 // --------------------------------------------------------------- device
-struct SmemCtl {
-  uint32_t tmem_base;
-  int abort;
-  int shift[27];     // staged-pixel offset of each tap
-  float red[4][64];  // pool: per-warp partial sums
-};
+
 
 // Bounded wait on phase `parity` of `bar`.  On timeout: sets the status
 // bit, records where it gave up (block, thread, barrier index, parity, the
@@ -392,9 +402,21 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (tid < q.TAPS) {
-    const int kd = tid / 9, kh = (tid / 3) % 3, kw = tid % 3;
-    ctl->shift[tid] = (kd * q.RIN + kh) * q.RS + kw;
+  if (tid < q.KS) {
+    // staged-pixel shift of tap t = (kd, kh, kw): (kd*RIN + kh)*RS + kw
+    auto shift = [&](int t) { return ((t / 9) * q.RIN + (t / 3) % 3) * q.RS + t % 3; };
+    if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last tap)
+      const int t0 = 2 * tid;
+      ctl->koff[tid] = (uint32_t)shift(t0) * 16u;
+      ctl->klbo[tid] = (t0 + 1 < q.TAPS) ? (uint32_t)(shift(t0 + 1) - shift(t0)) * 16u : 16u;
+    } else {           // slices: planes 0 and 1 of tap ks
+      ctl->koff[tid] = (uint32_t)shift(tid) * 16u;
+      ctl->klbo[tid] = (uint32_t)q.plane_bytes;
+    }
+  }
+  for (int c = tid; c < q.COB * 64; c += kThreads) {
+    ctl->bias[c] = (c < p.CO && p.epi.bias) ? p.epi.bias[c] : 0.0f;
+    ctl->addend[c] = (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU && c < p.CO) ? p.epi.chan[1][c] : 0.0f;
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(&ctl->tmem_base, (uint32_t)q.tmem_cols);
@@ -422,9 +444,20 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::bulk_g2s(smem + q.off_b + off, bimg + off, nb, &b_full[0]);
       }
     }
-    const int items = q.P * q.NPIX;
-    const int rinrs = q.RIN * q.RS;
+    const int nrows = p.KD * q.RIN;  // staged rows per slice plane
+    const int jobs = q.P * nrows;     // (plane, staged row) pairs per stage
     const long cstride = (long)p.D * HW;
+    constexpr int kMaxCols = 5;       // ceil(130 / 32): staged row width <= 130
+    // Pixels past the staged rows are only read by discarded M rows; zero
+    // them once so those rows stay finite.
+    {
+      const int tail0 = nrows * q.RS;
+      for (int st = 0; st < q.S; ++st)
+        for (int pl = 0; pl < 2 * q.P; ++pl)
+          for (int px = tail0 + pt; px < q.NPIX; px += kProdThreads)
+            *reinterpret_cast<uint4 *>(smem + (long)st * q.a_stage_bytes + pl * q.plane_bytes +
+                                       px * 16) = make_uint4(0, 0, 0, 0);
+    }
     RT_DECL
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q, p);
@@ -459,40 +492,33 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         uint8_t *stage = smem + (long)s * q.a_stage_bytes;
         uint8_t *stage_lo = stage + q.P * q.plane_bytes;
         const int ci0 = c * q.chunk_ci;
-        for (int it0 = pt; it0 < items; it0 += 4 * kProdThreads) {
-          float v[4][E];
-          int dst_off[4];
+        for (int job = warp - kProdWarp0; job < jobs; job += kProdThreads / 32) {
+          const int plane = job / nrows;
+          const int sr = job - plane * nrows;
+          const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
+          const int id = up.od + kdp - p.pad_d, ih = oh0 + r - p.pad;
+          const bool rowok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
+          const int cbase = ci0 + plane * E;
+          const int iw0 = ow0 - p.pad;
+          const long rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
+          float v[kMaxCols][E];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * kProdThreads;
-            dst_off[k] = -1;
+          for (int k = 0; k < kMaxCols; ++k) {
+            const int cc = lane + 32 * k;
+            const bool colok = rowok && cc < q.RS && iw0 + cc >= 0 && iw0 + cc < p.W;
 #pragma unroll
-            for (int e = 0; e < E; ++e) v[k][e] = 0.0f;
-            if (it < items) {
-              const int plane = it / q.NPIX;
-              const int pix = it - plane * q.NPIX;
-              dst_off[k] = plane * q.plane_bytes + pix * 16;
-              const int kdp = pix / rinrs;
-              const int rem = pix - kdp * rinrs;
-              const int r = rem / q.RS;
-              const int cc = rem - r * q.RS;
-              const int id = up.od + kdp - p.pad_d;
-              const int ih = oh0 + r - p.pad;
-              const int iw = ow0 + cc - p.pad;
-              if (kdp < p.KD && id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 &&
-                  iw < p.W) {
-                const long base = xn + (long)id * HW + (long)ih * p.W + iw;
-                const int cbase = ci0 + plane * E;
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                  if (cbase + e < p.C) v[k][e] = __ldg(p.x + base + (long)(cbase + e) * cstride);
-              }
-            }
+            for (int e = 0; e < E; ++e)
+              v[k][e] = (colok && cbase + e < p.C)
+                            ? __ldg(p.x + rowbase + cc + (long)(cbase + e) * cstride)
+                            : 0.0f;
           }
+          uint8_t *dhi = stage + plane * q.plane_bytes + sr * q.RS * 16;
+          uint8_t *dlo = stage_lo + plane * q.plane_bytes + sr * q.RS * 16;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (dst_off[k] >= 0)
-              store_slice<PREC, E>(stage + dst_off[k], stage_lo + dst_off[k], v[k], range_bad);
+          for (int k = 0; k < kMaxCols; ++k) {
+            const int cc = lane + 32 * k;
+            if (cc < q.RS) store_slice<PREC, E>(dhi + cc * 16, dlo + cc * 16, v[k], range_bad);
+          }
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -513,9 +539,9 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
-    // The warp stays converged; one leader lane (fixed for the whole kernel,
-    // so every commit tracks every MMA) issues each short burst.
-    const bool leader = (q.dbg & 1) ? (lane == 0) : ptx::elect_one();
+    // The warp stays converged; every MMA burst and every commit is issued
+    // under elect.sync, which picks the same (lowest) lane each time, so each
+    // commit tracks all MMAs before it.
     constexpr uint32_t fmt = PREC ? 0u : 2u;
     constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
     constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
@@ -556,15 +582,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t a_lo = a_hi + (uint32_t)(q.P * q.plane_bytes);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
         for (int ks = 0; ks < q.KS; ++ks) {
-          uint32_t off0, lbo;
-          if (q.pairtaps) {
-            const int t0 = 2 * ks;
-            off0 = (uint32_t)ctl->shift[t0] * 16u;
-            lbo = (t0 + 1 < q.TAPS) ? (uint32_t)(ctl->shift[t0 + 1] - ctl->shift[t0]) * 16u : 16u;
-          } else {
-            off0 = (uint32_t)ctl->shift[ks] * 16u;
-            lbo = (uint32_t)q.plane_bytes;
-          }
+          const uint32_t off0 = ctl->koff[ks], lbo = ctl->klbo[ks];
           const uint64_t bdesc = ptx::smem_desc(bbase + (uint32_t)ks * kBStep, 2048, 128);
           const uint32_t accum = (c | ks) != 0;
           uint64_t ah[U], al[U];
@@ -574,7 +592,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             ah[t] = ptx::smem_desc(a_hi + off0 + moff, lbo, 128);
             al[t] = ptx::smem_desc(a_lo + off0 + moff, lbo, 128);
           }
-          if (leader) {
+          if (ptx::elect_one()) {
 #pragma unroll
             for (int t = 0; t < U; ++t) {
               const uint32_t d = dacc + (uint32_t)(t * 128);
@@ -589,7 +607,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           }
           __syncwarp();
         }
-        if (leader) {
+        if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
           if (!q.b_resident) ptx::tc_commit(&b_empty[sb]);
         }
@@ -598,11 +616,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         RT_MARK(3);  // issuing MMAs
       }
       if (!ok) break;
-      if (leader) ptx::tc_commit(&acc_full[acc]);
+      if (ptx::elect_one()) ptx::tc_commit(&acc_full[acc]);
       __syncwarp();
     }
     // wait until every MMA this warp issued has completed
-    if (leader) ptx::tc_commit(drain);
+    if (ptx::elect_one()) ptx::tc_commit(drain);
     __syncwarp();
     wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u, q.dbg);
     RT_MARK(4);
@@ -630,8 +648,9 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
         const long plane = (long)p.Ho * p.Wo;
         const long cstride = (long)p.Do * plane;
-        float *ybase = p.y + ((long)up.n * p.CO * p.Do + up.od) * plane;
-        const long yoff = (long)oh * p.Wo + ow;
+        float *yp = p.y + (((long)up.n * p.CO + co_base) * p.Do + up.od) * plane +
+                    (long)oh * p.Wo + ow;
+        const int nco = p.CO - co_base < 64 ? p.CO - co_base : 64;
         const uint32_t col0 = (uint32_t)(acc * 128);
 #pragma unroll 1
         for (int cc = 0; cc < 64; cc += 16) {
@@ -641,15 +660,24 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
           ptx::tmem_wait_ld();
           RT_MARK(2);  // tensor-memory loads
+          float bv[16], av[16];
+#pragma unroll
+          for (int j = 0; j < 16; j += 4) {
+            *reinterpret_cast<float4 *>(&bv[j]) =
+                *reinterpret_cast<const float4 *>(&ctl->bias[co_base + cc + j]);
+            if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU)
+              *reinterpret_cast<float4 *>(&av[j]) =
+                  *reinterpret_cast<const float4 *>(&ctl->addend[co_base + cc + j]);
+            else
+              av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
+          }
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int co = co_base + cc + j;
-              if (co < p.CO) {
-                const float bias = p.epi.bias ? __ldg(p.epi.bias + co) : 0.0f;
-                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bias;
-                v = apply_chain<CHAIN>(p.epi, co, v, chain_addend<CHAIN>(p.epi, co));
-                ybase[(long)co * cstride + yoff] = v;
+              if (cc + j < nco) {
+                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                v = apply_chain<CHAIN>(p.epi, co_base + cc + j, v, av[j]);
+                yp[(long)(cc + j) * cstride] = v;
               }
             }
           }
@@ -675,7 +703,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int co = co_base + cc + j;
-            const float bias = (co < p.CO && p.epi.bias) ? __ldg(p.epi.bias + co) : 0.0f;
+            const float bias = ctl->bias[co];
             const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
             const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
             float mx = fmaxf(v0, v1);
