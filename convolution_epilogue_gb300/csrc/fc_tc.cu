@@ -70,6 +70,7 @@ constexpr int kProdThreads = 256;
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
+constexpr uint32_t kSleepHintNs = 20000;  // hardware sleep per poll while waiting
 constexpr unsigned int kWaitRecords = 32;  // diagnostic records kept after the status word
 
 struct TcPlan {
@@ -215,8 +216,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parit
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 127u) == 0) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if ((i & 7u) == 0) {
       if (*abort) {
         record_timeout(status, bar, idx, parity, tag | 0x08000000u);
         return false;
