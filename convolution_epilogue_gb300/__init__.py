@@ -30,7 +30,7 @@ VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 MAX_OPS = 8
 
 # every symbol include/fusedconv.h declares
-EXPORTS = ("fc_conv2d_epi", "fc_conv3d_epi", "fc_convT2d_pool_mean",
+EXPORTS = ("fc_conv2d_epi", "fc_conv2d_epi_noalloc", "fc_conv3d_epi", "fc_convT2d_pool_mean",
            "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
@@ -70,6 +70,8 @@ def lib():
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.fc_conv2d_epi.restype = I
             L.fc_conv2d_epi.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P, P, S, P]
+            L.fc_conv2d_epi_noalloc.restype = I
+            L.fc_conv2d_epi_noalloc.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P, P]
             L.fc_conv3d_epi.restype = I
             L.fc_conv3d_epi.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I, P, P,
                                         P, S, P]
@@ -226,6 +228,27 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
                              ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
                              _stream_handle(stream))
     _check(st, "fc_conv2d_epi")
+    del keep
+    return y
+
+
+def fc_conv2d_epi_noalloc(x, w, y, bias=None, ops=(), pad=0, stream=None):
+    """fc_conv2d_epi without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed 1 MiB device
+    array (shared by all calls on a device; overlapping calls race).  The
+    caller passes every tensor, including the output y; nothing is
+    allocated here."""
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    _require_cuda_f32("y", y)
+    N, C, H, W = x.shape
+    CO, C2, KH, KW = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    e, keep = make_epilogue(bias, ops)
+    st = lib().fc_conv2d_epi_noalloc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad,
+                                     ctypes.byref(e), _ptr(y), _stream_handle(stream))
+    _check(st, "fc_conv2d_epi_noalloc")
     del keep
     return y
 

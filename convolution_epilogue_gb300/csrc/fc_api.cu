@@ -198,7 +198,56 @@ WsLayout ws_layout(const ConvProblem &p) {
 
 using namespace fc;
 
+// ---------------------------------------------------------------------------
+// Workspace for fc_conv2d_epi_noalloc.  Some callers cannot allocate device
+// memory at all: code running inside a host-side callback or a custom
+// allocator hook, real-time or safety-certified paths that forbid allocation
+// after start-up, and plug-in hosts that own the device memory pool.  For
+// them the library keeps this fixed array in device memory; it exists on
+// every GPU that loads the library, until the process exits.
+static constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char fc_noalloc_scratch[kNoAllocScratchBytes];
+// In host code `fc_noalloc_scratch` names a host-side stand-in, not device
+// memory: kernels must get the address cudaGetSymbolAddress returns, looked
+// up once per device (with that device current) and cached here.
+static unsigned char *g_noalloc_ptr[64];
+
+static fc_status noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FC_ERR_CUDA;
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, fc_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return FC_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<unsigned char *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FC_OK;
+}
+
 extern "C" {
+
+fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
+                                const float *w, int C_out, int kH, int kW, int stride,
+                                int pad, const fc_epilogue *epi, float *y, void *stream) {
+  // The shapes' workspace must fit the fixed array; anything larger is
+  // refused before touching the device.
+  const int dims[7] = {N, C_in, H, W, C_out, kH, pad};
+  if (kH == kW && N >= 0 && C_in >= 1 && C_out >= 1 && H >= 1 && W >= 1 && pad >= 0) {
+    const size_t need = fc_workspace_bytes(0, dims);
+    if (need > kNoAllocScratchBytes) return FC_ERR_WORKSPACE;
+  }
+  void *scratch = nullptr;
+  const fc_status s = noalloc_scratch(&scratch);
+  if (s != FC_OK) return s;
+  // The packed weights are rewritten in the array by every call before use,
+  // so nothing in it has to start at zero.
+  return fc_conv2d_epi(x, N, C_in, H, W, w, C_out, kH, kW, stride, pad, epi, y, scratch,
+                       kNoAllocScratchBytes, stream);
+}
 
 fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,

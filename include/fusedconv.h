@@ -121,6 +121,27 @@ FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         int pad, const fc_epilogue *epi, float *y, void *ws,
                         size_t ws_bytes, void *stream);
 
+/* fc_conv2d_epi for callers that cannot allocate device memory (code run
+ * from a host callback or an allocator hook, allocation-free real-time or
+ * certified paths, plug-ins whose host owns the memory pool).  The pages
+ * have no counterpart to this call; it exists for those callers.
+ * Same arguments and results as fc_conv2d_epi minus ws / ws_bytes: the
+ * workspace is a fixed 1 MiB device array inside the library (held on every
+ * GPU that loads the library until the process exits).  The caller still
+ * passes x, w, the epilogue tensors and y.  Shapes whose workspace
+ * (fc_workspace_bytes(0, dims)) exceeds 1 MiB are refused with
+ * FC_ERR_WORKSPACE.  Nothing is allocated: no cudaMalloc / cudaFree and no
+ * allocating library routine (keep fc_profile_enable off).
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's
+ * contents (each call rewrites what it reads first); calls that overlap on
+ * the GPU -- on different streams or host threads -- race on it. */
+FC_API fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
+                                       const float *w, int C_out, int kH, int kW,
+                                       int stride, int pad, const fc_epilogue *epi,
+                                       float *y, void *stream);
+
 /* Conv3d + bias + elementwise epilogue chain; same ops as fc_conv2d_epi.
  * x [N][C_in][D][H][W]; w [C_out][C_in][kD][kH][kW];
  * y [N][C_out][Do][Ho][Wo], each extent in + 2 pad - k + 1.
