@@ -87,7 +87,8 @@ fc_status decode_eltwise(const fc_epilogue *epi, EpiDev *e, int *chain) {
            e->kind[1] == FC_EPI_ADD_CHANNEL &&
            (e->kind[2] == FC_EPI_CLAMP || e->kind[2] == FC_EPI_HARDTANH) &&
            e->kind[3] == FC_EPI_GELU_ERF)
-    *chain = CHAIN_LEAKY_ADD_CLAMP_GELU;
+    *chain = (e->a[2] >= -1.0f && e->b[2] <= 1.0f) ? CHAIN_LEAKY_ADD_CLAMP1_GELU
+                                                   : CHAIN_LEAKY_ADD_CLAMP_GELU;
   else
     *chain = CHAIN_GENERIC;
   return FC_OK;

@@ -13,9 +13,29 @@
 
 namespace fc {
 
+// x * clamp((x + 3) / 6, 0, 1), the gate as one saturated multiply-add.
 __device__ __forceinline__ float op_hardswish(float v) {
-  float g = fminf(fmaxf((v + 3.0f) * (1.0f / 6.0f), 0.0f), 1.0f);
-  return v * g;
+  return v * __saturatef(fmaf(v, 1.0f / 6.0f, 0.5f));
+}
+
+// erf(z) by its Maclaurin series, erf(z) = 2/sqrt(pi) sum_n (-1)^n
+// z^(2n+1) / (n! (2n+1)), truncated after n = 8 (Horner in z^2).  For
+// |z| <= 1/sqrt(2) the first omitted term is below 3e-10, far under fp32
+// rounding; used only where the argument is known to be that small.
+__device__ __forceinline__ float erf_maclaurin(float z) {
+  constexpr float c[9] = {1.128379167e+00f, -3.761263890e-01f, 1.128379167e-01f, -2.686617065e-02f, 5.223977625e-03f, -8.548327023e-04f, 1.205533298e-04f, -1.492565036e-05f, 1.646211437e-06f};
+  const float z2 = z * z;
+  float p = c[8];
+#pragma unroll
+  for (int n = 7; n >= 0; --n) p = fmaf(p, z2, c[n]);
+  return z * p;
+}
+
+// GELU for |v| <= 1 (its argument v / sqrt 2 is then within the series'
+// range).
+__device__ __forceinline__ float op_gelu_small(float v) {
+  const float h = 0.5f * v;
+  return fmaf(h, erf_maclaurin(v * 0.70710678118654752f), h);
 }
 
 __device__ __forceinline__ float op_gelu_erf(float v) {
@@ -51,6 +71,11 @@ __device__ __forceinline__ float apply_chain(const EpiDev &e, int co, float v,
     v = v + add;
     v = fminf(fmaxf(v, e.a[2]), e.b[2]);
     return op_gelu_erf(v);
+  } else if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+    v = v > 0.0f ? v : e.a[0] * v;
+    v = v + add;
+    v = fminf(fmaxf(v, e.a[2]), e.b[2]);  // inside [-1, 1]
+    return op_gelu_small(v);
   } else {
     for (int i = 0; i < e.n_ops; ++i)
       v = apply_op(e.kind[i], e.a[i], e.b[i], e.chan[i], co, v);
@@ -61,7 +86,8 @@ __device__ __forceinline__ float apply_chain(const EpiDev &e, int co, float v,
 // Per-channel addend used by CHAIN_LEAKY_ADD_CLAMP_GELU (op 1).
 template <int CHAIN>
 __device__ __forceinline__ float chain_addend(const EpiDev &e, int co) {
-  if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU) return __ldg(e.chan[1] + co);
+  if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU)
+    return __ldg(e.chan[1] + co);
   else return 0.0f;
 }
 

@@ -251,6 +251,8 @@ cudaError_t launch_eltwise(const ConvProblem &p, const float *wp, int Cp, int CO
       return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
       return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU>(p, wp, Cp, COp, nullptr, s);
+    case CHAIN_LEAKY_ADD_CLAMP1_GELU:
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP1_GELU>(p, wp, Cp, COp, nullptr, s);
     default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC>(p, wp, Cp, COp, nullptr, s);
   }
 }

@@ -14,7 +14,8 @@ enum ChainId : int {
   CHAIN_GENERIC = 0,
   CHAIN_NONE = 1,             // no op after the bias
   CHAIN_RELU_HARDSWISH = 2,   // relu -> hardswish
-  CHAIN_LEAKY_ADD_CLAMP_GELU = 3  // leaky(a) -> + chan -> clamp[a,b] -> gelu
+  CHAIN_LEAKY_ADD_CLAMP_GELU = 3,  // leaky(a) -> + chan -> clamp[a,b] -> gelu
+  CHAIN_LEAKY_ADD_CLAMP1_GELU = 4  // the same with [a,b] inside [-1,1]
 };
 
 // Epilogue as the kernels see it (passed by value).

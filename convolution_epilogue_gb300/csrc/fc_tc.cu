@@ -25,10 +25,11 @@
 // a different descriptor start address, no data movement per tap.  This is
 // the GB300 form of the traces' shared-memory halo tile.
 //
-// Roles (416 threads): warps 0-3 epilogue (TMEM lanes 32w..32w+31), warp 4
+// Roles (512 threads): warps 0-7 epilogue (warp w: TMEM lanes 32(w%4)..+31,
+// channels 32(w/4)..+31), warp 8
 // TMEM allocation + MMA issue (the warp runs converged; each burst of MMAs
 // and each commit is issued by the lane elect.sync picks, the same lowest
-// lane every time), warps 5-12 producers (one staged input row per warp
+// lane every time), warps 9-15 producers (one staged input row per warp
 // pass, lanes across its pixels: global loads, hi/lo split, st.shared into
 // the stage ring; one producer lane also streams packed weights with bulk
 // copies).  All waits are
@@ -62,11 +63,11 @@ namespace fc {
 
 namespace {
 
-constexpr int kThreads = 416;
-constexpr int kEpiWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
-constexpr int kProdThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 32 channels each
+constexpr int kMmaWarp = 8;
+constexpr int kProdWarp0 = 9;
+constexpr int kProdThreads = 224;  // 7 producer warps
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
@@ -98,6 +99,7 @@ struct TcPlan {
   long units;
   int smem_bytes;
   int off_b, off_bar, off_misc;
+  int ncol;  // 32-pixel column groups per staged row
   int dbg;  // diagnostics: bit 0 MMA issue from lane 0, bit 1 every lane polls
 };
 
@@ -143,6 +145,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
     q.R = 1;
   }
   q.RIN = q.U * q.R + 2;
+  q.ncol = cdiv(q.RS, 32);
   // last staged pixel any MMA can touch (+1 for the paired-tap slice)
   const int maxread = ((p.KD - 1) * q.RIN + 2) * q.RS + 2 + (q.U - 1) * q.R * q.RS + 127 + 1;
   int npix = maxread + 1;
@@ -245,13 +248,13 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// AND of a predicate over the 128 epilogue threads (named barrier 1).
+// AND of a predicate over the 256 epilogue threads (named barrier 1).
 __device__ __forceinline__ bool epi_all(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -259,7 +262,7 @@ __device__ __forceinline__ bool epi_all(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 struct UnitPos {
   int cb, n, od, rt, ct;
@@ -361,6 +364,30 @@ __device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, co
   }
 }
 
+// One staged row of one slice plane: lanes take pixels cc = lane + 32k,
+// load E input channels per pixel (zero outside the image), split them into
+// hi / lo parts and store the two 16-byte slices.  NCOL = column groups.
+template <int PREC, int E, int NCOL>
+__device__ __forceinline__ void fill_row(const float *__restrict__ x, long rowbase, long cstride,
+                                         int iw0, int W, int RS, bool rowok, int cbase, int C,
+                                         uint8_t *dhi, uint8_t *dlo, int lane, bool &range_bad) {
+  float v[NCOL][E];
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    const int cc = lane + 32 * k;
+    const bool colok = rowok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      v[k][e] = (colok && cbase + e < C) ? __ldg(x + rowbase + cc + (long)(cbase + e) * cstride)
+                                         : 0.0f;
+  }
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    const int cc = lane + 32 * k;
+    if (cc < RS) store_slice<PREC, E>(dhi + cc * 16, dlo + cc * 16, v[k], range_bad);
+  }
+}
+
 template <int PREC, int CHAIN, bool POOL>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
@@ -417,7 +444,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   }
   for (int c = tid; c < q.COB * 64; c += kThreads) {
     ctl->bias[c] = (c < p.CO && p.epi.bias) ? p.epi.bias[c] : 0.0f;
-    ctl->addend[c] = (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU && c < p.CO) ? p.epi.chan[1][c] : 0.0f;
+    ctl->addend[c] = ((CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU ||
+                       CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) && c < p.CO)
+                         ? p.epi.chan[1][c]
+                         : 0.0f;
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(&ctl->tmem_base, (uint32_t)q.tmem_cols);
@@ -448,7 +478,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const int nrows = p.KD * q.RIN;  // staged rows per slice plane
     const int jobs = q.P * nrows;     // (plane, staged row) pairs per stage
     const long cstride = (long)p.D * HW;
-    constexpr int kMaxCols = 5;       // ceil(130 / 32): staged row width <= 130
     // Pixels past the staged rows are only read by discarded M rows; zero
     // them once so those rows stay finite.
     {
@@ -502,23 +531,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           const int cbase = ci0 + plane * E;
           const int iw0 = ow0 - p.pad;
           const long rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
-          float v[kMaxCols][E];
-#pragma unroll
-          for (int k = 0; k < kMaxCols; ++k) {
-            const int cc = lane + 32 * k;
-            const bool colok = rowok && cc < q.RS && iw0 + cc >= 0 && iw0 + cc < p.W;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-              v[k][e] = (colok && cbase + e < p.C)
-                            ? __ldg(p.x + rowbase + cc + (long)(cbase + e) * cstride)
-                            : 0.0f;
-          }
           uint8_t *dhi = stage + plane * q.plane_bytes + sr * q.RS * 16;
           uint8_t *dlo = stage_lo + plane * q.plane_bytes + sr * q.RS * 16;
-#pragma unroll
-          for (int k = 0; k < kMaxCols; ++k) {
-            const int cc = lane + 32 * k;
-            if (cc < q.RS) store_slice<PREC, E>(dhi + cc * 16, dlo + cc * 16, v[k], range_bad);
+          switch (q.ncol) {
+            case 1: fill_row<PREC, E, 1>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
+            case 2: fill_row<PREC, E, 2>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
+            case 3: fill_row<PREC, E, 3>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
+            case 4: fill_row<PREC, E, 4>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
+            default: fill_row<PREC, E, 5>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
           }
         }
         ptx::fence_proxy_async_smem();
@@ -628,7 +648,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     RT_STORE(1);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int m = warp * 32 + lane;  // TMEM lane = M row = output pixel
+    // Warp w reads TMEM lane quadrant w % 4 (one output pixel per lane) and
+    // channel half w / 4 (32 of the 64 channels).
+    const int quad = warp & 3, half = warp >> 2;
+    const int m = quad * 32 + lane;  // TMEM lane = M row = output pixel
     const float scale = PREC ? (1.0f / 2048.0f) : 1.0f;
     uint32_t it = 0;
     RT_DECL
@@ -641,20 +664,21 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       if (!okw) break;
       ptx::tc_fence_after();
       RT_MARK(1);  // waiting for a finished accumulator
-      const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
       const int co_base = up.cb * 64;
+      const int ch0 = half * 32;  // first channel (within the block) of this warp
       if constexpr (!POOL) {
         const int r = m / q.RS, c = m - r * q.RS;
         const int oh = up.rt * q.R + r, ow = up.ct * q.WT + c;
         const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
         const long plane = (long)p.Ho * p.Wo;
         const long cstride = (long)p.Do * plane;
-        float *yp = p.y + (((long)up.n * p.CO + co_base) * p.Do + up.od) * plane +
+        float *yp = p.y + (((long)up.n * p.CO + co_base + ch0) * p.Do + up.od) * plane +
                     (long)oh * p.Wo + ow;
-        const int nco = p.CO - co_base < 64 ? p.CO - co_base : 64;
-        const uint32_t col0 = (uint32_t)(acc * 128);
+        const int nco = p.CO - co_base - ch0;  // channels of this warp that exist
+        const uint32_t col0 = (uint32_t)(acc * 128 + ch0);
 #pragma unroll 1
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
           uint32_t hi[16], lo[16];
           RT_MARK(0);
           ptx::tmem_ld16(tl + col0 + cc, hi);
@@ -662,24 +686,32 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ptx::tmem_wait_ld();
           RT_MARK(2);  // tensor-memory loads
           float bv[16], av[16];
+          const float *sb = &ctl->bias[co_base + ch0 + cc];
+          const float *sa = &ctl->addend[co_base + ch0 + cc];
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
-            *reinterpret_cast<float4 *>(&bv[j]) =
-                *reinterpret_cast<const float4 *>(&ctl->bias[co_base + cc + j]);
-            if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU)
-              *reinterpret_cast<float4 *>(&av[j]) =
-                  *reinterpret_cast<const float4 *>(&ctl->addend[co_base + cc + j]);
+            *reinterpret_cast<float4 *>(&bv[j]) = *reinterpret_cast<const float4 *>(sb + j);
+            if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU)
+              *reinterpret_cast<float4 *>(&av[j]) = *reinterpret_cast<const float4 *>(sa + j);
             else
               av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
           }
-          if (valid) {
+          float *yc = yp + (long)cc * cstride;
+          if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+              *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+              yc += cstride;
+            }
+          } else if (valid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (cc + j < nco) {
                 float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                v = apply_chain<CHAIN>(p.epi, co_base + cc + j, v, av[j]);
-                yp[(long)(cc + j) * cstride] = v;
+                *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
               }
+              yc += cstride;
             }
           }
           RT_MARK(3);  // epilogue math + stores
@@ -691,9 +723,9 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const int c = m;  // one output row per M tile
         const int ow = up.ct * q.WT + c;
         const bool valid = ((c & 1) == 0) && (c + 1 < q.WT) && (ow + 1 < p.Wo);
-        const uint32_t col0 = (uint32_t)(acc * 256);
+        const uint32_t col0 = (uint32_t)(acc * 256 + ch0);
 #pragma unroll 1
-        for (int cc = 0; cc < 64; cc += 16) {
+        for (int cc = 0; cc < 32; cc += 16) {
           uint32_t h0[16], l0[16], h1[16], l1[16];
           ptx::tmem_ld16(tl + col0 + cc, h0);
           ptx::tmem_ld16(tl + col0 + 64 + cc, l0);
@@ -703,8 +735,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           float part[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int co = co_base + cc + j;
-            const float bias = ctl->bias[co];
+            const float bias = ctl->bias[co_base + ch0 + cc + j];
             const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
             const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
             float mx = fmaxf(v0, v1);
@@ -718,7 +749,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             for (int j = 0; j < 16; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
           if (lane == 0)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ctl->red[warp][cc + j] = part[j];
+            for (int j = 0; j < 16; ++j) ctl->red[quad][ch0 + cc + j] = part[j];
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -778,6 +809,8 @@ cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bi
       return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false>(p, q, bimg, partial, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
       return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false>(p, q, bimg, partial, s);
+    case CHAIN_LEAKY_ADD_CLAMP1_GELU:
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false>(p, q, bimg, partial, s);
     default: return launch_kernel<PREC, CHAIN_GENERIC, false>(p, q, bimg, partial, s);
   }
 }
