@@ -100,18 +100,25 @@ struct TcPlan {
   int smem_bytes;
   int off_b, off_bar, off_misc;
   int ncol;  // 32-pixel column groups per staged row
+  int nb;    // staged rows a producer warp loads at once
+  int png;   // producer groups (each fills its own stages)
+  int pgs;   // warps per producer group
   int dbg;  // diagnostics: bit 0 MMA issue from lane 0, bit 1 every lane polls
 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Rows a producer warp loads at once for a row width of ncol 32-pixel
+// groups of e values each (<= 40 values per lane in flight).
+__host__ __device__ constexpr int rows_per_batch(int ncol, int e) {
+  return 40 / (ncol * e) < 1 ? 1 : (40 / (ncol * e) > 4 ? 4 : 40 / (ncol * e));
+}
 
 constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in smem
 
 struct SmemCtl {
   uint32_t tmem_base;
   int abort;
-  uint32_t koff[27];          // byte offset of K step ks's first slice in a stage
-  uint32_t klbo[27];          // byte distance to its second slice
   float red[4][64];           // pool: per-warp partial sums
   float bias[kMaxCoTc];       // bias per output channel (0 without bias)
   float addend[kMaxCoTc];     // per-channel addend of the fused GELU chain
@@ -182,6 +189,22 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.off_misc = q.off_bar + 512;
   q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
+  // Producer groups: group k fills the chunks g with g % png == k, so png
+  // stages fill concurrently; a warp loads nb rows at once (<= 40 values
+  // per lane in flight).  Pick the split that fills chunks fastest.
+  {
+    const int E = q.E;
+    q.nb = rows_per_batch(q.ncol, E);
+    const int jobs = q.P * p.KD * q.RIN;
+    const int pw = kProdThreads / 32;
+    double best = -1.0;
+    for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
+      const int gs = pw / ng;
+      const int rounds = cdiv(jobs, gs * q.nb);
+      const double score = (double)ng / rounds;
+      if (score >= best) { best = score; q.png = ng; q.pgs = gs; }
+    }
+  }
   q.ok = 1;
   return q;
 }
@@ -364,28 +387,61 @@ __device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, co
   }
 }
 
-// One staged row of one slice plane: lanes take pixels cc = lane + 32k,
-// load E input channels per pixel (zero outside the image), split them into
-// hi / lo parts and store the two 16-byte slices.  NCOL = column groups.
+// Staged-pixel shift of tap t = (kd, kh, kw): (kd*RIN + kh)*RS + kw.
+__device__ __forceinline__ int tap_shift(int t, int RIN, int RS) {
+  return ((t / 9) * RIN + (t / 3) % 3) * RS + t % 3;
+}
+
+// Rows a producer warp loads at once for a row width of NCOL 32-pixel
+// groups (<= 40 values per lane in flight); the host plan uses the same rule.
+
+
+struct RowJob {
+  long rowbase;   // element index of (n, channel 0, id, ih, iw0)
+  int cbase;      // first input channel of the slice plane
+  uint32_t dst;   // byte offset of the row in the hi planes of the stage
+  bool ok;        // the input row exists (else zeros)
+};
+
+// NB staged rows of slice planes: lanes take pixels cc = lane + 32k, load E
+// input channels per pixel (zero outside the image), split them into hi /
+// lo parts and store the two 16-byte slices.  All loads of the batch are in
+// flight before the first store.
+template <int PREC, int E, int NCOL, int NB>
+__device__ __forceinline__ void fill_rows(const float *__restrict__ x, const RowJob (&jb)[4],
+                                          int nvalid, long cstride, int iw0, int W, int RS, int C,
+                                          uint8_t *stage, int lo_off, int lane, bool &range_bad) {
+  float v[NB][NCOL][E];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int k = 0; k < NCOL; ++k) {
+      const int cc = lane + 32 * k;
+      const bool colok = b < nvalid && jb[b].ok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        v[b][k][e] = (colok && jb[b].cbase + e < C)
+                         ? __ldg(x + jb[b].rowbase + cc + (long)(jb[b].cbase + e) * cstride)
+                         : 0.0f;
+    }
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+    if (b < nvalid)
+#pragma unroll
+      for (int k = 0; k < NCOL; ++k) {
+        const int cc = lane + 32 * k;
+        if (cc < RS)
+          store_slice<PREC, E>(stage + jb[b].dst + cc * 16, stage + lo_off + jb[b].dst + cc * 16,
+                               v[b][k], range_bad);
+      }
+}
+
 template <int PREC, int E, int NCOL>
-__device__ __forceinline__ void fill_row(const float *__restrict__ x, long rowbase, long cstride,
-                                         int iw0, int W, int RS, bool rowok, int cbase, int C,
-                                         uint8_t *dhi, uint8_t *dlo, int lane, bool &range_bad) {
-  float v[NCOL][E];
-#pragma unroll
-  for (int k = 0; k < NCOL; ++k) {
-    const int cc = lane + 32 * k;
-    const bool colok = rowok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      v[k][e] = (colok && cbase + e < C) ? __ldg(x + rowbase + cc + (long)(cbase + e) * cstride)
-                                         : 0.0f;
-  }
-#pragma unroll
-  for (int k = 0; k < NCOL; ++k) {
-    const int cc = lane + 32 * k;
-    if (cc < RS) store_slice<PREC, E>(dhi + cc * 16, dlo + cc * 16, v[k], range_bad);
-  }
+__device__ __forceinline__ void fill_rows_n(const float *__restrict__ x, const RowJob (&jb)[4],
+                                            int nvalid, long cstride, int iw0, int W, int RS, int C,
+                                            uint8_t *stage, int lo_off, int lane, bool &range_bad) {
+  fill_rows<PREC, E, NCOL, rows_per_batch(NCOL, E)>(x, jb, nvalid, cstride, iw0, W, RS, C, stage,
+                                                    lo_off, lane, range_bad);
 }
 
 template <int PREC, int CHAIN, bool POOL>
@@ -415,7 +471,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 
   if (tid == 0) {
     for (int s = 0; s < q.S; ++s) {
-      ptx::mbar_init(&a_full[s], kProdThreads / 32);
+      ptx::mbar_init(&a_full[s], (uint32_t)q.pgs);
       ptx::mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -429,18 +485,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     ptx::mbar_init(drain, 1);
     ctl->abort = 0;
     ptx::fence_mbar_init();
-  }
-  if (tid < q.KS) {
-    // staged-pixel shift of tap t = (kd, kh, kw): (kd*RIN + kh)*RS + kw
-    auto shift = [&](int t) { return ((t / 9) * q.RIN + (t / 3) % 3) * q.RS + t % 3; };
-    if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last tap)
-      const int t0 = 2 * tid;
-      ctl->koff[tid] = (uint32_t)shift(t0) * 16u;
-      ctl->klbo[tid] = (t0 + 1 < q.TAPS) ? (uint32_t)(shift(t0 + 1) - shift(t0)) * 16u : 16u;
-    } else {           // slices: planes 0 and 1 of tap ks
-      ctl->koff[tid] = (uint32_t)shift(tid) * 16u;
-      ctl->klbo[tid] = (uint32_t)q.plane_bytes;
-    }
   }
   for (int c = tid; c < q.COB * 64; c += kThreads) {
     ctl->bias[c] = (c < p.CO && p.epi.bias) ? p.epi.bias[c] : 0.0f;
@@ -465,7 +509,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // ------------------------------------------------------------ producers
     const int pt = tid - kProdWarp0 * 32;
     bool range_bad = false;
-    uint32_t g = 0, gb = 0;
+    uint32_t g = 0;
     bool ok = true;
     if (q.b_resident && pt == 0) {
       const long total = (long)q.COB * q.NCH * q.b_chunk_bytes;
@@ -488,22 +532,30 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             *reinterpret_cast<uint4 *>(smem + (long)st * q.a_stage_bytes + pl * q.plane_bytes +
                                        px * 16) = make_uint4(0, 0, 0, 0);
     }
+    // Group grp fills the chunks g with g % png == grp; warp wig of the group
+    // takes batches of nb consecutive (plane, row) jobs.
+    const int pw = warp - kProdWarp0;
+    const int grp = pw / q.pgs, wig = pw - grp * q.pgs;
+    const bool active = grp < q.png;
+    uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
     RT_DECL
-    for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    for (long u = blockIdx.x; ok && active && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q, p);
       const int oh0 = up.rt * U * q.R;  // first output row of the unit
       const int ow0 = up.ct * q.WT;
+      const int iw0 = ow0 - p.pad;
       const long xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
+        if ((int)(g % (uint32_t)q.png) != grp) continue;
         const int s = (int)(g % q.S);
         RT_MARK(0);
         if (!wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag, p.status, 0x10000000u | g, q.dbg)) {
           ok = false;
           break;
         }
-        if (!q.b_resident && warp == kProdWarp0) {
-          const int sb = (int)(gb % q.SB);
-          if (!wait_bar_warp(bars, B_EMPTY + sb, ((gb / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | gb, q.dbg)) {
+        if (!q.b_resident && wig == 0) {
+          const int sb = (int)(g % q.SB);
+          if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | g, q.dbg)) {
             ok = false;
             break;
           }
@@ -516,29 +568,40 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               ptx::bulk_g2s(dst + off, src + off, (uint32_t)nb, &b_full[sb]);
             }
           }
-          ++gb;
+          last_b = g;
         }
         RT_MARK(1);  // waiting for a free stage
         uint8_t *stage = smem + (long)s * q.a_stage_bytes;
-        uint8_t *stage_lo = stage + q.P * q.plane_bytes;
+        const int lo_off = q.P * q.plane_bytes;
         const int ci0 = c * q.chunk_ci;
-        for (int job = warp - kProdWarp0; job < jobs; job += kProdThreads / 32) {
-          const int plane = job / nrows;
-          const int sr = job - plane * nrows;
-          const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
-          const int id = up.od + kdp - p.pad_d, ih = oh0 + r - p.pad;
-          const bool rowok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
-          const int cbase = ci0 + plane * E;
-          const int iw0 = ow0 - p.pad;
-          const long rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
-          uint8_t *dhi = stage + plane * q.plane_bytes + sr * q.RS * 16;
-          uint8_t *dlo = stage_lo + plane * q.plane_bytes + sr * q.RS * 16;
+        for (int j0 = wig * q.nb; j0 < jobs; j0 += q.pgs * q.nb) {
+          RowJob jb[4];
+          int nvalid = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int job = j0 + b;
+            jb[b].ok = false;
+            jb[b].rowbase = 0;
+            jb[b].cbase = 0;
+            jb[b].dst = 0;
+            if (b < q.nb && job < jobs) {
+              const int plane = job / nrows;
+              const int sr = job - plane * nrows;
+              const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
+              const int id = up.od + kdp - p.pad_d, ih = oh0 + r - p.pad;
+              jb[b].ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
+              jb[b].rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
+              jb[b].cbase = ci0 + plane * E;
+              jb[b].dst = (uint32_t)(plane * q.plane_bytes + sr * q.RS * 16);
+              nvalid = b + 1;
+            }
+          }
           switch (q.ncol) {
-            case 1: fill_row<PREC, E, 1>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
-            case 2: fill_row<PREC, E, 2>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
-            case 3: fill_row<PREC, E, 3>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
-            case 4: fill_row<PREC, E, 4>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
-            default: fill_row<PREC, E, 5>(p.x, rowbase, cstride, iw0, p.W, q.RS, rowok, cbase, p.C, dhi, dlo, lane, range_bad); break;
+            case 1: fill_rows_n<PREC, E, 1>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 2: fill_rows_n<PREC, E, 2>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 3: fill_rows_n<PREC, E, 3>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 4: fill_rows_n<PREC, E, 4>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            default: fill_rows_n<PREC, E, 5>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
           }
         }
         ptx::fence_proxy_async_smem();
@@ -550,14 +613,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     RT_STORE(warp == kProdWarp0 ? 2 : -1);
     if (range_bad) atomicOr(p.status, ST_RANGE);
     // drain outstanding weight copies before the CTA can exit
-    if (pt == 0) {
-      if (q.b_resident) {
-        wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
-      } else if (gb > 0) {
-        for (uint32_t k = (gb > (uint32_t)q.SB ? gb - q.SB : 0); k < gb; ++k)
-          wait_bar(bars, B_FULL + (int)(k % q.SB), (k / q.SB) & 1, abort_flag, p.status, 0x13000000u | k);
-      }
-    }
+    if (pt == 0 && q.b_resident) wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
+    if (lane == 0 && last_b != 0xffffffffu)
+      wait_bar(bars, B_FULL + (int)(last_b % q.SB), (last_b / q.SB) & 1, abort_flag, p.status,
+               0x13000000u | last_b);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
     // The warp stays converged; every MMA burst and every commit is issued
@@ -603,7 +662,16 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t a_lo = a_hi + (uint32_t)(q.P * q.plane_bytes);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
         for (int ks = 0; ks < q.KS; ++ks) {
-          const uint32_t off0 = ctl->koff[ks], lbo = ctl->klbo[ks];
+          uint32_t off0, lbo;
+          if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
+            const int t0 = 2 * ks;
+            const int s0 = tap_shift(t0, q.RIN, q.RS);
+            off0 = (uint32_t)s0 * 16u;
+            lbo = (t0 + 1 < q.TAPS) ? (uint32_t)(tap_shift(t0 + 1, q.RIN, q.RS) - s0) * 16u : 16u;
+          } else {           // slices: planes 0 and 1 of tap ks
+            off0 = (uint32_t)tap_shift(ks, q.RIN, q.RS) * 16u;
+            lbo = (uint32_t)q.plane_bytes;
+          }
           const uint64_t bdesc = ptx::smem_desc(bbase + (uint32_t)ks * kBStep, 2048, 128);
           const uint32_t accum = (c | ks) != 0;
           uint64_t ah[U], al[U];
