@@ -37,6 +37,7 @@
 // bit, every role drains, and the CTA frees its tensor memory and exits.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdlib.h>
 
 #include "fc_epi.cuh"
@@ -119,10 +120,14 @@ constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in
 struct SmemCtl {
   uint32_t tmem_base;
   int abort;
-  float red[4][64];           // pool: per-warp partial sums
-  float bias[kMaxCoTc];       // bias per output channel (0 without bias)
-  float addend[kMaxCoTc];     // per-channel addend of the fused GELU chain
+  alignas(16) float red[4][64];          // pool: per-warp partial sums
+  alignas(16) float bias[kMaxCoTc];      // bias per output channel (0 without bias)
+  alignas(16) float addend[kMaxCoTc];    // per-channel addend of the fused GELU chain
 };
+// The epilogue reads bias / addend as float4.
+static_assert(offsetof(SmemCtl, bias) % 16 == 0 && offsetof(SmemCtl, addend) % 16 == 0,
+              "16-byte aligned per-channel arrays");
+static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
 TcPlan make_plan(const ConvProblem &p, int prec) {
   TcPlan q{};
@@ -186,7 +191,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.SB = resident ? 1 : SB;
   q.off_b = S * q.a_stage_bytes;
   q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
-  q.off_misc = q.off_bar + 512;
+  q.off_misc = q.off_bar + 512;  // 16-byte aligned: off_b and the B region are
   q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
   // Producer groups: group k fills the chunks g with g % png == k, so png
