@@ -631,24 +631,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
     constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
     const uint32_t sbase = ptx::smem_u32(smem);
-    // Descriptor delta of each K step: start-address field (+ slice-distance
-    // field) of its first A slice relative to the stage start, in 16-byte
-    // units: tap (kd, kh, kw) sits (kd*RIN + kh)*RS + kw pixels in.
-    uint32_t kdelta[27];
-#pragma unroll
-    for (int ks = 0; ks < 27; ++ks) {
-      uint32_t off16, lbo16;
-      if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
-        const int t0 = 2 * ks;
-        const int s0 = tap_shift(t0, q.RIN, q.RS);
-        off16 = (uint32_t)s0;
-        lbo16 = (t0 + 1 < q.TAPS) ? (uint32_t)(tap_shift(t0 + 1, q.RIN, q.RS) - s0) : 1u;
-      } else {           // slices: planes 0 and 1 of tap ks
-        off16 = (uint32_t)tap_shift(ks, q.RIN, q.RS);
-        lbo16 = (uint32_t)(q.plane_bytes >> 4);
-      }
-      kdelta[ks] = (off16 & 0x3FFFu) | ((lbo16 & 0x3FFFu) << 16);
-    }
     const uint32_t lo_delta = (uint32_t)((q.P * q.plane_bytes) >> 4);  // hi -> lo planes
     const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile (pool)
     uint32_t g = 0, gb = 0, it = 0;
@@ -688,29 +670,43 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint64_t a0 = ptx::smem_desc(sbase + (uint32_t)(s * q.a_stage_bytes), 0, 128);
         const uint64_t b0 = ptx::smem_desc(bbase, 2048, 128);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
+        // Walk the taps (kd, kh, kw) with a running staged-pixel offset
+        // (kd*RIN + kh)*RS + kw, in 16-byte units: uniform adds only, so the
+        // descriptors stay on the uniform datapath.
+        int kw = 0, kh = 0;
+        uint32_t shift = 0;
+        const uint32_t plane16 = (uint32_t)(q.plane_bytes >> 4);
+        const uint32_t row_wrap = (uint32_t)(q.RS - 3);
+        const uint32_t depth_wrap = (uint32_t)(q.RIN * q.RS - 3 * q.RS);
+        for (int ks = 0; ks < q.KS; ++ks) {
+          uint32_t s0 = shift, lbo16;
+          // next tap
+          if (++kw == 3) { kw = 0; shift += row_wrap + 1; if (++kh == 3) { kh = 0; shift += depth_wrap; } } else { shift += 1; }
+          if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
+            lbo16 = (2 * ks + 1 < q.TAPS) ? shift - s0 : 1u;
+            if (++kw == 3) { kw = 0; shift += row_wrap + 1; if (++kh == 3) { kh = 0; shift += depth_wrap; } } else { shift += 1; }
+          } else {           // slices: planes 0 and 1 of tap ks
+            lbo16 = plane16;
+          }
+          const uint64_t bdesc = b0 + (uint64_t)(ks * (kBStep >> 4));
+          const uint32_t accum = (c | ks) != 0;
+          const uint64_t ah0 = a0 + (uint64_t)(s0 | (lbo16 << 16));
+          if (ptx::elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < 27; ++ks) {
-          if (ks < q.KS) {
-            const uint64_t bdesc = b0 + (uint64_t)(ks * (kBStep >> 4));
-            const uint32_t accum = (c | ks) != 0;
-            const uint64_t ah0 = a0 + kdelta[ks];
-            if (ptx::elect_one()) {
-#pragma unroll
-              for (int t = 0; t < U; ++t) {
-                const uint64_t ah = ah0 + (uint64_t)(t * tile_delta);
-                const uint64_t al = ah + lo_delta;
-                const uint32_t d = dacc + (uint32_t)(t * 128);
-                if constexpr (PREC == 0) {
-                  ptx::mma_tf32(d, ah, bdesc, idesc1, accum);
-                  ptx::mma_tf32(d + 64, al, bdesc, idesc2, 1u);
-                } else {
-                  ptx::mma_f16(d, ah, bdesc, idesc1, accum);
-                  ptx::mma_f16(d + 64, al, bdesc, idesc2, 1u);
-                }
+            for (int t = 0; t < U; ++t) {
+              const uint64_t ah = ah0 + (uint64_t)(t * tile_delta);
+              const uint64_t al = ah + lo_delta;
+              const uint32_t d = dacc + (uint32_t)(t * 128);
+              if constexpr (PREC == 0) {
+                ptx::mma_tf32(d, ah, bdesc, idesc1, accum);
+                ptx::mma_tf32(d + 64, al, bdesc, idesc2, 1u);
+              } else {
+                ptx::mma_f16(d, ah, bdesc, idesc1, accum);
+                ptx::mma_f16(d + 64, al, bdesc, idesc2, 1u);
               }
             }
-            __syncwarp();
           }
+          __syncwarp();
         }
         if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
