@@ -199,15 +199,22 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   // per lane in flight).  Pick the split that fills chunks fastest.
   {
     const int E = q.E;
-    q.nb = rows_per_batch(q.ncol, E);
+    // Measured on GB300: loading one row per warp pass beats batching rows,
+    // and all producer warps on one stage beat concurrent groups once a
+    // stage holds >= 8 rows; smaller stages gain from concurrent groups.
+    (void)E;
+    q.nb = 1;
     const int jobs = q.P * p.KD * q.RIN;
     const int pw = kProdThreads / 32;
-    double best = -1.0;
-    for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
-      const int gs = pw / ng;
-      const int rounds = cdiv(jobs, gs * q.nb);
-      const double score = (double)ng / rounds;
-      if (score >= best) { best = score; q.png = ng; q.pgs = gs; }
+    q.png = 1;
+    q.pgs = pw;
+    if (jobs < 8) {
+      double best = -1.0;
+      for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
+        const int gs = pw / ng;
+        const double score = (double)ng / cdiv(jobs, gs);
+        if (score > best) { best = score; q.png = ng; q.pgs = gs; }
+      }
     }
   }
   q.ok = 1;
