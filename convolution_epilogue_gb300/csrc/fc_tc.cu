@@ -25,14 +25,14 @@
 // a different descriptor start address, no data movement per tap.  This is
 // the GB300 form of the traces' shared-memory halo tile.
 //
-// Roles (640 threads): warps 0-7 epilogue (warp w: TMEM lanes 32(w%4)..+31,
+// Roles (512 threads): warps 0-7 epilogue (warp w: TMEM lanes 32(w%4)..+31,
 // channels 32(w/4)..+31), warp 8
 // TMEM allocation + MMA issue (the warp runs converged; each burst of MMAs
 // and each commit is issued by the lane elect.sync picks, the same lowest
-// lane every time), warps 9-19 producers (each pass loads a batch of
-// 32-pixel pieces of staged input rows -- 40 values per lane in flight --
-// then splits them into hi/lo parts and stores the slices; one producer lane
-// also streams packed weights with bulk copies).  All waits are
+// lane every time), warps 9-15 producers (one staged input row per warp
+// pass, lanes across its pixels: global loads, hi/lo split, st.shared into
+// the stage ring; one producer lane also streams packed weights with bulk
+// copies).  All waits are
 // bounded (4 s on %globaltimer) and warp-uniform; a timeout sets a status
 // bit, every role drains, and the CTA frees its tensor memory and exits.
 #include <cuda_fp16.h>
@@ -64,11 +64,11 @@ namespace fc {
 
 namespace {
 
-constexpr int kThreads = 640;
+constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 32 channels each
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdThreads = 352;  // 11 producer warps
+constexpr int kProdThreads = 224;  // 7 producer warps
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
@@ -109,11 +109,11 @@ struct TcPlan {
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Pieces a producer warp loads per pass: 40 values per lane for fp16 parts
-// (5 pieces of 8 channels), 24 for tf32 parts (6 pieces of 4 channels).
-__host__ __device__ constexpr int pieces_per_batch(int e) { return e == 8 ? 5 : 6; }
-
-
+// Rows a producer warp loads at once for a row width of ncol 32-pixel
+// groups of e values each (<= 40 values per lane in flight).
+__host__ __device__ constexpr int rows_per_batch(int ncol, int e) {
+  return 40 / (ncol * e) < 1 ? 1 : (40 / (ncol * e) > 4 ? 4 : 40 / (ncol * e));
+}
 
 constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in smem
 
@@ -199,20 +199,23 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   // per lane in flight).  Pick the split that fills chunks fastest.
   {
     const int E = q.E;
-    // A producer job is one 32-pixel piece of one staged row of one slice
-    // plane; a warp pass loads a batch of pieces_per_batch(E) jobs.  Group g fills the chunks with index % png == g: several
-    // groups fill different stages concurrently when that finishes stages
-    // sooner (ties go to fewer groups).
-    const int jobs = q.P * p.KD * q.RIN * q.ncol;
-    const int batches = cdiv(jobs, pieces_per_batch(E));
+    // Measured on GB300: loading one row per warp pass beats batching rows,
+    // and all producer warps on one stage beat concurrent groups once a
+    // stage holds >= 8 rows; smaller stages gain from concurrent groups.
+    (void)E;
+    q.nb = 1;
+    const int jobs = q.P * p.KD * q.RIN;
     const int pw = kProdThreads / 32;
-    double best = -1.0;
-    for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
-      const int gs = pw / ng;
-      const double score = (double)ng / cdiv(batches, gs);
-      if (score > best) { best = score; q.png = ng; q.pgs = gs; }
+    q.png = 1;
+    q.pgs = pw;
+    if (jobs < 8) {
+      double best = -1.0;
+      for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
+        const int gs = pw / ng;
+        const double score = (double)ng / cdiv(jobs, gs);
+        if (score > best) { best = score; q.png = ng; q.pgs = gs; }
+      }
     }
-    q.nb = pieces_per_batch(E);
   }
   q.ok = 1;
   return q;
@@ -405,43 +408,52 @@ __device__ __forceinline__ int tap_shift(int t, int RIN, int RS) {
 // groups (<= 40 values per lane in flight); the host plan uses the same rule.
 
 
-
-
-struct PieceJob {
-  int rowbase;    // element index of (n, channel 0, id, ih, iw0) (tensors < 2^31)
+struct RowJob {
+  long rowbase;   // element index of (n, channel 0, id, ih, iw0)
   int cbase;      // first input channel of the slice plane
-  int col;        // first pixel of the 32-pixel piece
   uint32_t dst;   // byte offset of the row in the hi planes of the stage
   bool ok;        // the input row exists (else zeros)
 };
 
-// NB pieces (32 staged pixels of one row of one slice plane each): lane
-// `lane` owns pixel col + lane of every piece, loads its E input channels
-// (zero outside the image), splits them into hi / lo parts and stores the
-// two 16-byte slices.  All NB * E loads are in flight before the first store.
-template <int PREC, int E, int NB>
-__device__ __forceinline__ void fill_pieces(const float *__restrict__ x, const PieceJob (&jb)[NB],
-                                            int nvalid, long cstride, int iw0, int W, int RS,
-                                            int C, uint8_t *stage, int lo_off, int lane,
-                                            bool &range_bad) {
-  float v[NB][E];
+// NB staged rows of slice planes: lanes take pixels cc = lane + 32k, load E
+// input channels per pixel (zero outside the image), split them into hi /
+// lo parts and store the two 16-byte slices.  All loads of the batch are in
+// flight before the first store.
+template <int PREC, int E, int NCOL, int NB>
+__device__ __forceinline__ void fill_rows(const float *__restrict__ x, const RowJob (&jb)[4],
+                                          int nvalid, long cstride, int iw0, int W, int RS, int C,
+                                          uint8_t *stage, int lo_off, int lane, bool &range_bad) {
+  float v[NB][NCOL][E];
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    const int cc = jb[b].col + lane;
-    const bool colok = b < nvalid && jb[b].ok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
+  for (int b = 0; b < NB; ++b)
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-      v[b][e] = (colok && jb[b].cbase + e < C)
-                    ? __ldg(x + ((long)jb[b].rowbase + cc + (long)(jb[b].cbase + e) * cstride))
-                    : 0.0f;
-  }
+    for (int k = 0; k < NCOL; ++k) {
+      const int cc = lane + 32 * k;
+      const bool colok = b < nvalid && jb[b].ok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    const int cc = jb[b].col + lane;
-    if (b < nvalid && cc < RS)
-      store_slice<PREC, E>(stage + jb[b].dst + cc * 16, stage + lo_off + jb[b].dst + cc * 16,
-                           v[b], range_bad);
-  }
+      for (int e = 0; e < E; ++e)
+        v[b][k][e] = (colok && jb[b].cbase + e < C)
+                         ? __ldg(x + jb[b].rowbase + cc + (long)(jb[b].cbase + e) * cstride)
+                         : 0.0f;
+    }
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+    if (b < nvalid)
+#pragma unroll
+      for (int k = 0; k < NCOL; ++k) {
+        const int cc = lane + 32 * k;
+        if (cc < RS)
+          store_slice<PREC, E>(stage + jb[b].dst + cc * 16, stage + lo_off + jb[b].dst + cc * 16,
+                               v[b][k], range_bad);
+      }
+}
+
+template <int PREC, int E, int NCOL>
+__device__ __forceinline__ void fill_rows_n(const float *__restrict__ x, const RowJob (&jb)[4],
+                                            int nvalid, long cstride, int iw0, int W, int RS, int C,
+                                            uint8_t *stage, int lo_off, int lane, bool &range_bad) {
+  fill_rows<PREC, E, NCOL, rows_per_batch(NCOL, E)>(x, jb, nvalid, cstride, iw0, W, RS, C, stage,
+                                                    lo_off, lane, range_bad);
 }
 
 template <int PREC, int CHAIN, bool POOL>
@@ -520,7 +532,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     const int nrows = p.KD * q.RIN;  // staged rows per slice plane
-    const int pjobs = q.P * nrows * q.ncol;  // 32-pixel pieces per stage
+    const int jobs = q.P * nrows;     // (plane, staged row) pairs per stage
     const long cstride = (long)p.D * HW;
     // Pixels past the staged rows are only read by discarded M rows; zero
     // them once so those rows stay finite.
@@ -574,35 +586,35 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         uint8_t *stage = smem + (long)s * q.a_stage_bytes;
         const int lo_off = q.P * q.plane_bytes;
         const int ci0 = c * q.chunk_ci;
-        constexpr int NB = pieces_per_batch(E);
-        for (int j0 = wig * NB; j0 < pjobs; j0 += q.pgs * NB) {
-          PieceJob jb[NB];
+        for (int j0 = wig * q.nb; j0 < jobs; j0 += q.pgs * q.nb) {
+          RowJob jb[4];
           int nvalid = 0;
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
+          for (int b = 0; b < 4; ++b) {
             const int job = j0 + b;
             jb[b].ok = false;
             jb[b].rowbase = 0;
             jb[b].cbase = 0;
-            jb[b].col = 0;
             jb[b].dst = 0;
-            if (job < pjobs) {
-              const int row_job = job / q.ncol;          // (plane, staged row)
-              const int piece = job - row_job * q.ncol;  // 32-pixel piece of the row
-              const int plane = row_job / nrows;
-              const int sr = row_job - plane * nrows;
+            if (b < q.nb && job < jobs) {
+              const int plane = job / nrows;
+              const int sr = job - plane * nrows;
               const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
               const int id = up.od + kdp - p.pad_d, ih = oh0 + r - p.pad;
               jb[b].ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
-              jb[b].rowbase = (int)(xn + (long)id * HW + (long)ih * p.W + iw0);
+              jb[b].rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
               jb[b].cbase = ci0 + plane * E;
-              jb[b].col = piece * 32;
               jb[b].dst = (uint32_t)(plane * q.plane_bytes + sr * q.RS * 16);
               nvalid = b + 1;
             }
           }
-          fill_pieces<PREC, E, NB>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off,
-                                   lane, range_bad);
+          switch (q.ncol) {
+            case 1: fill_rows_n<PREC, E, 1>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 2: fill_rows_n<PREC, E, 2>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 3: fill_rows_n<PREC, E, 3>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            case 4: fill_rows_n<PREC, E, 4>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+            default: fill_rows_n<PREC, E, 5>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
+          }
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
