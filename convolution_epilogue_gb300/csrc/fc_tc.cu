@@ -120,6 +120,7 @@ constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in
 struct SmemCtl {
   uint32_t tmem_base;
   int abort;
+  uint32_t kdelta[28];  // per K step: A start (16-byte units) | slice distance << 16
   alignas(16) float red[4][64];          // pool: per-warp partial sums
   alignas(16) float bias[kMaxCoTc];      // bias per output channel (0 without bias)
   alignas(16) float addend[kMaxCoTc];    // per-channel addend of the fused GELU chain
@@ -498,6 +499,21 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
+  if (tid < q.KS) {
+    uint32_t off16, lbo16;
+    if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
+      const int t0 = 2 * tid;
+      const int s0 = tap_shift(t0, q.RIN, q.RS);
+      off16 = (uint32_t)s0;
+      lbo16 = (t0 + 1 < q.TAPS) ? (uint32_t)(tap_shift(t0 + 1, q.RIN, q.RS) - s0) : 1u;
+    } else {           // slices: planes 0 and 1 of tap ks
+      off16 = (uint32_t)tap_shift(tid, q.RIN, q.RS);
+      lbo16 = (uint32_t)(q.plane_bytes >> 4);
+    }
+    ctl->kdelta[tid] = (off16 & 0x3FFFu) | ((lbo16 & 0x3FFFu) << 16);
+  } else if (tid < 28) {
+    ctl->kdelta[tid] = 0;  // read (unused) by the last step's prefetch
+  }
   for (int c = tid; c < q.COB * 64; c += kThreads) {
     ctl->bias[c] = (c < p.CO && p.epi.bias) ? p.epi.bias[c] : 0.0f;
     ctl->addend[c] = ((CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU ||
@@ -677,27 +693,16 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint64_t a0 = ptx::smem_desc(sbase + (uint32_t)(s * q.a_stage_bytes), 0, 128);
         const uint64_t b0 = ptx::smem_desc(bbase, 2048, 128);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
-        // Walk the taps (kd, kh, kw) with a running staged-pixel offset
-        // (kd*RIN + kh)*RS + kw, in 16-byte units: uniform adds only, so the
-        // descriptors stay on the uniform datapath.
-        int kw = 0, kh = 0;
-        uint32_t shift = 0;
-        const uint32_t plane16 = (uint32_t)(q.plane_bytes >> 4);
-        const uint32_t row_wrap = (uint32_t)(q.RS - 3);
-        const uint32_t depth_wrap = (uint32_t)(q.RIN * q.RS - 3 * q.RS);
+        // Per-K-step descriptor deltas come from a table in shared memory; the
+        // next step's entry is loaded while this step's MMAs are issued.
+        const volatile uint32_t *kd_tab = ctl->kdelta;
+        uint32_t kd_next = kd_tab[0];
         for (int ks = 0; ks < q.KS; ++ks) {
-          uint32_t s0 = shift, lbo16;
-          // next tap
-          if (++kw == 3) { kw = 0; shift += row_wrap + 1; if (++kh == 3) { kh = 0; shift += depth_wrap; } } else { shift += 1; }
-          if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
-            lbo16 = (2 * ks + 1 < q.TAPS) ? shift - s0 : 1u;
-            if (++kw == 3) { kw = 0; shift += row_wrap + 1; if (++kh == 3) { kh = 0; shift += depth_wrap; } } else { shift += 1; }
-          } else {           // slices: planes 0 and 1 of tap ks
-            lbo16 = plane16;
-          }
+          const uint32_t kd_cur = kd_next;
+          kd_next = kd_tab[ks + 1];
           const uint64_t bdesc = b0 + (uint64_t)(ks * (kBStep >> 4));
           const uint32_t accum = (c | ks) != 0;
-          const uint64_t ah0 = a0 + (uint64_t)(s0 | (lbo16 << 16));
+          const uint64_t ah0 = a0 + (uint64_t)kd_cur;
           if (ptx::elect_one()) {
 #pragma unroll
             for (int t = 0; t < U; ++t) {
