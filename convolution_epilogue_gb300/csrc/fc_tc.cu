@@ -200,7 +200,8 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   // per lane in flight).  Pick the split that fills chunks fastest.
   {
     const int E = q.E;
-    // Measured on GB300: loading one row per warp pass beats batching rows,
+    // Measured on GB300: loading one row per warp pass beats batching rows
+    // (the fill always loads one row per pass),
     // and all producer warps on one stage beat concurrent groups once a
     // stage holds >= 8 rows; smaller stages gain from concurrent groups.
     (void)E;
@@ -453,8 +454,8 @@ template <int PREC, int E, int NCOL>
 __device__ __forceinline__ void fill_rows_n(const float *__restrict__ x, const RowJob (&jb)[4],
                                             int nvalid, long cstride, int iw0, int W, int RS, int C,
                                             uint8_t *stage, int lo_off, int lane, bool &range_bad) {
-  fill_rows<PREC, E, NCOL, rows_per_batch(NCOL, E)>(x, jb, nvalid, cstride, iw0, W, RS, C, stage,
-                                                    lo_off, lane, range_bad);
+  fill_rows<PREC, E, NCOL, 1>(x, jb, nvalid, cstride, iw0, W, RS, C, stage, lo_off, lane,
+                              range_bad);
 }
 
 template <int PREC, int CHAIN, bool POOL>
