@@ -109,12 +109,6 @@ struct TcPlan {
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Rows a producer warp loads at once for a row width of ncol 32-pixel
-// groups of e values each (<= 40 values per lane in flight).
-__host__ __device__ constexpr int rows_per_batch(int ncol, int e) {
-  return 40 / (ncol * e) < 1 ? 1 : (40 / (ncol * e) > 4 ? 4 : 40 / (ncol * e));
-}
-
 constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in smem
 
 struct SmemCtl {
