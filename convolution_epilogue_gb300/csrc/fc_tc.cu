@@ -104,7 +104,6 @@ struct TcPlan {
   int nb;    // staged rows a producer warp loads at once
   int png;   // producer groups (each fills its own stages)
   int pgs;   // warps per producer group
-  int dbg;  // diagnostics: bit 0 MMA issue from lane 0, bit 1 every lane polls
 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -269,11 +268,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parit
 // warp never splits around .sync.aligned instructions or named barriers.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t parity,
                                               volatile int *abort, unsigned int *status,
-                                              uint32_t tag, int dbg = 0) {
-  if (dbg & 2) {
-    const int okl = wait_bar(bars, idx, parity, abort, status, tag) ? 1 : 0;
-    return __all_sync(0xffffffffu, okl) != 0;
-  }
+                                              uint32_t tag) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = wait_bar(bars, idx, parity, abort, status, tag) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -572,13 +567,13 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         if ((int)(g % (uint32_t)q.png) != grp) continue;
         const int s = (int)(g % q.S);
         RT_MARK(0);
-        if (!wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag, p.status, 0x10000000u | g, q.dbg)) {
+        if (!wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag, p.status, 0x10000000u | g)) {
           ok = false;
           break;
         }
         if (!q.b_resident && wig == 0) {
           const int sb = (int)(g % q.SB);
-          if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | g, q.dbg)) {
+          if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | g)) {
             ok = false;
             break;
           }
@@ -654,18 +649,18 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     uint32_t g = 0, gb = 0, it = 0;
     bool ok = true;
     RT_DECL
-    if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u, q.dbg);
+    if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)(u / ((long)p.N * p.Do * q.n_rt * q.n_ct));
       const int acc = (int)(it % q.NACC);
       RT_MARK(0);
-      if (!wait_bar_warp(bars, ACC_EMPTY + acc, ((it / q.NACC) & 1) ^ 1, abort_flag, p.status, 0x21000000u | it, q.dbg)) break;
+      if (!wait_bar_warp(bars, ACC_EMPTY + acc, ((it / q.NACC) & 1) ^ 1, abort_flag, p.status, 0x21000000u | it)) break;
       ptx::tc_fence_after();
       RT_MARK(1);  // waiting for a free accumulator
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = (int)(g % q.S);
         RT_MARK(0);
-        if (!wait_bar_warp(bars, A_FULL + s, (g / q.S) & 1, abort_flag, p.status, 0x22000000u | g, q.dbg)) {
+        if (!wait_bar_warp(bars, A_FULL + s, (g / q.S) & 1, abort_flag, p.status, 0x22000000u | g)) {
           ok = false;
           break;
         }
@@ -675,7 +670,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           bbase = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
         } else {
           sb = (int)(gb % q.SB);
-          if (!wait_bar_warp(bars, B_FULL + sb, (gb / q.SB) & 1, abort_flag, p.status, 0x23000000u | gb, q.dbg)) {
+          if (!wait_bar_warp(bars, B_FULL + sb, (gb / q.SB) & 1, abort_flag, p.status, 0x23000000u | gb)) {
             ok = false;
             break;
           }
@@ -730,7 +725,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // wait until every MMA this warp issued has completed
     if (ptx::elect_one()) ptx::tc_commit(drain);
     __syncwarp();
-    wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u, q.dbg);
+    wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u);
     RT_MARK(4);
     RT_STORE(1);
   } else {
@@ -746,7 +741,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       const UnitPos up = decode_unit(u, q, p);
       const int acc = (int)(it % q.NACC);
       RT_MARK(0);
-      bool okw = wait_bar_warp(bars, ACC_FULL + acc, (it / q.NACC) & 1, abort_flag, p.status, 0x30000000u | it, q.dbg);
+      bool okw = wait_bar_warp(bars, ACC_FULL + acc, (it / q.NACC) & 1, abort_flag, p.status, 0x30000000u | it);
       if constexpr (POOL) okw = epi_all(okw);
       if (!okw) break;
       ptx::tc_fence_after();
@@ -932,7 +927,6 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
                       cudaStream_t s, int *launches) {
   TcPlan q = make_plan(p, prec);
   if (!q.ok) return cudaErrorNotSupported;
-  if (const char *e = getenv("FC_TC_DEBUG")) q.dbg = atoi(e);
   uint8_t *bimg = static_cast<uint8_t *>(ws) + L.tc_w;
   float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
   const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
