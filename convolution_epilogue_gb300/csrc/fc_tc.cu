@@ -68,7 +68,8 @@ constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 32 channels each
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdThreads = 224;  // 7 producer warps
+constexpr int kProdWarps = 7;
+constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
@@ -100,10 +101,6 @@ struct TcPlan {
   long units;
   int smem_bytes;
   int off_b, off_bar, off_misc;
-  int ncol;  // 32-pixel column groups per staged row
-  int nb;    // staged rows a producer warp loads at once
-  int png;   // producer groups (each fills its own stages)
-  int pgs;   // warps per producer group
 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -151,7 +148,6 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
     q.R = 1;
   }
   q.RIN = q.U * q.R + 2;
-  q.ncol = cdiv(q.RS, 32);
   // last staged pixel any MMA can touch (+1 for the paired-tap slice)
   const int maxread = ((p.KD - 1) * q.RIN + 2) * q.RS + 2 + (q.U - 1) * q.R * q.RS + 127 + 1;
   int npix = maxread + 1;
@@ -188,30 +184,6 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.off_misc = q.off_bar + 512;  // 16-byte aligned: off_b and the B region are
   q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
-  // Producer groups: group k fills the chunks g with g % png == k, so png
-  // stages fill concurrently; a warp loads nb rows at once (<= 40 values
-  // per lane in flight).  Pick the split that fills chunks fastest.
-  {
-    const int E = q.E;
-    // Measured on GB300: loading one row per warp pass beats batching rows
-    // (the fill always loads one row per pass),
-    // and all producer warps on one stage beat concurrent groups once a
-    // stage holds >= 8 rows; smaller stages gain from concurrent groups.
-    (void)E;
-    q.nb = 1;
-    const int jobs = q.P * p.KD * q.RIN;
-    const int pw = kProdThreads / 32;
-    q.png = 1;
-    q.pgs = pw;
-    if (jobs < 8) {
-      double best = -1.0;
-      for (int ng = 1; ng <= pw && ng <= q.S; ++ng) {
-        const int gs = pw / ng;
-        const double score = (double)ng / cdiv(jobs, gs);
-        if (score > best) { best = score; q.png = ng; q.pgs = gs; }
-      }
-    }
-  }
   q.ok = 1;
   return q;
 }
@@ -361,33 +333,34 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
   }
 }
 
+// Splits E input channels of one pixel into hi / lo parts and stores the
+// two 16-byte slices.  fp16: hi = rn(v), lo = rn((v - hi) * 2^11), and |v|
+// is folded into `amax` for the range check; tf32: hi = rna(v),
+// lo = rna(v - hi).
 template <int PREC, int E>
 __device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, const float (&v)[E],
-                                            bool &range_bad) {
+                                            float &amax) {
+  uint32_t h[4], l[4];
   if constexpr (PREC == 0) {
-    uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       h[e] = tf32_rna(v[e]);
       l[e] = tf32_rna(v[e] - __uint_as_float(h[e]));
     }
-    *reinterpret_cast<uint4 *>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
   } else {
-    uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float a = v[2 * e], b = v[2 * e + 1];
-      range_bad |= f16_out_of_range(a) || f16_out_of_range(b);
-      const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
-      const __half la = __float2half_rn((a - __half2float(ha)) * 2048.0f);
-      const __half lb = __float2half_rn((b - __half2float(hb)) * 2048.0f);
-      h[e] = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
-      l[e] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+      amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));  // NaN is not flagged
+      h[e] = ptx::cvt_f16x2(a, b);
+      float ha, hb, da, db;
+      ptx::f16x2_to_f32(h[e], ha, hb);
+      ptx::sub_mul_f32x2(a, b, ha, hb, 2048.0f, da, db);
+      l[e] = ptx::cvt_f16x2(da, db);
     }
-    *reinterpret_cast<uint4 *>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
   }
+  *reinterpret_cast<uint4 *>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Staged-pixel shift of tap t = (kd, kh, kw): (kd*RIN + kh)*RS + kw.
@@ -395,10 +368,7 @@ __device__ __forceinline__ int tap_shift(int t, int RIN, int RS) {
   return ((t / 9) * RIN + (t / 3) % 3) * RS + t % 3;
 }
 
-// Rows a producer warp loads at once for a row width of NCOL 32-pixel
-// groups (<= 40 values per lane in flight); the host plan uses the same rule.
-
-
+// One staged row of one slice plane.
 struct RowJob {
   long rowbase;   // element index of (n, channel 0, id, ih, iw0)
   int cbase;      // first input channel of the slice plane
@@ -406,45 +376,55 @@ struct RowJob {
   bool ok;        // the input row exists (else zeros)
 };
 
-// NB staged rows of slice planes: lanes take pixels cc = lane + 32k, load E
-// input channels per pixel (zero outside the image), split them into hi /
-// lo parts and store the two 16-byte slices.  All loads of the batch are in
-// flight before the first store.
-template <int PREC, int E, int NCOL, int NB>
-__device__ __forceinline__ void fill_rows(const float *__restrict__ x, const RowJob (&jb)[4],
-                                          int nvalid, long cstride, int iw0, int W, int RS, int C,
-                                          uint8_t *stage, int lo_off, int lane, bool &range_bad) {
-  float v[NB][NCOL][E];
-#pragma unroll
-  for (int b = 0; b < NB; ++b)
-#pragma unroll
-    for (int k = 0; k < NCOL; ++k) {
-      const int cc = lane + 32 * k;
-      const bool colok = b < nvalid && jb[b].ok && cc < RS && iw0 + cc >= 0 && iw0 + cc < W;
-#pragma unroll
-      for (int e = 0; e < E; ++e)
-        v[b][k][e] = (colok && jb[b].cbase + e < C)
-                         ? __ldg(x + jb[b].rowbase + cc + (long)(jb[b].cbase + e) * cstride)
-                         : 0.0f;
-    }
-#pragma unroll
-  for (int b = 0; b < NB; ++b)
-    if (b < nvalid)
-#pragma unroll
-      for (int k = 0; k < NCOL; ++k) {
-        const int cc = lane + 32 * k;
-        if (cc < RS)
-          store_slice<PREC, E>(stage + jb[b].dst + cc * 16, stage + lo_off + jb[b].dst + cc * 16,
-                               v[b][k], range_bad);
-      }
+// Where the stage's rows come from: unit position, first channel of the
+// chunk and the staging geometry.
+struct StageSrc {
+  long xn;        // element index of image n
+  int od, oh0, iw0, ci0;
+};
+
+__device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, const TcPlan &q,
+                                          const ConvProblem &p, int nrows, int E) {
+  RowJob jb;
+  const int plane = job / nrows;
+  const int sr = job - plane * nrows;
+  const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
+  const int id = ss.od + kdp - p.pad_d, ih = ss.oh0 + r - p.pad;
+  jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
+  jb.rowbase = ss.xn + ((long)id * p.H + ih) * p.W + ss.iw0;
+  jb.cbase = ss.ci0 + plane * E;
+  jb.dst = (uint32_t)(plane * q.plane_bytes + sr * q.RS * 16);
+  return jb;
 }
 
-template <int PREC, int E, int NCOL>
-__device__ __forceinline__ void fill_rows_n(const float *__restrict__ x, const RowJob (&jb)[4],
-                                            int nvalid, long cstride, int iw0, int W, int RS, int C,
-                                            uint8_t *stage, int lo_off, int lane, bool &range_bad) {
-  fill_rows<PREC, E, NCOL, 1>(x, jb, nvalid, cstride, iw0, W, RS, C, stage, lo_off, lane,
-                              range_bad);
+// Loads E channels of staged pixel cc of a row (zero outside the image).
+template <int E>
+__device__ __forceinline__ void load_pixel(const float *__restrict__ x, const RowJob &jb, int cc,
+                                           long cstride, int iw0, int W, int C, float (&v)[E]) {
+  const bool colok = jb.ok && iw0 + cc >= 0 && iw0 + cc < W;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    v[e] = (colok && jb.cbase + e < C) ? __ldg(x + jb.rowbase + cc + (long)(jb.cbase + e) * cstride)
+                                        : 0.0f;
+}
+
+// Main job: pixels cc = lane + 32k (k < NCOL) of one row, all loads in
+// flight before the first store.  `wait_stage` runs between the loads and
+// the stores (the stage may still be in use while the loads travel).
+template <int PREC, int E, int NCOL, class Wait>
+__device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJob &jb, long cstride,
+                                         int iw0, int W, int C, uint8_t *stage, int lo_off, int lane,
+                                         float &amax, Wait &&wait_stage) {
+  float v[NCOL][E];
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) load_pixel<E>(x, jb, lane + 32 * k, cstride, iw0, W, C, v[k]);
+  if (!wait_stage()) return false;
+#pragma unroll
+  for (int k = 0; k < NCOL; ++k) {
+    const uint32_t o = jb.dst + (uint32_t)(lane + 32 * k) * 16u;
+    store_slice<PREC, E>(stage + o, stage + lo_off + o, v[k], amax);
+  }
+  return true;
 }
 
 template <int PREC, int CHAIN, bool POOL>
@@ -474,7 +454,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 
   if (tid == 0) {
     for (int s = 0; s < q.S; ++s) {
-      ptx::mbar_init(&a_full[s], (uint32_t)q.pgs);
+      ptx::mbar_init(&a_full[s], (uint32_t)kProdWarps);
       ptx::mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -526,7 +506,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ producers
     const int pt = tid - kProdWarp0 * 32;
-    bool range_bad = false;
+    const int pw = warp - kProdWarp0;  // producer warp index
+    float amax = 0.0f;                 // largest |x| staged (fp16 range check)
     uint32_t g = 0;
     bool ok = true;
     if (q.b_resident && pt == 0) {
@@ -540,6 +521,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const int nrows = p.KD * q.RIN;  // staged rows per slice plane
     const int jobs = q.P * nrows;     // (plane, staged row) pairs per stage
     const long cstride = (long)p.D * HW;
+    // A stage is filled by main jobs (one row: its full 32-pixel column
+    // groups) and tail jobs (32 of the rows' remaining pixels each).
+    const int ncm = q.RS >> 5;
+    const int tail = q.RS - 32 * ncm;
+    const int mjobs = ncm ? jobs : 0;
+    const int njobs = mjobs + cdiv(jobs * tail, 32);
     // Pixels past the staged rows are only read by discarded M rows; zero
     // them once so those rows stay finite.
     {
@@ -550,28 +537,24 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             *reinterpret_cast<uint4 *>(smem + (long)st * q.a_stage_bytes + pl * q.plane_bytes +
                                        px * 16) = make_uint4(0, 0, 0, 0);
     }
-    // Group grp fills the chunks g with g % png == grp; warp wig of the group
-    // takes batches of nb consecutive (plane, row) jobs.
-    const int pw = warp - kProdWarp0;
-    const int grp = pw / q.pgs, wig = pw - grp * q.pgs;
-    const bool active = grp < q.png;
+    // Job J of a stage goes to producer warp (rot + J) % kProdWarps, where
+    // rot counts the jobs of all earlier stages: the remainder of
+    // njobs / kProdWarps moves round the warps instead of always landing on
+    // the first ones.
+    int rot = 0;
     uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
     RT_DECL
-    for (long u = blockIdx.x; ok && active && u < units; u += gridDim.x) {
+    for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q, p);
-      const int oh0 = up.rt * U * q.R;  // first output row of the unit
-      const int ow0 = up.ct * q.WT;
-      const int iw0 = ow0 - p.pad;
-      const long xn = (long)up.n * p.C * p.D * HW;
+      StageSrc ss;
+      ss.od = up.od;
+      ss.oh0 = up.rt * U * q.R;  // first output row of the unit
+      ss.iw0 = up.ct * q.WT - p.pad;
+      ss.xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
-        if ((int)(g % (uint32_t)q.png) != grp) continue;
         const int s = (int)(g % q.S);
         RT_MARK(0);
-        if (!wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag, p.status, 0x10000000u | g)) {
-          ok = false;
-          break;
-        }
-        if (!q.b_resident && wig == 0) {
+        if (!q.b_resident && pw == 0) {
           const int sb = (int)(g % q.SB);
           if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | g)) {
             ok = false;
@@ -588,40 +571,56 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           }
           last_b = g;
         }
-        RT_MARK(1);  // waiting for a free stage
         uint8_t *stage = smem + (long)s * q.a_stage_bytes;
         const int lo_off = q.P * q.plane_bytes;
-        const int ci0 = c * q.chunk_ci;
-        for (int j0 = wig * q.nb; j0 < jobs; j0 += q.pgs * q.nb) {
-          RowJob jb[4];
-          int nvalid = 0;
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int job = j0 + b;
-            jb[b].ok = false;
-            jb[b].rowbase = 0;
-            jb[b].cbase = 0;
-            jb[b].dst = 0;
-            if (b < q.nb && job < jobs) {
-              const int plane = job / nrows;
-              const int sr = job - plane * nrows;
-              const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
-              const int id = up.od + kdp - p.pad_d, ih = oh0 + r - p.pad;
-              jb[b].ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
-              jb[b].rowbase = xn + (long)id * HW + (long)ih * p.W + iw0;
-              jb[b].cbase = ci0 + plane * E;
-              jb[b].dst = (uint32_t)(plane * q.plane_bytes + sr * q.RS * 16);
-              nvalid = b + 1;
+        ss.ci0 = c * q.chunk_ci;
+        // the stage is free once the MMAs that read it S chunks ago are done;
+        // a warp's first loads of the stage are issued before it waits
+        bool waited = false;
+        auto wait_stage = [&]() -> bool {
+          if (waited) return true;
+          waited = true;
+          RT_MARK(2);
+          const bool w = wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag,
+                                       p.status, 0x10000000u | g);
+          RT_MARK(1);
+          return w;
+        };
+        int J = pw - rot;
+        if (J < 0) J += kProdWarps;
+        for (; ok && J < njobs; J += kProdWarps) {
+          if (J < mjobs) {
+            const RowJob jb = row_job(J, ss, q, p, nrows, E);
+            switch (ncm) {
+              case 1: ok = fill_row<PREC, E, 1>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
+              case 2: ok = fill_row<PREC, E, 2>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
+              case 3: ok = fill_row<PREC, E, 3>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
+              default: ok = fill_row<PREC, E, 4>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
+            }
+          } else {
+            // lane -> (row job, tail pixel) pair
+            const int l = (J - mjobs) * 32 + lane;
+            const int job = l / tail;
+            const int cc = 32 * ncm + (l - job * tail);
+            float v[E];
+            RowJob jb;
+            if (job < jobs) {
+              jb = row_job(job, ss, q, p, nrows, E);
+              load_pixel<E>(p.x, jb, cc, cstride, ss.iw0, p.W, p.C, v);
+            }
+            ok = wait_stage();
+            if (ok && job < jobs) {
+              const uint32_t o = jb.dst + (uint32_t)cc * 16u;
+              store_slice<PREC, E>(stage + o, stage + lo_off + o, v, amax);
             }
           }
-          switch (q.ncol) {
-            case 1: fill_rows_n<PREC, E, 1>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
-            case 2: fill_rows_n<PREC, E, 2>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
-            case 3: fill_rows_n<PREC, E, 3>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
-            case 4: fill_rows_n<PREC, E, 4>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
-            default: fill_rows_n<PREC, E, 5>(p.x, jb, nvalid, cstride, iw0, p.W, q.RS, p.C, stage, lo_off, lane, range_bad); break;
-          }
         }
+        if (!ok || !wait_stage()) {
+          ok = false;
+          break;
+        }
+        rot += njobs % kProdWarps;
+        if (rot >= kProdWarps) rot -= kProdWarps;
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&a_full[s]);
@@ -629,7 +628,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     RT_STORE(warp == kProdWarp0 ? 2 : -1);
-    if (range_bad) atomicOr(p.status, ST_RANGE);
+    if (amax > 65504.0f) atomicOr(p.status, ST_RANGE);
     // drain outstanding weight copies before the CTA can exit
     if (pt == 0 && q.b_resident) wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
     if (lane == 0 && last_b != 0xffffffffu)

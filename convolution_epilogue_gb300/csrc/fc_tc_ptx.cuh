@@ -95,6 +95,34 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------ packed conversions
+// Two fp32 -> fp16x2, round to nearest even; `a` lands in the low half.
+__device__ __forceinline__ uint32_t cvt_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// fp16x2 -> two fp32 (exact); the low half goes to `a`.
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h, float &a, float &b) {
+  asm("{\n\t.reg .f16 l, u;\n\tmov.b32 {l, u}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(h));
+}
+
+// ((a - c) * s, (b - d) * s) on the paired fp32 pipe.
+__device__ __forceinline__ void sub_mul_f32x2(float a, float b, float c, float d, float s,
+                                              float &x, float &y) {
+  uint64_t ab, cd, ss, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(cd) : "f"(c), "f"(d));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ab), "l"(cd));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(r) : "l"(ss));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
