@@ -76,6 +76,33 @@ constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr uint32_t kSleepHintNs = 20000;  // hardware sleep per poll while waiting
 constexpr unsigned int kWaitRecords = 32;  // diagnostic records kept after the status word
 
+// Division of 0 <= n < 2^31 by a divisor fixed at plan time, as a
+// multiply-high, add and shift (the round-up method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(m, n) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = (uint32_t)(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+  return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+#ifdef __CUDA_ARCH__
+  const uint32_t hi = __umulhi(n, f.m);
+#else
+  const uint32_t hi = (uint32_t)(((uint64_t)n * f.m) >> 32);
+#endif
+  return (hi + n) >> f.l;
+}
+
 struct TcPlan {
   int ok;
   int prec;       // 0 tf32, 1 f16
@@ -99,6 +126,7 @@ struct TcPlan {
   int tmem_cols;
   int n_rt, n_ct;
   long units;
+  FastDiv fd_ct, fd_rt, fd_do, fd_n, fd_cb;  // unit index -> position
   int smem_bytes;
   int off_b, off_bar, off_misc;
 };
@@ -160,6 +188,12 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.b_chunk_bytes = q.KS * kBStep;
   q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
+  if (q.units >= (1L << 31)) return q;  // unit indices are 32-bit
+  q.fd_ct = make_fastdiv((uint32_t)q.n_ct);
+  q.fd_rt = make_fastdiv((uint32_t)q.n_rt);
+  q.fd_do = make_fastdiv((uint32_t)p.Do);
+  q.fd_n = make_fastdiv((uint32_t)p.N);
+  q.fd_cb = make_fastdiv((uint32_t)((long)p.N * p.Do * q.n_rt * q.n_ct));
   q.NACC = p.pool ? 2 : 4;
   q.tmem_cols = q.NACC * q.U * 128;
   if (q.tmem_cols > 512) return q;
@@ -266,13 +300,13 @@ struct UnitPos {
   int cb, n, od, rt, ct;
 };
 
-__device__ __forceinline__ UnitPos decode_unit(long u, const TcPlan &q, const ConvProblem &p) {
+__device__ __forceinline__ UnitPos decode_unit(long unit, const TcPlan &q) {
   UnitPos r;
-  r.ct = (int)(u % q.n_ct); u /= q.n_ct;
-  r.rt = (int)(u % q.n_rt); u /= q.n_rt;
-  r.od = (int)(u % p.Do); u /= p.Do;
-  r.n = (int)(u % p.N); u /= p.N;
-  r.cb = (int)u;
+  uint32_t u = (uint32_t)unit, t;
+  t = fdiv(u, q.fd_ct); r.ct = (int)(u - t * q.fd_ct.d); u = t;
+  t = fdiv(u, q.fd_rt); r.rt = (int)(u - t * q.fd_rt.d); u = t;
+  t = fdiv(u, q.fd_do); r.od = (int)(u - t * q.fd_do.d); u = t;
+  t = fdiv(u, q.fd_n); r.n = (int)(u - t * q.fd_n.d); r.cb = (int)t;
   return r;
 }
 
@@ -386,9 +420,11 @@ struct StageSrc {
 __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, const TcPlan &q,
                                           const ConvProblem &p, int nrows, int E) {
   RowJob jb;
-  const int plane = job / nrows;
+  // a stage holds at most 2 slice planes of at most 3 depth slices
+  const int plane = job >= nrows ? 1 : 0;
   const int sr = job - plane * nrows;
-  const int kdp = sr / q.RIN, r = sr - kdp * q.RIN;
+  const int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
+  const int r = sr - kdp * q.RIN;
   const int id = ss.od + kdp - p.pad_d, ih = ss.oh0 + r - p.pad;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
   jb.rowbase = ss.xn + ((long)id * p.H + ih) * p.W + ss.iw0;
@@ -425,6 +461,22 @@ __device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJ
     store_slice<PREC, E>(stage + o, stage + lo_off + o, v[k], amax);
   }
   return true;
+}
+
+// Sums v[0..15] over the 32 lanes of a warp: after the call lane l holds in
+// v[0] the total of the value v[(l >> 1) & 15] had on every lane.
+__device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int h = 8, o = 16; h >= 1; h >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 template <int PREC, int CHAIN, bool POOL>
@@ -545,7 +597,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
     RT_DECL
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const UnitPos up = decode_unit(u, q, p);
+      const UnitPos up = decode_unit(u, q);
       StageSrc ss;
       ss.od = up.od;
       ss.oh0 = up.rt * U * q.R;  // first output row of the unit
@@ -650,7 +702,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     RT_DECL
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
-      const int cb = (int)(u / ((long)p.N * p.Do * q.n_rt * q.n_ct));
+      const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
       const int acc = (int)(it % q.NACC);
       RT_MARK(0);
       if (!wait_bar_warp(bars, ACC_EMPTY + acc, ((it / q.NACC) & 1) ^ 1, abort_flag, p.status, 0x21000000u | it)) break;
@@ -733,11 +785,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // channel half w / 4 (32 of the 64 channels).
     const int quad = warp & 3, half = warp >> 2;
     const int m = quad * 32 + lane;  // TMEM lane = M row = output pixel
+    const int m_row = m / q.RS, m_col = m - m_row * q.RS;  // staged row / column of m
     const float scale = PREC ? (1.0f / 2048.0f) : 1.0f;
     uint32_t it = 0;
     RT_DECL
     for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-      const UnitPos up = decode_unit(u, q, p);
+      const UnitPos up = decode_unit(u, q);
       const int acc = (int)(it % q.NACC);
       RT_MARK(0);
       bool okw = wait_bar_warp(bars, ACC_FULL + acc, (it / q.NACC) & 1, abort_flag, p.status, 0x30000000u | it);
@@ -749,7 +802,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       const int co_base = up.cb * 64;
       const int ch0 = half * 32;  // first channel (within the block) of this warp
       if constexpr (!POOL) {
-        const int r = m / q.RS, c = m - r * q.RS;
+        const int r = m_row, c = m_col;
         const int oh = up.rt * q.R + r, ow = up.ct * q.WT + c;
         const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
         const long plane = (long)p.Ho * p.Wo;
@@ -813,10 +866,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ptx::tmem_ld16(tl + col0 + 128 + cc, h1);
           ptx::tmem_ld16(tl + col0 + 192 + cc, l1);
           ptx::tmem_wait_ld();
-          float part[16];
+          float part[16], bv[16];
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(&bv[j]) =
+                *reinterpret_cast<const float4 *>(&ctl->bias[co_base + ch0 + cc + j]);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float bias = ctl->bias[co_base + ch0 + cc + j];
+            const float bias = bv[j];
             const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
             const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
             float mx = fmaxf(v0, v1);
@@ -824,13 +881,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             mx = fminf(fmaxf(mx, p.ht_lo), p.ht_hi);
             part[j] = valid ? mx : 0.0f;
           }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
-          if (lane == 0)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) ctl->red[quad][ch0 + cc + j] = part[j];
+          // Sum over the warp's 32 pixels by halving exchanges: at each step a
+          // lane keeps half of its channels and adds its partner's sums of
+          // them.  Lane l ends with channel (l >> 1) & 15.
+          lane_sum16(part, lane);
+          if ((lane & 1) == 0) ctl->red[quad][ch0 + cc + ((lane >> 1) & 15)] = part[0];
         }
         ptx::tc_fence_before();
         __syncwarp();
