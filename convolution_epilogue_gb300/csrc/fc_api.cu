@@ -87,8 +87,11 @@ fc_status decode_eltwise(const fc_epilogue *epi, EpiDev *e, int *chain) {
            e->kind[1] == FC_EPI_ADD_CHANNEL &&
            (e->kind[2] == FC_EPI_CLAMP || e->kind[2] == FC_EPI_HARDTANH) &&
            e->kind[3] == FC_EPI_GELU_ERF)
-    *chain = (e->a[2] >= -1.0f && e->b[2] <= 1.0f) ? CHAIN_LEAKY_ADD_CLAMP1_GELU
-                                                   : CHAIN_LEAKY_ADD_CLAMP_GELU;
+    // GELU's argument within [-1, 1] and a slope in [0, 1]: the polynomial
+    // GELU and LeakyReLU as max(v, a v)
+    *chain = (e->a[2] >= -1.0f && e->b[2] <= 1.0f && e->a[0] >= 0.0f && e->a[0] <= 1.0f)
+                 ? CHAIN_LEAKY_ADD_CLAMP1_GELU
+                 : CHAIN_LEAKY_ADD_CLAMP_GELU;
   else
     *chain = CHAIN_GENERIC;
   return FC_OK;

@@ -10,6 +10,7 @@
 // erff / tanhf are CUDA's own functions (no fast-math approximations).
 #pragma once
 #include "fc_internal.h"
+#include "fc_tc_ptx.cuh"
 
 namespace fc {
 
@@ -18,24 +19,36 @@ __device__ __forceinline__ float op_hardswish(float v) {
   return v * __saturatef(fmaf(v, 1.0f / 6.0f, 0.5f));
 }
 
-// erf(z) by its Maclaurin series, erf(z) = 2/sqrt(pi) sum_n (-1)^n
-// z^(2n+1) / (n! (2n+1)), truncated after n = 8 (Horner in z^2).  For
-// |z| <= 1/sqrt(2) the first omitted term is below 3e-10, far under fp32
-// rounding; used only where the argument is known to be that small.
-__device__ __forceinline__ float erf_maclaurin(float z) {
-  constexpr float c[9] = {1.128379167e+00f, -3.761263890e-01f, 1.128379167e-01f, -2.686617065e-02f, 5.223977625e-03f, -8.548327023e-04f, 1.205533298e-04f, -1.492565036e-05f, 1.646211437e-06f};
-  const float z2 = z * z;
-  float p = c[8];
-#pragma unroll
-  for (int n = 7; n >= 0; --n) p = fmaf(p, z2, c[n]);
-  return z * p;
+// GELU for |v| <= 1 from the Maclaurin series of erf,
+//   erf(z) = 2/sqrt(pi) sum_n (-1)^n z^(2n+1) / (n! (2n+1)).
+// With z = v / sqrt 2 and s = v^2 this gives
+//   GELU(v) = v/2 + v/2 erf(v / sqrt 2) = v/2 + s R(s),
+//   R(s) = sum_n d_n s^n,  d_n = (-1)^n / (sqrt(2 pi) 2^n n! (2n+1)),
+// evaluated by Horner in s and truncated after n = 7: for |v| <= 1 the first
+// omitted term is below 2.3e-10, far under fp32 rounding of the result.
+constexpr double kInvSqrt2Pi = 0.39894228040143267794;  // 1 / sqrt(2 pi)
+
+__host__ __device__ constexpr float gelu_series_d(int n) {
+  double d = kInvSqrt2Pi;
+  for (int k = 1; k <= n; ++k) d /= 2.0 * k;  // 2^n n!
+  return (float)(((n & 1) ? -d : d) / (2 * n + 1));
 }
 
-// GELU for |v| <= 1 (its argument v / sqrt 2 is then within the series'
-// range).
 __device__ __forceinline__ float op_gelu_small(float v) {
-  const float h = 0.5f * v;
-  return fmaf(h, erf_maclaurin(v * 0.70710678118654752f), h);
+  const float s = v * v;
+  float r = gelu_series_d(7);
+#pragma unroll
+  for (int n = 6; n >= 0; --n) r = fmaf(r, s, gelu_series_d(n));
+  return fmaf(s, r, 0.5f * v);
+}
+
+// The same for two values on the paired fp32 pipe (bit-identical per lane).
+__device__ __forceinline__ uint64_t op_gelu_small2(uint64_t v) {
+  const uint64_t s = ptx::mul2(v, v);
+  uint64_t r = ptx::pk2(gelu_series_d(7), gelu_series_d(7));
+#pragma unroll
+  for (int n = 6; n >= 0; --n) r = ptx::fma2(r, s, ptx::pk2(gelu_series_d(n), gelu_series_d(n)));
+  return ptx::fma2(s, r, ptx::mul2(v, ptx::pk2(0.5f, 0.5f)));
 }
 
 __device__ __forceinline__ float op_gelu_erf(float v) {
@@ -72,7 +85,7 @@ __device__ __forceinline__ float apply_chain(const EpiDev &e, int co, float v,
     v = fminf(fmaxf(v, e.a[2]), e.b[2]);
     return op_gelu_erf(v);
   } else if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
-    v = v > 0.0f ? v : e.a[0] * v;
+    v = fmaxf(v, e.a[0] * v);  // LeakyReLU for a slope in [0, 1]
     v = v + add;
     v = fminf(fmaxf(v, e.a[2]), e.b[2]);  // inside [-1, 1]
     return op_gelu_small(v);
@@ -80,6 +93,35 @@ __device__ __forceinline__ float apply_chain(const EpiDev &e, int co, float v,
     for (int i = 0; i < e.n_ops; ++i)
       v = apply_op(e.kind[i], e.a[i], e.b[i], e.chan[i], co, v);
     return v;
+  }
+}
+
+// Two adjacent channels of one pixel through the fused chains on the paired
+// fp32 pipe: y = chain(hi + scale * lo + bias).  Bit-identical to
+// apply_chain on each lane.  Only the two fixed chains.
+template <int CHAIN>
+__device__ __forceinline__ void apply_chain2(const EpiDev &e, float scale, float h0, float h1,
+                                             float l0, float l1, float b0, float b1, float a0,
+                                             float a1, float &o0, float &o1) {
+  uint64_t x = ptx::fma2(ptx::pk2(scale, scale), ptx::pk2(l0, l1), ptx::pk2(h0, h1));
+  x = ptx::add2(x, ptx::pk2(b0, b1));
+  float x0, x1;
+  if constexpr (CHAIN == CHAIN_RELU_HARDSWISH) {
+    ptx::upk2(x, x0, x1);
+    x0 = fmaxf(x0, 0.0f);
+    x1 = fmaxf(x1, 0.0f);
+    const float g0 = __saturatef(fmaf(x0, 1.0f / 6.0f, 0.5f));
+    const float g1 = __saturatef(fmaf(x1, 1.0f / 6.0f, 0.5f));
+    ptx::upk2(ptx::mul2(ptx::pk2(x0, x1), ptx::pk2(g0, g1)), o0, o1);
+  } else {  // CHAIN_LEAKY_ADD_CLAMP1_GELU
+    float t0, t1;
+    ptx::upk2(x, x0, x1);
+    ptx::upk2(ptx::mul2(x, ptx::pk2(e.a[0], e.a[0])), t0, t1);
+    x = ptx::add2(ptx::pk2(fmaxf(x0, t0), fmaxf(x1, t1)), ptx::pk2(a0, a1));
+    ptx::upk2(x, x0, x1);
+    x0 = fminf(fmaxf(x0, e.a[2]), e.b[2]);
+    x1 = fminf(fmaxf(x1, e.a[2]), e.b[2]);
+    ptx::upk2(op_gelu_small2(ptx::pk2(x0, x1)), o0, o1);
   }
 }
 

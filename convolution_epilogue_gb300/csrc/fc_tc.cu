@@ -463,6 +463,83 @@ __device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJ
   return true;
 }
 
+// Issues the MMAs of one chunk: KS K steps x U M tiles, each an N=128
+// product (A_hi against [W_hi | W_lo]) and an N=64 product (A_lo against
+// W_hi).  Fully unrolled: per K step only the A and B start addresses move
+// (kd[ks] and ks x 4 KB), so the issuing warp spends few instructions per
+// MMA pair.  Every MMA pair is issued under elect.sync by the converged
+// warp.  `first_accum` is 0 for the first chunk of an accumulator.
+template <int PREC, int U, int KS>
+__device__ __forceinline__ void issue_chunk(const uint32_t (&kd)[28], uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t dacc, uint32_t lo_delta, uint32_t tile_delta,
+                                            uint32_t first_accum) {
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;  // SBO 128 B, version 1
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t ah = a_lo + kd[ks];
+    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+    const uint32_t accum = ks ? 1u : first_accum;
+    if (ptx::elect_one()) {
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        const uint32_t aht = ah + (uint32_t)t * tile_delta;
+        const uint64_t dh = desc_hi | aht;
+        const uint64_t dl = desc_hi | (aht + lo_delta);
+        const uint32_t d = dacc + (uint32_t)(t * 128);
+        if constexpr (PREC == 0) {
+          ptx::mma_tf32(d, dh, bd, idesc1, accum);
+          ptx::mma_tf32(d + 64, dl, bd, idesc2, 1u);
+        } else {
+          ptx::mma_f16(d, dh, bd, idesc1, accum);
+          ptx::mma_f16(d + 64, dl, bd, idesc2, 1u);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// The same MMAs as issue_chunk with a run-time K-step count: each step's
+// delta is read from the table in shared memory one step ahead.
+template <int PREC, int U>
+__device__ __forceinline__ void issue_chunk_loop(const uint32_t *kd_smem, int KS, uint32_t a_lo,
+                                                 uint32_t b_lo, uint32_t dacc, uint32_t lo_delta,
+                                                 uint32_t tile_delta, uint32_t first_accum) {
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
+  const volatile uint32_t *kt = kd_smem;
+  uint32_t kd_next = kt[0];
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t kd_cur = kd_next;
+    kd_next = kt[ks + 1];
+    const uint32_t ah = a_lo + kd_cur;
+    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+    const uint32_t accum = ks ? 1u : first_accum;
+    if (ptx::elect_one()) {
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        const uint32_t aht = ah + (uint32_t)t * tile_delta;
+        const uint64_t dh = desc_hi | aht;
+        const uint64_t dl = desc_hi | (aht + lo_delta);
+        const uint32_t d = dacc + (uint32_t)(t * 128);
+        if constexpr (PREC == 0) {
+          ptx::mma_tf32(d, dh, bd, idesc1, accum);
+          ptx::mma_tf32(d + 64, dl, bd, idesc2, 1u);
+        } else {
+          ptx::mma_f16(d, dh, bd, idesc1, accum);
+          ptx::mma_f16(d + 64, dl, bd, idesc2, 1u);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Sums v[0..15] over the 32 lanes of a warp: after the call lane l holds in
 // v[0] the total of the value v[(l >> 1) & 15] had on every lane.
 __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
@@ -691,10 +768,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // The warp stays converged; every MMA burst and every commit is issued
     // under elect.sync, which picks the same (lowest) lane each time, so each
     // commit tracks all MMAs before it.
-    constexpr uint32_t fmt = PREC ? 0u : 2u;
-    constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
-    constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
     const uint32_t sbase = ptx::smem_u32(smem);
+    // per-K-step A descriptor deltas, constant for the launch, kept in
+    // registers (every index below is a compile-time constant)
+    uint32_t kdr[28];
+#pragma unroll
+    for (int i = 0; i < 28; ++i) kdr[i] = ctl->kdelta[i];
     const uint32_t lo_delta = (uint32_t)((q.P * q.plane_bytes) >> 4);  // hi -> lo planes
     const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile (pool)
     uint32_t g = 0, gb = 0, it = 0;
@@ -729,37 +808,23 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
         ptx::tc_fence_after();
         RT_MARK(2);  // waiting for a filled stage
-        // descriptors of this stage / weight chunk; each K step only adds its
-        // precomputed delta (no arithmetic on the issue path)
-        const uint64_t a0 = ptx::smem_desc(sbase + (uint32_t)(s * q.a_stage_bytes), 0, 128);
-        const uint64_t b0 = ptx::smem_desc(bbase, 2048, 128);
+        // low descriptor words of this stage / weight chunk (start address
+        // and leading byte offset); the high word is the same for all
+        const uint32_t a_lo = ((sbase + (uint32_t)(s * q.a_stage_bytes)) >> 4) & 0x3FFFu;
+        const uint32_t b_lo = ((bbase >> 4) & 0x3FFFu) | ((2048u >> 4) << 16);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
-        // Per-K-step descriptor deltas come from a table in shared memory; the
-        // next step's entry is loaded while this step's MMAs are issued.
-        const volatile uint32_t *kd_tab = ctl->kdelta;
-        uint32_t kd_next = kd_tab[0];
-        for (int ks = 0; ks < q.KS; ++ks) {
-          const uint32_t kd_cur = kd_next;
-          kd_next = kd_tab[ks + 1];
-          const uint64_t bdesc = b0 + (uint64_t)(ks * (kBStep >> 4));
-          const uint32_t accum = (c | ks) != 0;
-          const uint64_t ah0 = a0 + (uint64_t)kd_cur;
-          if (ptx::elect_one()) {
-#pragma unroll
-            for (int t = 0; t < U; ++t) {
-              const uint64_t ah = ah0 + (uint64_t)(t * tile_delta);
-              const uint64_t al = ah + lo_delta;
-              const uint32_t d = dacc + (uint32_t)(t * 128);
-              if constexpr (PREC == 0) {
-                ptx::mma_tf32(d, ah, bdesc, idesc1, accum);
-                ptx::mma_tf32(d + 64, al, bdesc, idesc2, 1u);
-              } else {
-                ptx::mma_f16(d, ah, bdesc, idesc1, accum);
-                ptx::mma_f16(d + 64, al, bdesc, idesc2, 1u);
-              }
-            }
+        const uint32_t first = c != 0;
+        // Measured on GB300: the unrolled issue wins for one M tile per
+        // chunk, the table-driven loop for the pooled two-tile chunks.
+        if constexpr (U == 1) {
+          switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
+            case 5: issue_chunk<PREC, 1, 5>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            case 9: issue_chunk<PREC, 1, 9>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            case 14: issue_chunk<PREC, 1, 14>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            default: issue_chunk<PREC, 1, 27>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
           }
-          __syncwarp();
+        } else {
+          issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
         }
         if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
@@ -832,11 +897,24 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           }
           float *yc = yp + (long)cc * cstride;
           if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
+            if constexpr (CHAIN == CHAIN_RELU_HARDSWISH || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-              *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-              yc += cstride;
+              for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
+                float o0, o1;
+                apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
+                                    __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
+                                    bv[j + 1], av[j], av[j + 1], o0, o1);
+                yc[0] = o0;
+                yc[cstride] = o1;
+                yc += 2 * cstride;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                yc += cstride;
+              }
             }
           } else if (valid) {
 #pragma unroll
