@@ -148,9 +148,11 @@ static_assert(offsetof(SmemCtl, bias) % 16 == 0 && offsetof(SmemCtl, addend) % 1
               "16-byte aligned per-channel arrays");
 static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
-TcPlan make_plan(const ConvProblem &p, int prec) {
+// Plan with `U` M tiles per unit (pooling needs 2).
+TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   TcPlan q{};
   if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
+  if (p.pool && U != 2) return q;
   if (p.pool && p.KD != 1) return q;
   q.prec = prec;
   q.E = prec ? 8 : 4;
@@ -162,7 +164,6 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.TAPS = p.KD * 9;
   q.pairtaps = (q.P == 1);
   q.KS = q.pairtaps ? cdiv(q.TAPS, 2) : q.TAPS;
-  q.U = p.pool ? 2 : 1;
   const bool rowpack = (p.Wo + 2 <= 128);
   if (rowpack) {
     q.RS = p.Wo + 2;
@@ -175,6 +176,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
     q.n_ct = cdiv(p.Wo, 128);
     q.R = 1;
   }
+  q.U = U;
   q.RIN = q.U * q.R + 2;
   // last staged pixel any MMA can touch (+1 for the paired-tap slice)
   const int maxread = ((p.KD - 1) * q.RIN + 2) * q.RS + 2 + (q.U - 1) * q.R * q.RS + 127 + 1;
@@ -186,7 +188,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.COB = cdiv(p.CO, 64);
   if (q.COB * 64 > kMaxCoTc) return q;
   q.b_chunk_bytes = q.KS * kBStep;
-  q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.R);
+  q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.U * q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
   if (q.units >= (1L << 31)) return q;  // unit indices are 32-bit
   q.fd_ct = make_fastdiv((uint32_t)q.n_ct);
@@ -194,7 +196,7 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   q.fd_do = make_fastdiv((uint32_t)p.Do);
   q.fd_n = make_fastdiv((uint32_t)p.N);
   q.fd_cb = make_fastdiv((uint32_t)((long)p.N * p.Do * q.n_rt * q.n_ct));
-  q.NACC = p.pool ? 2 : 4;
+  q.NACC = q.U == 2 ? 2 : 4;
   q.tmem_cols = q.NACC * q.U * 128;
   if (q.tmem_cols > 512) return q;
   // shared memory: A stages + B (resident or a ring) + barriers/misc
@@ -220,6 +222,18 @@ TcPlan make_plan(const ConvProblem &p, int prec) {
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
   q.ok = 1;
   return q;
+}
+
+// Pooling pairs two output rows per unit.  Without pooling a unit also
+// takes two M tiles (half the barrier hand-offs per MMA, fewer re-staged
+// halo rows) when the image has rows for both and shared memory still holds
+// at least three stages; otherwise one.
+TcPlan make_plan(const ConvProblem &p, int prec) {
+  if (p.pool) return make_plan_u(p, prec, 2);
+  TcPlan q2 = make_plan_u(p, prec, 2);
+  if (q2.ok && q2.S >= 3 && p.Ho > q2.R) return q2;
+  TcPlan q1 = make_plan_u(p, prec, 1);
+  return q1.ok ? q1 : q2;
 }
 
 // --------------------------------------------------------------- device
@@ -556,12 +570,13 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL>
+template <int PREC, int CHAIN, bool POOL, int U>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial) {
   constexpr int E = PREC ? 8 : 4;
-  constexpr int U = POOL ? 2 : 1;
+  static_assert(U == 1 || U == 2, "one or two M tiles per unit");
+  static_assert(!POOL || U == 2, "pooling takes two output rows per unit");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -815,13 +830,13 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
         const uint32_t first = c != 0;
         // Measured on GB300: the unrolled issue wins for one M tile per
-        // chunk, the table-driven loop for the pooled two-tile chunks.
+        // chunk, the table-driven loop for two.
         if constexpr (U == 1) {
           switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
-            case 5: issue_chunk<PREC, 1, 5>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            case 9: issue_chunk<PREC, 1, 9>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            case 14: issue_chunk<PREC, 1, 14>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            default: issue_chunk<PREC, 1, 27>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            case 5: issue_chunk<PREC, U, 5>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            case 9: issue_chunk<PREC, U, 9>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            case 14: issue_chunk<PREC, U, 14>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
+            default: issue_chunk<PREC, U, 27>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
           }
         } else {
           issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
@@ -868,65 +883,69 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       const int ch0 = half * 32;  // first channel (within the block) of this warp
       if constexpr (!POOL) {
         const int r = m_row, c = m_col;
-        const int oh = up.rt * q.R + r, ow = up.ct * q.WT + c;
-        const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
+        const int ow = up.ct * q.WT + c;
         const long plane = (long)p.Ho * p.Wo;
         const long cstride = (long)p.Do * plane;
-        float *yp = p.y + (((long)up.n * p.CO + co_base + ch0) * p.Do + up.od) * plane +
-                    (long)oh * p.Wo + ow;
         const int nco = p.CO - co_base - ch0;  // channels of this warp that exist
-        const uint32_t col0 = (uint32_t)(acc * 128 + ch0);
 #pragma unroll 1
-        for (int cc = 0; cc < 32; cc += 16) {
-          uint32_t hi[16], lo[16];
-          RT_MARK(0);
-          ptx::tmem_ld16(tl + col0 + cc, hi);
-          ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
-          ptx::tmem_wait_ld();
-          RT_MARK(2);  // tensor-memory loads
-          float bv[16], av[16];
-          const float *sb = &ctl->bias[co_base + ch0 + cc];
-          const float *sa = &ctl->addend[co_base + ch0 + cc];
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            *reinterpret_cast<float4 *>(&bv[j]) = *reinterpret_cast<const float4 *>(sb + j);
-            if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU)
-              *reinterpret_cast<float4 *>(&av[j]) = *reinterpret_cast<const float4 *>(sa + j);
-            else
-              av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
-          }
-          float *yc = yp + (long)cc * cstride;
-          if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
-            if constexpr (CHAIN == CHAIN_RELU_HARDSWISH || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
-                float o0, o1;
-                apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
-                                    __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
-                                    bv[j + 1], av[j], av[j + 1], o0, o1);
-                yc[0] = o0;
-                yc[cstride] = o1;
-                yc += 2 * cstride;
+        for (int t = 0; t < U; ++t) {  // the unit's M tiles, R output rows each
+          const int oh = (up.rt * U + t) * q.R + r;
+          const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
+          float *yp = p.y + (((long)up.n * p.CO + co_base + ch0) * p.Do + up.od) * plane +
+                      (long)oh * p.Wo + ow;
+          const uint32_t col0 = (uint32_t)((acc * U + t) * 128 + ch0);
+  #pragma unroll 1
+          for (int cc = 0; cc < 32; cc += 16) {
+            uint32_t hi[16], lo[16];
+            RT_MARK(0);
+            ptx::tmem_ld16(tl + col0 + cc, hi);
+            ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
+            ptx::tmem_wait_ld();
+            RT_MARK(2);  // tensor-memory loads
+            float bv[16], av[16];
+            const float *sb = &ctl->bias[co_base + ch0 + cc];
+            const float *sa = &ctl->addend[co_base + ch0 + cc];
+  #pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              *reinterpret_cast<float4 *>(&bv[j]) = *reinterpret_cast<const float4 *>(sb + j);
+              if constexpr (CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU)
+                *reinterpret_cast<float4 *>(&av[j]) = *reinterpret_cast<const float4 *>(sa + j);
+              else
+                av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
+            }
+            float *yc = yp + (long)cc * cstride;
+            if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
+              if constexpr (CHAIN == CHAIN_RELU_HARDSWISH || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+  #pragma unroll
+                for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
+                  float o0, o1;
+                  apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
+                                      __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
+                                      bv[j + 1], av[j], av[j + 1], o0, o1);
+                  yc[0] = o0;
+                  yc[cstride] = o1;
+                  yc += 2 * cstride;
+                }
+              } else {
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                  *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                  yc += cstride;
+                }
               }
-            } else {
-#pragma unroll
+            } else if (valid) {
+  #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                if (cc + j < nco) {
+                  float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                  *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                }
                 yc += cstride;
               }
             }
-          } else if (valid) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (cc + j < nco) {
-                float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-              }
-              yc += cstride;
-            }
+            RT_MARK(3);  // epilogue math + stores
           }
-          RT_MARK(3);  // epilogue math + stores
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -993,10 +1012,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 
 int g_num_sms = 0;
 
-template <int PREC, int CHAIN, bool POOL>
+template <int PREC, int CHAIN, bool POOL, int U>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                           float *partial, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL>;
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1013,20 +1032,27 @@ cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *
   return cudaGetLastError();
 }
 
+template <int PREC, int U>
+cudaError_t launch_chain(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
+                         float *partial, cudaStream_t s) {
+  switch (p.chain) {
+    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U>(p, q, bimg, partial, s);
+    case CHAIN_RELU_HARDSWISH:
+      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U>(p, q, bimg, partial, s);
+    case CHAIN_LEAKY_ADD_CLAMP_GELU:
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U>(p, q, bimg, partial, s);
+    case CHAIN_LEAKY_ADD_CLAMP1_GELU:
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U>(p, q, bimg, partial, s);
+    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U>(p, q, bimg, partial, s);
+  }
+}
+
 template <int PREC>
 cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                         float *partial, cudaStream_t s) {
-  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true>(p, q, bimg, partial, s);
-  switch (p.chain) {
-    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false>(p, q, bimg, partial, s);
-    case CHAIN_RELU_HARDSWISH:
-      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false>(p, q, bimg, partial, s);
-    case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false>(p, q, bimg, partial, s);
-    case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false>(p, q, bimg, partial, s);
-    default: return launch_kernel<PREC, CHAIN_GENERIC, false>(p, q, bimg, partial, s);
-  }
+  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, s);
+  return q.U == 2 ? launch_chain<PREC, 2>(p, q, bimg, partial, s)
+                  : launch_chain<PREC, 1>(p, q, bimg, partial, s);
 }
 
 }  // namespace
