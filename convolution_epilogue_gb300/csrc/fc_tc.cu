@@ -383,8 +383,8 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
 
 // Splits E input channels of one pixel into hi / lo parts and stores the
 // two 16-byte slices.  fp16: hi = rn(v), lo = rn((v - hi) * 2^11), and |v|
-// is folded into `amax` for the range check; tf32: hi = rna(v),
-// lo = rna(v - hi).
+// is folded into the running maximum `amax` for the range check (hi is
+// infinite once |v| >= 65520); tf32: hi = rna(v), lo = rna(v - hi).
 template <int PREC, int E>
 __device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, const float (&v)[E],
                                             float &amax) {
@@ -772,7 +772,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     RT_STORE(warp == kProdWarp0 ? 2 : -1);
-    if (amax > 65504.0f) atomicOr(p.status, ST_RANGE);
+    if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
     // drain outstanding weight copies before the CTA can exit
     if (pt == 0 && q.b_resident) wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
     if (lane == 0 && last_b != 0xffffffffu)

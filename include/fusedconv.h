@@ -100,8 +100,9 @@ typedef struct {
  * high part and a tf32 remainder, three products (hi*hi + hi*lo + lo*hi)
  * accumulated in fp32 in tensor memory.  TC_F16X3: the same split with fp16
  * parts (the remainder scaled by 2^11): same accuracy as TC_TF32X3 for
- * |x|, |w| < 65504, twice the tensor rate; values outside that range set
- * FC_ERR_RANGE in the device status word. */
+ * |x| < 65520 and |w| <= 65504 (fp16's largest finite value), twice the
+ * tensor rate; values outside that range set FC_ERR_RANGE in the device
+ * status word. */
 typedef enum {
   FC_VARIANT_AUTO = 0,
   FC_VARIANT_FFMA = 1,

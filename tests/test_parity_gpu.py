@@ -289,3 +289,28 @@ def test_workload5_full_size_sampled(variant):
     _check(got, ref, f"workload 5 sampled [{variant}]")
     # every output is finite and inside tanh's range for clamped means
     assert np.all(np.abs(ynp) <= np.tanh(1.0) + 1e-6)
+
+
+def test_f16_split_range_boundary():
+    """tc_f16x3 splits each x into an fp16 hi part and a scaled fp16 lo part.
+    While the hi part stays finite (|x| < 65520; 65510 rounds to fp16's
+    largest finite value, 65504) the result meets the tolerance; once it
+    overflows (|x| >= 65520) the call reports FC_ERR_RANGE (7) in the device
+    status word rather than a wrong result."""
+    st = synth.seeded(777)
+    x = st.normal((1, 8, 12, 12))
+    w = st.uniform((64, 8, 3, 3), 1.0 / np.sqrt(72.0))
+    b = st.uniform((64,), 1.0 / np.sqrt(72.0))
+    x[0, 3, 5, 5] = 65510.0
+    ref = oracle.conv_epi(x, w, b, ())
+    _check(_run_conv("tc_f16x3", x, w, b, ()), ref, "x = 65510")
+    x[0, 3, 5, 5] = -70000.0
+    m = fc()
+    m.set_variant("tc_f16x3")
+    try:
+        m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), ())
+        assert m.last_variant() == "tc_f16x3"
+        assert m.get_last_device_error() == 7
+        assert m.get_last_device_error() == 0  # reading clears the word
+    finally:
+        m.set_variant("auto")
