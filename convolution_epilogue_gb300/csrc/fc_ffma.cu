@@ -210,16 +210,38 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
 
 // Second stage of the pooled mean: y[n][co] = tanh(sum_t partial[n][t][co] /
 // count), summed in double in index order.
-__global__ void pool_finish_kernel(const float *__restrict__ partial, int N,
-                                   int CO, int T, double inv_count,
-                                   float *__restrict__ y) {
-  int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N * CO) return;
-  int n = i / CO, co = i % CO;
-  const float *src = partial + (long)n * T * CO + co;
-  double s = 0.0;
-  for (int t = 0; t < T; ++t) s += (double)src[(long)t * CO];
-  y[i] = (float)tanh(s * inv_count);
+// y[n][c] = tanh(sum_t partial[n][t][c] * inv_count).  One block of 256
+// threads per image, 64 channels at a time: thread (q, c) sums, in double and
+// in index order, the t of quarter q, and the four quarter sums are added in
+// the order 0, 1, 2, 3.  A fixed order, so the result does not depend on
+// scheduling.
+constexpr int kFinishQ = 4;
+constexpr int kFinishThreads = 64 * kFinishQ;
+
+__global__ void __launch_bounds__(kFinishThreads)
+pool_finish_kernel(const float *__restrict__ partial, int N, int CO, int T, double inv_count,
+                   float *__restrict__ y) {
+  __shared__ double qsum[kFinishQ][64];
+  const int n = blockIdx.x;
+  const int q = threadIdx.x / 64, cl = threadIdx.x % 64;
+  const int tq = (T + kFinishQ - 1) / kFinishQ;
+  const int t0 = q * tq, t1 = min(T, t0 + tq);
+  for (int c0 = 0; c0 < CO; c0 += 64) {
+    const int co = c0 + cl;
+    double s = 0.0;
+    if (co < CO) {
+      const float *src = partial + (long)n * T * CO + co;
+      for (int t = t0; t < t1; ++t) s += (double)src[(long)t * CO];
+    }
+    qsum[q][cl] = s;
+    __syncthreads();
+    if (q == 0 && co < CO) {
+      double tot = qsum[0][cl];
+      for (int k = 1; k < kFinishQ; ++k) tot += qsum[k][cl];
+      y[(long)n * CO + co] = (float)tanh(tot * inv_count);
+    }
+    __syncthreads();
+  }
 }
 
 template <int KD, int PR, int PC, bool POOL, int CHAIN>
@@ -267,8 +289,9 @@ cudaError_t pool_finish_launch(const ConvProblem &p, const float *partials,
                                int tiles_per_image, cudaStream_t s) {
   int total = p.N * p.CO;
   int count = (p.Ho / 2) * (p.Wo / 2);
-  pool_finish_kernel<<<ceil_div(total, 128), 128, 0, s>>>(
-      partials, p.N, p.CO, tiles_per_image, 1.0 / (double)count, p.y);
+  (void)total;
+  pool_finish_kernel<<<p.N, kFinishThreads, 0, s>>>(partials, p.N, p.CO, tiles_per_image,
+                                                    1.0 / (double)count, p.y);
   return cudaGetLastError();
 }
 
