@@ -34,7 +34,8 @@ EXPORTS = ("fc_conv2d_epi", "fc_conv2d_epi_noalloc", "fc_conv3d_epi", "fc_convT2
            "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
-           "fc_profile_read", "fc_profile_reset", "fc_wait_report")
+           "fc_profile_read", "fc_profile_reset", "fc_wait_report",
+           "fc_selftest_wait_timeout")
 
 
 class FcError(RuntimeError):
@@ -97,6 +98,8 @@ def lib():
             L.fc_profile_reset.restype = None
             L.fc_wait_report.restype = I
             L.fc_wait_report.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I]
+            L.fc_selftest_wait_timeout.restype = I
+            L.fc_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
             _lib = L
     return _lib
 
@@ -170,6 +173,12 @@ def last_variant() -> str:
 
 def last_launch_count() -> int:
     return int(lib().fc_last_launch_count())
+
+
+def selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch the bounded-wait self-test (see fc_selftest_wait_timeout)."""
+    _check(lib().fc_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
+           "fc_selftest_wait_timeout")
 
 
 def get_last_device_error(stream=None) -> int:

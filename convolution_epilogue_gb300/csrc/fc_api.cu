@@ -426,6 +426,17 @@ fc_status fc_get_last_device_error(void *stream) {
 
 int fc_version(void) { return 100; }
 
+fc_status fc_selftest_wait_timeout(unsigned int limit_us, void *stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FC_ERR_INVALID_ARG;
+  unsigned int *st = nullptr;
+  fc_status s = status_ptr(&st);
+  if (s != FC_OK) return s;
+  if (selftest_wait_launch(st, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FC_ERR_CUDA;
+  return FC_OK;
+}
+
 int fc_wait_report(void *stream, unsigned int *out, int max_words) {
   unsigned int *st = nullptr;
   if (status_ptr(&st) != FC_OK || !out || max_words < 1) return -1;

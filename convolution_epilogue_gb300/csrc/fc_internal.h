@@ -79,5 +79,6 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws,
                       const WsLayout &L, cudaStream_t s, int *launches);
 int tc_pool_tiles_per_image(const ConvProblem &p);
 size_t tc_weight_bytes(const ConvProblem &p);
+cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace fc

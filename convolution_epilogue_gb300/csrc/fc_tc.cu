@@ -264,7 +264,7 @@ __device__ __noinline__ void record_timeout(unsigned int *status, const uint64_t
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parity,
                                          volatile int *abort, unsigned int *status,
-                                         uint32_t tag) {
+                                         uint32_t tag, uint64_t limit_ns = kWaitNs) {
   uint64_t *bar = bars + idx;
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -275,7 +275,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parit
         record_timeout(status, bar, idx, parity, tag | 0x08000000u);
         return false;
       }
-      if (ptx::globaltimer_ns() - t0 > kWaitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         record_timeout(status, bar, idx, parity, tag);
         *abort = 1;
         return false;
@@ -288,9 +288,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parit
 // warp never splits around .sync.aligned instructions or named barriers.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t parity,
                                               volatile int *abort, unsigned int *status,
-                                              uint32_t tag) {
+                                              uint32_t tag, uint64_t limit_ns = kWaitNs) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bars, idx, parity, abort, status, tag) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0)
+    ok = wait_bar(bars, idx, parity, abort, status, tag, limit_ns) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -1010,6 +1011,30 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
 }
 
+// Failure-detection self-test: warp 0 waits, with a limit of `limit_ns`, on
+// an mbarrier whose phase nothing completes; it gives up, records the wait
+// (tag 0x71000001) and raises the block's abort flag.  Warp 1 waits on a
+// second such barrier under the kernels' normal limit and gives up as soon
+// as it sees the flag (record tag 0x71000002 | 0x08000000).  No fault, no
+// hang: both waits are bounded and nothing else is in flight.
+__global__ void selftest_wait_kernel(unsigned int *status, uint64_t limit_ns) {
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars[0], 1);
+    ptx::mbar_init(&bars[1], 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int *ab = &abort_flag;
+  if (threadIdx.x < 32)
+    wait_bar_warp(bars, 0, 0, ab, status, 0x71000001u, limit_ns);
+  else
+    wait_bar_warp(bars, 1, 0, ab, status, 0x71000002u);
+  __syncthreads();
+}
+
 int g_num_sms = 0;
 
 template <int PREC, int CHAIN, bool POOL, int U>
@@ -1058,6 +1083,11 @@ cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bi
 }  // namespace
 
 bool tc_supported(const ConvProblem &p, int prec) { return make_plan(p, prec).ok != 0; }
+
+cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 64, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 size_t tc_weight_bytes(const ConvProblem &p) {
   size_t m = 0;

@@ -189,6 +189,19 @@ FC_API int fc_last_launch_count(void);
 /* Human-readable name of a status code (static string). */
 FC_API const char *fc_status_string(fc_status s);
 
+/* Self-test of the kernels' bounded waits (failure detection without a GPU
+ * fault).  Launches one block on `stream` in which one warp waits, with the
+ * bounded-wait routine the conv kernels use and a limit of `limit_us`
+ * microseconds, on an mbarrier that nothing completes: it gives up, records
+ * the wait and raises the block's abort flag.  A second warp, waiting on
+ * another such barrier under the kernels' normal 4 s limit, sees the flag
+ * and gives up at once.  Afterwards fc_get_last_device_error returns
+ * FC_ERR_TIMEOUT and fc_wait_report lists both waits (role tags 0x71000001,
+ * and 0x79000002 for the one ended by the flag).  limit_us in
+ * [1, 1000000], else FC_ERR_INVALID_ARG; FC_ERR_CUDA if the launch fails.
+ * The pages have no counterpart: it tests this library's failure path. */
+FC_API fc_status fc_selftest_wait_timeout(unsigned int limit_us, void *stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FC_OK, FC_ERR_TIMEOUT, FC_ERR_RANGE or FC_ERR_CUDA. */
 FC_API fc_status fc_get_last_device_error(void *stream);
