@@ -287,9 +287,7 @@ int ffma_pool_tiles_per_image(const ConvProblem &p) {
 
 cudaError_t pool_finish_launch(const ConvProblem &p, const float *partials,
                                int tiles_per_image, cudaStream_t s) {
-  int total = p.N * p.CO;
   int count = (p.Ho / 2) * (p.Wo / 2);
-  (void)total;
   pool_finish_kernel<<<p.N, kFinishThreads, 0, s>>>(partials, p.N, p.CO, tiles_per_image,
                                                     1.0 / (double)count, p.y);
   return cudaGetLastError();
