@@ -799,9 +799,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
       const int acc = (int)(it % q.NACC);
+      const uint32_t acc_par = ((it / q.NACC) & 1) ^ 1;
       RT_MARK(0);
-      if (!wait_bar_warp(bars, ACC_EMPTY + acc, ((it / q.NACC) & 1) ^ 1, abort_flag, p.status, 0x21000000u | it)) break;
-      ptx::tc_fence_after();
+      if constexpr (POOL) {  // the pooled epilogue takes both tiles at once
+        if (!wait_bar_warp(bars, ACC_EMPTY + acc, acc_par, abort_flag, p.status, 0x21000000u | it)) break;
+        ptx::tc_fence_after();
+      }
       RT_MARK(1);  // waiting for a free accumulator
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = (int)(g % q.S);
@@ -830,17 +833,37 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t b_lo = ((bbase >> 4) & 0x3FFFu) | ((2048u >> 4) << 16);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
         const uint32_t first = c != 0;
-        // Measured on GB300: the unrolled issue wins for one M tile per
-        // chunk, the table-driven loop for two.
-        if constexpr (U == 1) {
-          switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
-            case 5: issue_chunk<PREC, U, 5>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            case 9: issue_chunk<PREC, U, 9>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            case 14: issue_chunk<PREC, U, 14>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-            default: issue_chunk<PREC, U, 27>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first); break;
-          }
-        } else {
+        if constexpr (POOL) {
+          // both tiles per K step (measured faster for the pooled chunks)
           issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
+        } else {
+          // Tile by tile, each with its own accumulator barriers: a tile's
+          // MMAs start once the epilogue has freed that tile, and the
+          // epilogue starts on a tile once its last chunk's MMAs are done.
+          bool okt = true;
+#pragma unroll 1
+          for (int t = 0; t < U && okt; ++t) {
+            const int ab = acc * U + t;
+            if (c == 0) {
+              okt = wait_bar_warp(bars, ACC_EMPTY + ab, acc_par, abort_flag, p.status, 0x21000000u | it);
+              ptx::tc_fence_after();
+            }
+            const uint32_t at = a_lo + (uint32_t)t * tile_delta, dt = dacc + (uint32_t)(t * 128);
+            switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
+              case 5: issue_chunk<PREC, 1, 5>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+              case 9: issue_chunk<PREC, 1, 9>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+              case 14: issue_chunk<PREC, 1, 14>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+              default: issue_chunk<PREC, 1, 27>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+            }
+            if (c == q.NCH - 1) {
+              if (ptx::elect_one()) ptx::tc_commit(&acc_full[ab]);
+              __syncwarp();
+            }
+          }
+          if (!okt) {
+            ok = false;
+            break;
+          }
         }
         if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
@@ -851,8 +874,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         RT_MARK(3);  // issuing MMAs
       }
       if (!ok) break;
-      if (ptx::elect_one()) ptx::tc_commit(&acc_full[acc]);
-      __syncwarp();
+      if constexpr (POOL) {
+        if (ptx::elect_one()) ptx::tc_commit(&acc_full[acc]);
+        __syncwarp();
+      }
     }
     // wait until every MMA this warp issued has completed
     if (ptx::elect_one()) ptx::tc_commit(drain);
@@ -873,11 +898,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const UnitPos up = decode_unit(u, q);
       const int acc = (int)(it % q.NACC);
+      const uint32_t acc_par = (it / q.NACC) & 1;
       RT_MARK(0);
-      bool okw = wait_bar_warp(bars, ACC_FULL + acc, (it / q.NACC) & 1, abort_flag, p.status, 0x30000000u | it);
-      if constexpr (POOL) okw = epi_all(okw);
-      if (!okw) break;
-      ptx::tc_fence_after();
+      if constexpr (POOL) {
+        bool okw = wait_bar_warp(bars, ACC_FULL + acc, acc_par, abort_flag, p.status, 0x30000000u | it);
+        okw = epi_all(okw);
+        if (!okw) break;
+        ptx::tc_fence_after();
+      }
       RT_MARK(1);  // waiting for a finished accumulator
       const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
       const int co_base = up.cb * 64;
@@ -888,8 +916,15 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const long plane = (long)p.Ho * p.Wo;
         const long cstride = (long)p.Do * plane;
         const int nco = p.CO - co_base - ch0;  // channels of this warp that exist
+        bool okt = true;
 #pragma unroll 1
         for (int t = 0; t < U; ++t) {  // the unit's M tiles, R output rows each
+          if (!wait_bar_warp(bars, ACC_FULL + acc * U + t, acc_par, abort_flag, p.status,
+                             0x30000000u | ((uint32_t)t << 20) | (it & 0xFFFFFu))) {
+            okt = false;
+            break;
+          }
+          ptx::tc_fence_after();
           const int oh = (up.rt * U + t) * q.R + r;
           const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
           float *yp = p.y + (((long)up.n * p.CO + co_base + ch0) * p.Do + up.od) * plane +
@@ -947,10 +982,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             }
             RT_MARK(3);  // epilogue math + stores
           }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[acc * U + t]);
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+        if (!okt) break;
       } else {
         const int c = m;  // one output row per M tile
         const int ow = up.ct * q.WT + c;
