@@ -396,6 +396,27 @@ def run_ours(args):
             "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / med,
             "kernel_ms": kern[w][0]}
 
+    # the same calls back to back without the L2 flush (inputs may sit in
+    # L2 between calls); reported beside the flushed series, not used for
+    # the roofline fraction
+    for w in WORKLOADS:
+        evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(20)]
+        for e0, e1 in evw:
+            e0.record(stream)
+            calls[w]()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        per_cfg[synth.WORKLOADS[w]["name"]]["ms_median_no_flush"] = statistics.median(
+            e0.elapsed_time(e1) for e0, e1 in evw)
+
+    # fusion ablation for the pooled workload: the transposed conv as a
+    # materialised conv (swapped, flipped weights, padding 1; 2.15 GB
+    # written and read back) followed by the standalone tail kernel
+    ablation = None
+    if not args.no_ablation:
+        ablation = fusion_ablation(fc, d[5], flush, stream, per[5])
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -414,6 +435,8 @@ def run_ours(args):
             "device_status": status, "wall_s_timed": t_wall}
     if e2e is not None:
         line["e2e"] = e2e
+    if ablation is not None:
+        line["fusion_ablation"] = ablation
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_scale)
     if rank == 0:
@@ -421,6 +444,45 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def fusion_ablation(fc, d5, flush, stream, fused_ms_list, reps=10):
+    """Unfused pipeline for the pooled workload, same L2 flushing as the
+    fused timing: conv (y_conv materialised) then fc_pool_mean_tail."""
+    import torch
+    x, w, b = d5["x"], d5["w"], d5["b"]
+    w_conv = torch.flip(w.permute(1, 0, 2, 3), dims=(2, 3)).contiguous()
+    N, C, H, W = x.shape
+    y_conv = torch.empty((N, w.shape[1], H, W), dtype=torch.float32, device=x.device)
+    y = torch.empty((N, w.shape[1], 1, 1), dtype=torch.float32, device=x.device)
+    ws = torch.empty(fc.workspace_bytes(0, (N, C, H, W, w.shape[1], 3, 1)), dtype=torch.uint8,
+                     device=x.device)
+    conv = lambda: fc.fc_conv2d_epi(x, w_conv, b, (), pad=1, y=y_conv, ws=ws)
+    tail = lambda: fc.fc_pool_mean_tail(y_conv, y=y)
+    conv()
+    conv_variant = fc.last_variant()
+    tail()
+    torch.cuda.synchronize()
+    t_conv, t_tail = [], []
+    for _ in range(reps):
+        for fn, out in ((conv, t_conv), (tail, t_tail)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1))
+    if fc.get_last_device_error() != 0:
+        raise RuntimeError("device status word set in the ablation")
+    mc, mt = statistics.median(t_conv), statistics.median(t_tail)
+    fused = statistics.median(fused_ms_list)
+    tail_bytes = y_conv.numel() * 4
+    del y_conv
+    return {"workload": "convT2d_pool_mean_128x64x256x256",
+            "unfused_conv_ms": mc, "unfused_tail_ms": mt, "unfused_total_ms": mc + mt,
+            "fused_ms": fused, "fused_speedup": (mc + mt) / fused,
+            "tail_gbs": tail_bytes / (mt * 1e-3) / 1e9, "conv_variant": conv_variant}
 
 
 def measure_e2e(args, fc, host, dev, stream, chain4_host):
@@ -508,6 +570,7 @@ def main():
     ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tc_tf32x3", "tc_f16x3"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--cpu-scale", type=int, default=128)
     ap.add_argument("--ref-scale", type=int, default=2)
     ap.add_argument("--profile-workload", type=int, default=0,

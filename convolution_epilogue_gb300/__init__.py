@@ -35,7 +35,7 @@ EXPORTS = ("fc_conv2d_epi", "fc_conv2d_epi_noalloc", "fc_conv3d_epi", "fc_convT2
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
            "fc_profile_read", "fc_profile_reset", "fc_wait_report",
-           "fc_selftest_wait_timeout")
+           "fc_selftest_wait_timeout", "fc_pool_mean_tail")
 
 
 class FcError(RuntimeError):
@@ -100,6 +100,9 @@ def lib():
             L.fc_wait_report.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I]
             L.fc_selftest_wait_timeout.restype = I
             L.fc_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+            F = ctypes.c_float
+            L.fc_pool_mean_tail.restype = I
+            L.fc_pool_mean_tail.argtypes = [P, I, I, I, I, I, I, F, F, P, P]
             _lib = L
     return _lib
 
@@ -313,3 +316,19 @@ def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
     _check(st, "fc_convT2d_pool_mean")
     del keep
     return y
+
+
+def fc_pool_mean_tail(x, k=2, s=2, hardtanh=(-1.0, 1.0), y=None, stream=None):
+    """MaxPool(k, s) -> hardtanh -> mean(H, W) -> tanh on a conv output
+    x [N, C, H, W]; returns y [N, C, 1, 1]."""
+    import torch
+    _require_cuda_f32("x", x)
+    N, C, H, W = x.shape
+    if y is None:
+        y = torch.empty((N, C, 1, 1), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    _check(lib().fc_pool_mean_tail(_ptr(x), N, C, H, W, int(k), int(s), float(hardtanh[0]),
+                                   float(hardtanh[1]), _ptr(y), _stream_handle(stream)),
+           "fc_pool_mean_tail")
+    return y
+

@@ -352,6 +352,28 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   return run(p, ws, ws_bytes, stream);
 }
 
+fc_status fc_pool_mean_tail(const float *x, int N, int C, int H, int W, int k, int s,
+                            float ht_lo, float ht_hi, float *y, void *stream) {
+  if (N < 0 || C < 1 || H < 1 || W < 1 || k < 1 || s < 1 || k > H || k > W ||
+      !(ht_lo <= ht_hi))
+    return FC_ERR_INVALID_ARG;
+  if (!fits_int32((long long)N * C) || !fits_int32((long long)H * W)) return FC_ERR_UNSUPPORTED;
+  t_last_variant = 0;
+  t_last_launches = 0;
+  if (N == 0) return FC_OK;
+  if (!x || !y) return FC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) % 4) || (reinterpret_cast<uintptr_t>(y) % 4))
+    return FC_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FC_ERR_CUDA;
+  int launches = 0;
+  if (tail_launch(x, (long)N * C, H, W, k, s, ht_lo, ht_hi, y,
+                  static_cast<cudaStream_t>(stream), &launches) != cudaSuccess)
+    return FC_ERR_CUDA;
+  t_last_launches = launches;
+  return FC_OK;
+}
+
 size_t fc_workspace_bytes(int entry, const int *d) {
   if (!d) return 0;
   ConvProblem p{};

@@ -81,4 +81,8 @@ int tc_pool_tiles_per_image(const ConvProblem &p);
 size_t tc_weight_bytes(const ConvProblem &p);
 cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaStream_t s);
 
+// Standalone pooled-mean tail over `planes` H x W planes (fc_tail.cu).
+cudaError_t tail_launch(const float *x, long planes, int H, int W, int k, int s, float lo,
+                        float hi, float *y, cudaStream_t st, int *launches);
+
 }  // namespace fc

@@ -189,6 +189,25 @@ FC_API int fc_last_launch_count(void);
 /* Human-readable name of a status code (static string). */
 FC_API const char *fc_status_string(fc_status s);
 
+/* The pooled-mean tail alone, on a conv output the caller already holds
+ * (trace "Kimi-K2.6__l2_p10", tail-kernel and general max-pool paragraphs):
+ *   y[n][c] = tanh( mean_{i<Hp, j<Wp} clamp( max_{a,b<k} x[n][c][i*s+a][j*s+b],
+ *                                             ht_lo, ht_hi ) ),
+ *   Hp = (H - k) / s + 1, Wp = (W - k) / s + 1 (floor; rows/columns past the
+ *   last whole window are dropped).
+ * x: device, contiguous fp32 [N][C][H][W], 4-byte aligned.  y: device fp32
+ * [N][C] (the [N][C][1][1] of the pooled entry), written in full.  Any
+ * k >= 1, s >= 1 with k <= H, W (overlapping windows and gaps allowed).
+ * Deterministic: per-plane sums in a fixed order.  Asynchronous on `stream`.
+ * Errors: FC_ERR_INVALID_ARG (extents, k, s, ht_lo > ht_hi, null pointers
+ * with N > 0), FC_ERR_ALIGNMENT, FC_ERR_UNSUPPORTED (N*C or H*W beyond
+ * 2^31 - 1), FC_ERR_CUDA (launch failure).  fc_convT2d_pool_mean fuses this
+ * tail into the conv and never writes x; this call serves callers with a
+ * materialised conv output and measures what the fusion saves.  Its kernel
+ * time is profiled under entry 3 by fc_profile_read. */
+FC_API fc_status fc_pool_mean_tail(const float *x, int N, int C, int H, int W, int k, int s,
+                                   float ht_lo, float ht_hi, float *y, void *stream);
+
 /* Self-test of the kernels' bounded waits (failure detection without a GPU
  * fault).  Launches one block on `stream` in which one warp waits, with the
  * bounded-wait routine the conv kernels use and a limit of `limit_us`
@@ -210,7 +229,7 @@ FC_API fc_status fc_get_last_device_error(void *stream);
  * records a pair of CUDA events on its stream around its main (contraction
  * + epilogue) kernel; pack and finishing kernels are outside the pair.
  * fc_profile_read synchronises on the recorded events and returns, for one
- * entry (0 conv2d, 1 conv3d, 2 convT-pool-mean), the summed milliseconds and
+ * entry (0 conv2d, 1 conv3d, 2 convT-pool-mean, 3 pool-mean tail), the summed milliseconds and
  * the number of timed launches since the last fc_profile_reset.  At most
  * 4096 pairs are kept; later launches are not timed.  Host-thread safe only
  * when one thread uses it at a time. */

@@ -109,3 +109,27 @@ def test_set_variant(L):
     for v in range(4):
         assert L.fc_set_variant(v) == 0
     assert L.fc_set_variant(0) == 0
+
+
+def test_pool_mean_tail_host_validation(L):
+    """The standalone tail rejects bad extents, windows and clamps on the
+    host, before any CUDA call (no GPU here)."""
+    import ctypes
+    P = ctypes.c_void_p
+
+    def call(N=2, C=3, H=8, W=8, k=2, s=2, lo=-1.0, hi=1.0, x=256, y=512):
+        return L.fc_pool_mean_tail(P(x), N, C, H, W, k, s, ctypes.c_float(lo),
+                                   ctypes.c_float(hi), P(y), None)
+    L.fc_pool_mean_tail.restype = ctypes.c_int
+    L.fc_pool_mean_tail.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                    P, P]
+    INVALID = 1
+    assert call(N=-1) == INVALID
+    assert call(C=0) == INVALID
+    assert call(k=0) == INVALID
+    assert call(s=0) == INVALID
+    assert call(k=9) == INVALID          # window wider than the plane
+    assert call(lo=1.0, hi=-1.0) == INVALID
+    assert call(x=0) == INVALID          # NULL with N > 0
+    assert call(N=0) == 0                # nothing to do

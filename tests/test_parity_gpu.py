@@ -314,3 +314,41 @@ def test_f16_split_range_boundary():
         assert m.get_last_device_error() == 0  # reading clears the word
     finally:
         m.set_variant("auto")
+
+
+@pytest.mark.parametrize("k,s,shape,ht", [
+    (2, 2, (2, 5, 36, 40), (-1.0, 1.0)),    # the configs' pooling, even extents
+    (2, 2, (1, 3, 37, 41), (-1.0, 1.0)),    # odd extents: last row / column dropped
+    (3, 2, (2, 4, 19, 23), (-0.5, 0.75)),   # overlapping windows, other clamp
+    (2, 3, (1, 6, 20, 17), (-2.0, 2.0)),    # gaps between windows
+    (1, 1, (1, 2, 7, 9), (-1.0, 1.0)),      # no pooling at all
+])
+def test_pool_mean_tail_against_oracle(k, s, shape, ht):
+    """The standalone tail: maxpool(k, s) -> hardtanh -> mean -> tanh, vs
+    the oracle's max-pool and mean composed with clamp and tanh in double."""
+    st = synth.seeded(600 + 10 * k + s)
+    x = st.normal(shape)
+    m = fc()
+    y = m.fc_pool_mean_tail(_dev(x), k=k, s=s, hardtanh=ht)
+    assert m.get_last_device_error() == 0
+    pooled = np.clip(oracle.maxpool2d(x.astype(np.float64), k, s), ht[0], ht[1])
+    ref = np.tanh(oracle.mean_hw(pooled))
+    _check(y.cpu().numpy(), ref, f"tail k={k} s={s} {shape}")
+
+
+def test_unfused_conv_then_tail_matches_fused_entry():
+    """The pooled entry's result equals the unfused pipeline the pages
+    describe (the transposed conv as a conv with swapped, flipped weights
+    and padding k - 1 - p, materialised, then the standalone tail), and
+    both match the oracle."""
+    inp = synth.make_inputs(2)
+    x, w, b = inp["x"], inp["w"], inp["b"]
+    m = fc()
+    fused = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b)).cpu().numpy()
+    w_conv = np.ascontiguousarray(np.flip(w.transpose(1, 0, 2, 3), axis=(2, 3)))
+    conv = m.fc_conv2d_epi(_dev(x), _dev(w_conv), _dev(b), (), pad=1)
+    unfused = m.fc_pool_mean_tail(conv).cpu().numpy()
+    assert m.get_last_device_error() == 0
+    ref = oracle.convT_pool_mean(x, w, b)
+    _check(fused, ref, "fused")
+    _check(unfused, ref, "unfused")
