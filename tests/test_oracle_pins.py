@@ -165,6 +165,56 @@ def test_conv3d_brute_force_tiny():
     np.testing.assert_allclose(got, _brute_conv3d(x, w, b), rtol=0, atol=1e-12)
 
 
+def _brute_conv2d_strided(x, w, b, stride, pad):
+    """Independent loop for a strided conv: out (oh, ow) reads input rows
+    oh*stride + kh - pad and columns ow*stride + kw - pad."""
+    N, C, H, W = x.shape
+    CO, _, K, _ = w.shape
+    Ho, Wo = (H + 2 * pad - K) // stride + 1, (W + 2 * pad - K) // stride + 1
+    y = np.zeros((N, CO, Ho, Wo))
+    for n, co, oh, ow in np.ndindex(N, CO, Ho, Wo):
+        s = float(b[co])
+        for ci in range(C):
+            for kh in range(K):
+                for kw in range(K):
+                    ih, iw = oh * stride + kh - pad, ow * stride + kw - pad
+                    if 0 <= ih < H and 0 <= iw < W:
+                        s += float(x[n, ci, ih, iw]) * float(w[co, ci, kh, kw])
+        y[n, co, oh, ow] = s
+    return y
+
+
+def test_conv2d_stride2_brute_force_and_extent():
+    st = _rng(11)
+    x = st.normal((2, 3, 9, 8))
+    w = st.uniform((4, 3, 3, 3), 0.5)
+    b = st.uniform((4,), 0.5)
+    for pad in (0, 1, 2):
+        got = oracle.conv_epi(x, w, b, (), stride=2, pad=pad)
+        ref = _brute_conv2d_strided(x, w, b, 2, pad)
+        assert got.shape == ref.shape == (2, 4, (9 + 2 * pad - 3) // 2 + 1, (8 + 2 * pad - 3) // 2 + 1)
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_conv_stride2_delta_kernel_subsamples():
+    # centre tap, stride 2, pad 0: y[i, j] = x[2i + 1, 2j + 1] + b
+    st = _rng(12)
+    x = st.normal((1, 3, 9, 11))
+    w = np.zeros((3, 3, 3, 3), np.float32)
+    for c in range(3):
+        w[c, c, 1, 1] = 1.0
+    b = st.uniform((3,), 1.0)
+    y = oracle.conv_epi(x, w, b, (), stride=2)
+    ref = x[:, :, 1:-1:2, 1:-1:2].astype(np.float64) + b[None, :, None, None]
+    np.testing.assert_array_equal(y, ref)
+    # 3-D: tap (kd, kh, kw) = (2, 0, 1) picks x[2od + 2, 2oh, 2ow + 1]
+    x3 = st.normal((1, 2, 7, 7, 8))
+    w3 = np.zeros((1, 2, 3, 3, 3), np.float32)
+    w3[0, 1, 2, 0, 1] = 1.0
+    y3 = oracle.conv_epi(x3, w3, None, (), stride=2)
+    np.testing.assert_array_equal(y3[0, 0], x3[0, 1, 2:7:2, 0:5:2, 1:7:2])
+
+
 def test_conv_all_ones_closed_form():
     b = np.array([0.5, -1.0], dtype=np.float32)
     y2 = oracle.conv_epi(np.ones((1, 8, 5, 5), np.float32),
