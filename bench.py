@@ -417,6 +417,13 @@ def run_ours(args):
     if not args.no_ablation:
         ablation = fusion_ablation(fc, d[5], flush, stream, per[5])
 
+    # widened path beyond the headline workloads: stride-2 conv2d on the
+    # conv2d workload's input (runs on the CUDA-core kernel)
+    widened = None
+    if not args.no_ablation:
+        widened = {"conv2d_stride2_relu_hardswish_128x8x128x128": strided_conv(
+            fc, d[3], flush, stream, peaks)}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -437,6 +444,8 @@ def run_ours(args):
         line["e2e"] = e2e
     if ablation is not None:
         line["fusion_ablation"] = ablation
+    if widened is not None:
+        line["widened"] = widened
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_scale)
     if rank == 0:
@@ -483,6 +492,38 @@ def fusion_ablation(fc, d5, flush, stream, fused_ms_list, reps=10):
             "unfused_conv_ms": mc, "unfused_tail_ms": mt, "unfused_total_ms": mc + mt,
             "fused_ms": fused, "fused_speedup": (mc + mt) / fused,
             "tail_gbs": tail_bytes / (mt * 1e-3) / 1e9, "conv_variant": conv_variant}
+
+
+def strided_conv(fc, d3, flush, stream, peaks, reps=20):
+    """Stride-2 conv2d + ReLU + HardSwish on x [128,8,128,128] -> y
+    [128,64,63,63], L2 flushed before each call; roofline = max(FLOPs at the
+    FFMA peak, bytes at HBM bandwidth)."""
+    import torch
+    x, w, b = d3["x"], d3["w"], d3["b"]
+    N, C, H, W = x.shape
+    Ho, Wo = (H - 3) // 2 + 1, (W - 3) // 2 + 1
+    y = torch.empty((N, w.shape[0], Ho, Wo), dtype=torch.float32, device=x.device)
+    call = lambda: fc.fc_conv2d_epi(x, w, b, CHAIN_RH, y=y, stride=2)
+    call()
+    variant = fc.last_variant()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if fc.get_last_device_error() != 0:
+        raise RuntimeError("device status word set in the strided conv")
+    ms = statistics.median(ts)
+    flops = 2.0 * N * w.shape[0] * Ho * Wo * C * 9
+    nbytes = 4.0 * (x.numel() + w.numel() + b.numel() + y.numel())
+    pk, _, basis = pipe_peak_tflops(variant, peaks)
+    t_roof = max(flops / (pk * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    return {"variant": variant, "ms_median": ms, "gflops": flops / (ms * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms, "peak_basis": basis}
 
 
 def measure_e2e(args, fc, host, dev, stream, chain4_host):

@@ -220,8 +220,8 @@ def profile_read(entry: int):
     return ms.value, n.value
 
 
-def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
-    """Conv2d(k=3, stride 1, pad) + bias + elementwise ops -> y [N,CO,Ho,Wo]."""
+def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1):
+    """Conv2d(k=3, stride 1 or 2, pad) + bias + elementwise ops -> y [N,CO,Ho,Wo]."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -229,14 +229,14 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
     CO, C2, KH, KW = w.shape
     if C2 != C:
         raise ValueError("weight C_in mismatch")
-    Ho, Wo = H + 2 * pad - KH + 1, W + 2 * pad - KW + 1
+    Ho, Wo = (H + 2 * pad - KH) // stride + 1, (W + 2 * pad - KW) // stride + 1
     if y is None:
         y = torch.empty((N, CO, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
     if ws is None:
         ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
-    st = lib().fc_conv2d_epi(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad,
+    st = lib().fc_conv2d_epi(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, int(stride), pad,
                              ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
                              _stream_handle(stream))
     _check(st, "fc_conv2d_epi")
@@ -265,8 +265,8 @@ def fc_conv2d_epi_noalloc(x, w, y, bias=None, ops=(), pad=0, stream=None):
     return y
 
 
-def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
-    """Conv3d(k=3, stride 1, pad) + bias + elementwise ops."""
+def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1):
+    """Conv3d(k=3, stride 1 or 2, pad) + bias + elementwise ops."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -274,14 +274,15 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None):
     CO, C2, KD, KH, KW = w.shape
     if C2 != C:
         raise ValueError("weight C_in mismatch")
-    Do, Ho, Wo = D + 2 * pad - KD + 1, H + 2 * pad - KH + 1, W + 2 * pad - KW + 1
+    Do, Ho, Wo = ((D + 2 * pad - KD) // stride + 1, (H + 2 * pad - KH) // stride + 1,
+                  (W + 2 * pad - KW) // stride + 1)
     if y is None:
         y = torch.empty((N, CO, Do, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
     if ws is None:
         ws = _workspace(workspace_bytes(1, (N, C, D, H, W, CO, KD, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
-    st = lib().fc_conv3d_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, 1,
+    st = lib().fc_conv3d_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, int(stride),
                              pad, ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
                              _stream_handle(stream))
     _check(st, "fc_conv3d_epi")

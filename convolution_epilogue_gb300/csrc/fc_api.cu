@@ -260,8 +260,9 @@ fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
   if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || kH < 1 || kW < 1 ||
       stride < 1 || pad < 0)
     return FC_ERR_INVALID_ARG;
-  if (stride != 1 || kH != 3 || kW != 3 || pad > 2) return FC_ERR_UNSUPPORTED;
-  const int Ho = H + 2 * pad - kH + 1, Wo = W + 2 * pad - kW + 1;
+  if (stride > 2 || kH != 3 || kW != 3 || pad > 2) return FC_ERR_UNSUPPORTED;
+  if (H + 2 * pad < kH || W + 2 * pad < kW) return FC_ERR_INVALID_ARG;
+  const int Ho = (H + 2 * pad - kH) / stride + 1, Wo = (W + 2 * pad - kW) / stride + 1;
   if (Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
   if (!fits_int32((long long)N * C_in * H * W) ||
       !fits_int32((long long)N * C_out * Ho * Wo) ||
@@ -277,6 +278,7 @@ fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
   p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
   p.CO = C_out; p.KD = 1; p.KH = kH; p.KW = kW;
   p.pad_d = 0; p.pad = pad;
+  p.stride = stride;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 0;
@@ -290,10 +292,11 @@ fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
   if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 ||
       kH < 1 || kW < 1 || stride < 1 || pad < 0)
     return FC_ERR_INVALID_ARG;
-  if (stride != 1 || kD != 3 || kH != 3 || kW != 3 || pad > 2)
+  if (stride > 2 || kD != 3 || kH != 3 || kW != 3 || pad > 2)
     return FC_ERR_UNSUPPORTED;
-  const int Do = D + 2 * pad - kD + 1, Ho = H + 2 * pad - kH + 1,
-            Wo = W + 2 * pad - kW + 1;
+  if (D + 2 * pad < kD || H + 2 * pad < kH || W + 2 * pad < kW) return FC_ERR_INVALID_ARG;
+  const int Do = (D + 2 * pad - kD) / stride + 1, Ho = (H + 2 * pad - kH) / stride + 1,
+            Wo = (W + 2 * pad - kW) / stride + 1;
   if (Do < 1 || Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
   if (!fits_int32((long long)N * C_in * D * H * W) ||
       !fits_int32((long long)N * C_out * Do * Ho * Wo) ||
@@ -309,6 +312,7 @@ fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
   p.N = N; p.C = C_in; p.D = D; p.H = H; p.W = W;
   p.CO = C_out; p.KD = kD; p.KH = kH; p.KW = kW;
   p.pad_d = pad; p.pad = pad;
+  p.stride = stride;
   p.Do = Do; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 1;
@@ -343,6 +347,7 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   p.CO = C_out; p.KD = 1; p.KH = k; p.KW = k;
   // the equivalent conv: swapped + flipped weights, padding k - 1 - p
   p.pad_d = 0; p.pad = k - 1 - pad;
+  p.stride = 1;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 1;
   p.pool = 1;
@@ -377,6 +382,7 @@ fc_status fc_pool_mean_tail(const float *x, int N, int C, int H, int W, int k, i
 size_t fc_workspace_bytes(int entry, const int *d) {
   if (!d) return 0;
   ConvProblem p{};
+  p.stride = 1;  // the workspace does not depend on the stride
   switch (entry) {
     case 0:
       p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];

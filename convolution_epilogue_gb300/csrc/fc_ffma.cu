@@ -54,14 +54,16 @@ __global__ void ffma_pack_weights(const float *__restrict__ w, int C, int CO,
   }
 }
 
-template <int KD, int PR, int PC, bool POOL, int CHAIN>
+template <int KD, int PR, int PC, bool POOL, int CHAIN, int S>
 __global__ void __launch_bounds__(256)
 ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
                  float *__restrict__ partial, int n_th, int n_tw) {
   constexpr int K = 3;
   constexpr int TAPS = KD * K * K;
   constexpr int TW = 8 * PC, TH = 4 * PR;
-  constexpr int SW = TW + K - 1, SH = TH + K - 1;
+  // staged input extent of an output tile at stride S
+  constexpr int SW = (TW - 1) * S + K, SH = (TH - 1) * S + K;
+  static_assert(!POOL || S == 1, "the pooled path is stride 1");
   extern __shared__ __align__(16) float smem_f[];
   float (*s_w)[TAPS][kCoT] = reinterpret_cast<float (*)[TAPS][kCoT]>(smem_f);
   float (*s_in)[KD][SH][SW] =
@@ -99,7 +101,7 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
       int c = i % SW, r = (i / SW) % SH, kd = (i / (SW * SH)) % KD;
       int ci = i / (SW * SH * KD);
       int gci = ci0 + ci;
-      int id = od + kd - p.pad_d, ih = oh0 + r - p.pad, iw = ow0 + c - p.pad;
+      int id = od * S + kd - p.pad_d, ih = oh0 * S + r - p.pad, iw = ow0 * S + c - p.pad;
       float v = 0.0f;
       if (gci < p.C && id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 &&
           iw < p.W)
@@ -132,15 +134,16 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
           }
 #pragma unroll
           for (int a = 0; a < PR; ++a) {
-            float xin[PC + K - 1];
+            // input columns (gc*PC + c)*S + kw of staged row (gr*PR + a)*S + kh
+            float xin[(PC - 1) * S + K];
 #pragma unroll
-            for (int q = 0; q < PC + K - 1; ++q)
-              xin[q] = s_in[ci][kd][gr * PR + a + kh][gc * PC + q];
+            for (int q = 0; q < (PC - 1) * S + K; ++q)
+              xin[q] = s_in[ci][kd][(gr * PR + a) * S + kh][gc * PC * S + q];
 #pragma unroll
             for (int kw = 0; kw < K; ++kw)
 #pragma unroll
               for (int c = 0; c < PC; ++c) {
-                float xv = xin[c + kw];
+                float xv = xin[c * S + kw];
                 acc[a][c][0] = fmaf(xv, wv[kw][0].x, acc[a][c][0]);
                 acc[a][c][1] = fmaf(xv, wv[kw][0].y, acc[a][c][1]);
                 acc[a][c][2] = fmaf(xv, wv[kw][0].z, acc[a][c][2]);
@@ -244,7 +247,7 @@ pool_finish_kernel(const float *__restrict__ partial, int N, int CO, int T, doub
   }
 }
 
-template <int KD, int PR, int PC, bool POOL, int CHAIN>
+template <int KD, int PR, int PC, bool POOL, int CHAIN, int S = 1>
 cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
                        float *partial, cudaStream_t s) {
   constexpr int TW = 8 * PC, TH = 4 * PR;
@@ -253,8 +256,8 @@ cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   constexpr size_t smem = sizeof(float) * (kCiT * KD * 9 * kCoT +
-                                           kCiT * KD * (TH + 2) * (TW + 2));
-  auto kern = ffma_conv_kernel<KD, PR, PC, POOL, CHAIN>;
+                                           kCiT * KD * ((TH - 1) * S + 3) * ((TW - 1) * S + 3));
+  auto kern = ffma_conv_kernel<KD, PR, PC, POOL, CHAIN, S>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -264,18 +267,18 @@ cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
   return cudaGetLastError();
 }
 
-template <int KD>
+template <int KD, int S>
 cudaError_t launch_eltwise(const ConvProblem &p, const float *wp, int Cp, int COp,
                            cudaStream_t s) {
   switch (p.chain) {
-    case CHAIN_NONE: return launch_one<KD, 1, 4, false, CHAIN_NONE>(p, wp, Cp, COp, nullptr, s);
+    case CHAIN_NONE: return launch_one<KD, 1, 4, false, CHAIN_NONE, S>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_RELU_HARDSWISH:
-      return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH, S>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU, S>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP1_GELU>(p, wp, Cp, COp, nullptr, s);
-    default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP1_GELU, S>(p, wp, Cp, COp, nullptr, s);
+    default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC, S>(p, wp, Cp, COp, nullptr, s);
   }
 }
 
@@ -315,8 +318,12 @@ cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
     *launches += 2;
     return e;
   }
-  e = (p.KD == 1) ? launch_eltwise<1>(p, wp, Cp, COp, s)
-                  : launch_eltwise<3>(p, wp, Cp, COp, s);
+  if (p.stride == 2)
+    e = (p.KD == 1) ? launch_eltwise<1, 2>(p, wp, Cp, COp, s)
+                    : launch_eltwise<3, 2>(p, wp, Cp, COp, s);
+  else
+    e = (p.KD == 1) ? launch_eltwise<1, 1>(p, wp, Cp, COp, s)
+                    : launch_eltwise<3, 1>(p, wp, Cp, COp, s);
   *launches += 1;
   return e;
 }

@@ -152,6 +152,7 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   TcPlan q{};
   if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
+  if (p.stride > 1) return q;  // strided convs run on the CUDA-core kernel
   if (p.pool && U != 2) return q;
   if (p.pool && p.KD != 1) return q;
   q.prec = prec;

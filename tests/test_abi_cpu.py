@@ -72,7 +72,7 @@ def test_host_validation_rejects_before_launch(L):
     assert _conv2d(L, N=-1) == INVALID
     assert _conv2d(L, C=0) == INVALID
     assert _conv2d(L, stride=0) == INVALID
-    assert _conv2d(L, stride=2) == UNSUP
+    assert _conv2d(L, stride=3) == UNSUP  # stride 1 and 2 are supported
     assert _conv2d(L, k=5) == UNSUP
     assert _conv2d(L, pad=3) == UNSUP
     assert _conv2d(L, H=2) == INVALID  # Ho = 0

@@ -352,3 +352,49 @@ def test_unfused_conv_then_tail_matches_fused_entry():
     ref = oracle.convT_pool_mean(x, w, b)
     _check(fused, ref, "fused")
     _check(unfused, ref, "unfused")
+
+
+@pytest.mark.parametrize("shape,pad,ops", [
+    ((2, 8, 33, 37), 0, (("relu",), ("hardswish",))),
+    ((1, 5, 20, 71), 1, (("leaky_relu", 0.2), ("clamp", -1.0, 1.0), ("gelu_erf",))),
+    ((2, 16, 9, 12), 2, ()),
+])
+def test_conv2d_stride2(shape, pad, ops):
+    """Stride 2 (CUDA-core variant, chosen by AUTO) vs the oracle: odd and
+    even extents, pads 0-2, several tiles and ragged tails."""
+    st = synth.seeded(700 + pad)
+    N, C, H, W = shape
+    x = st.normal(shape)
+    w = st.uniform((70, C, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((70,), 0.1)
+    m = fc()
+    y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=2)
+    assert m.last_variant() == "ffma"
+    assert m.get_last_device_error() == 0
+    _check(y.cpu().numpy(), oracle.conv_epi(x, w, b, ops, stride=2, pad=pad), f"stride2 {shape} pad {pad}")
+
+
+def test_conv3d_stride2():
+    st = synth.seeded(710)
+    x = st.normal((2, 8, 9, 12, 35))
+    w = st.uniform((64, 8, 3, 3, 3), 1.0 / np.sqrt(216.0))
+    b = st.uniform((64,), 0.1)
+    s = st.normal((64,))
+    ops = (("leaky_relu", 0.2), ("add_channel", s), ("clamp", -1.0, 1.0), ("gelu_erf",))
+    m = fc()
+    y = m.fc_conv3d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=1, stride=2)
+    assert m.get_last_device_error() == 0
+    _check(y.cpu().numpy(), oracle.conv_epi(x, w, b, ops, stride=2, pad=1), "conv3d stride 2")
+
+
+def test_stride2_rejected_by_tensor_core_variants():
+    m = fc()
+    x = _dev(np.zeros((1, 8, 16, 16), np.float32))
+    w = _dev(np.zeros((64, 8, 3, 3), np.float32))
+    for v in ("tc_tf32x3", "tc_f16x3"):
+        m.set_variant(v)
+        try:
+            with pytest.raises(m.FcError):
+                m.fc_conv2d_epi(x, w, None, (), stride=2)
+        finally:
+            m.set_variant("auto")
