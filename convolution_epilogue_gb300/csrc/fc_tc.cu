@@ -114,6 +114,15 @@ struct TcPlan {
   int TAPS;
   int pairtaps;   // f16 with one plane per chunk: a K step spans two taps
   int U, R, RS, WT, RIN;
+  // Staging geometry.  RS is the pitch (pixels) between the M tile's output
+  // rows in a staged plane; RIN the input rows loaded per depth slice; LW
+  // the input pixels loaded per row; DSL the staged pixels per depth slice.
+  // Stride 2 (S2) stages each input slice deinterleaved into four
+  // sub-planes (even/odd rows x even/odd columns) of SR x RS pixels (SUB
+  // each), so that tap (kh, kw) reads sub-plane (kh & 1, kw & 1) at a shift
+  // of (kh >> 1, kw >> 1) -- again one shifted descriptor start per tap.
+  int S2, LW, SR, SUB, DSL;
+  uint8_t perm[28];  // K order of the taps (paired taps: increasing shifts)
   int NPIX;
   int plane_bytes;
   int a_stage_bytes;
@@ -148,11 +157,21 @@ static_assert(offsetof(SmemCtl, bias) % 16 == 0 && offsetof(SmemCtl, addend) % 1
               "16-byte aligned per-channel arrays");
 static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
+// Staged-pixel shift of tap t = (kd, kh, kw) from an M tile's first
+// pixel: stride 1 (kd*RIN + kh)*RS + kw; stride 2 sub-plane
+// (kh & 1, kw & 1) of depth slice kd, then (kh >> 1) rows and (kw >> 1)
+// columns.
+__host__ __device__ __forceinline__ int tap_shift(int t, const TcPlan &q) {
+  const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
+  if (!q.S2) return kd * q.DSL + kh * q.RS + kw;
+  return kd * q.DSL + (2 * (kh & 1) + (kw & 1)) * q.SUB + (kh >> 1) * q.RS + (kw >> 1);
+}
+
 // Plan with `U` M tiles per unit (pooling needs 2).
 TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   TcPlan q{};
   if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
-  if (p.stride > 1) return q;  // strided convs run on the CUDA-core kernel
+  if (p.stride > 2 || (p.stride == 2 && p.pool)) return q;
   if (p.pool && U != 2) return q;
   if (p.pool && p.KD != 1) return q;
   q.prec = prec;
@@ -165,24 +184,53 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.TAPS = p.KD * 9;
   q.pairtaps = (q.P == 1);
   q.KS = q.pairtaps ? cdiv(q.TAPS, 2) : q.TAPS;
-  const bool rowpack = (p.Wo + 2 <= 128);
+  q.S2 = p.stride == 2;
+  const int halo = q.S2 ? 1 : 2;  // staged columns past the tile's outputs
+  const bool rowpack = (p.Wo + halo <= 128);
   if (rowpack) {
-    q.RS = p.Wo + 2;
+    q.RS = p.Wo + halo;
     q.WT = p.Wo;
     q.n_ct = 1;
     q.R = p.pool ? 1 : 128 / q.RS;
   } else {
-    q.RS = 130;
+    q.RS = 128 + halo;
     q.WT = 128;
     q.n_ct = cdiv(p.Wo, 128);
     q.R = 1;
   }
   q.U = U;
-  q.RIN = q.U * q.R + 2;
-  // last staged pixel any MMA can touch (+1 for the paired-tap slice)
-  const int maxread = ((p.KD - 1) * q.RIN + 2) * q.RS + 2 + (q.U - 1) * q.R * q.RS + 127 + 1;
+  if (!q.S2) {
+    q.RIN = q.U * q.R + 2;
+    q.LW = q.RS;
+    q.DSL = q.RIN * q.RS;
+  } else {  // output rows u read input rows 2u + kh: 2UR + 1 rows, 2 RS columns
+    q.RIN = 2 * q.U * q.R + 1;
+    q.LW = 2 * q.RS;
+    q.SR = q.U * q.R + 1;
+    q.SUB = q.SR * q.RS;
+    q.DSL = 4 * q.SUB;
+  }
+  // K order of the taps: by increasing shift, so a K step's two paired taps
+  // are one positive LBO apart (stride 1: the natural order)
+  int shift[27];
+  for (int t = 0; t < q.TAPS; ++t) {
+    shift[t] = tap_shift(t, q);
+    q.perm[t] = (uint8_t)t;
+  }
+  for (int i = 1; i < q.TAPS; ++i)  // insertion sort by shift
+    for (int j = i; j > 0 && shift[q.perm[j]] < shift[q.perm[j - 1]]; --j) {
+      const uint8_t tmp = q.perm[j];
+      q.perm[j] = q.perm[j - 1];
+      q.perm[j - 1] = tmp;
+    }
+  for (int t = q.TAPS; t < 28; ++t) q.perm[t] = 255;  // zero-weight padding slot
+  // last staged pixel any MMA can touch: the largest tap shift (+1 for the
+  // paired zero-weight slice), the last tile, 128 rows
+  int maxshift = 0;
+  for (int t = 0; t < q.TAPS; ++t) maxshift = shift[t] > maxshift ? shift[t] : maxshift;
+  const int maxread = maxshift + 1 + (q.U - 1) * q.R * q.RS + 127;
   int npix = maxread + 1;
-  if (npix < p.KD * q.RIN * q.RS) npix = p.KD * q.RIN * q.RS;
+  if (npix < p.KD * q.DSL) npix = p.KD * q.DSL;
   q.NPIX = cdiv(npix, 8) * 8;
   q.plane_bytes = q.NPIX * 16;
   q.a_stage_bytes = 2 * q.P * q.plane_bytes;
@@ -352,10 +400,10 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
     const int cb = (int)(t / q.NCH);
     int tap, ci;
     if (q.pairtaps) {
-      tap = 2 * ks + k;
+      tap = q.perm[2 * ks + k];
       ci = c * q.chunk_ci + e;
     } else {
-      tap = ks;
+      tap = q.perm[ks];
       ci = c * q.chunk_ci + k * q.E + e;
     }
     const int co = cb * 64 + (row & 63);
@@ -413,10 +461,7 @@ __device__ __forceinline__ void store_slice(uint8_t *hi_dst, uint8_t *lo_dst, co
   *reinterpret_cast<uint4 *>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Staged-pixel shift of tap t = (kd, kh, kw): (kd*RIN + kh)*RS + kw.
-__device__ __forceinline__ int tap_shift(int t, int RIN, int RS) {
-  return ((t / 9) * RIN + (t / 3) % 3) * RS + t % 3;
-}
+
 
 // One staged row of one slice plane.
 struct RowJob {
@@ -430,23 +475,34 @@ struct RowJob {
 // chunk and the staging geometry.
 struct StageSrc {
   long xn;        // element index of image n
-  int od, oh0, iw0, ci0;
+  int id0, ih0, iw0, ci0;  // first input depth, row, column; first channel
 };
 
-__device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, const TcPlan &q,
-                                          const ConvProblem &p, int nrows, int E) {
+// Input row `job` of a stage: slice plane, depth slice, then the row r of
+// the RIN loaded per depth.  Its staged pixels start at jb.dst; the input
+// column cc lands at staged column col_px(cc) of that row.
+__host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, const TcPlan &q,
+                                                   const ConvProblem &p, int nrows, int E, bool s2) {
   RowJob jb;
   // a stage holds at most 2 slice planes of at most 3 depth slices
   const int plane = job >= nrows ? 1 : 0;
   const int sr = job - plane * nrows;
   const int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
   const int r = sr - kdp * q.RIN;
-  const int id = ss.od + kdp - p.pad_d, ih = ss.oh0 + r - p.pad;
+  const int id = ss.id0 + kdp, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
   jb.rowbase = ss.xn + ((long)id * p.H + ih) * p.W + ss.iw0;
   jb.cbase = ss.ci0 + plane * E;
-  jb.dst = (uint32_t)(plane * q.plane_bytes + sr * q.RS * 16);
+  // stride 2: even / odd rows go to sub-plane row r >> 1 of their parity
+  const int row_px = s2 ? 2 * (r & 1) * q.SUB + (r >> 1) * q.RS : r * q.RS;
+  jb.dst = (uint32_t)(plane * q.plane_bytes + (kdp * q.DSL + row_px) * 16);
   return jb;
+}
+
+// Staged column of input column cc of a loaded row (stride 2: even / odd
+// columns to their sub-planes).
+__host__ __device__ __forceinline__ int col_px(int cc, int s2sub) {
+  return s2sub ? (cc & 1) * s2sub + (cc >> 1) : cc;
 }
 
 // Loads E channels of staged pixel cc of a row (zero outside the image).
@@ -460,20 +516,35 @@ __device__ __forceinline__ void load_pixel(const float *__restrict__ x, const Ro
                                         : 0.0f;
 }
 
-// Main job: pixels cc = lane + 32k (k < NCOL) of one row, all loads in
+// A loaded row of LW pixels has G = LW / 32 full 32-pixel groups, taken by
+// ceil(G / 4) main jobs of at most 4 groups each (stride-2 column strips
+// load 258 pixels a row: two main jobs); the LW - 32 G pixels left over go
+// to tail jobs.  Main job J covers row J / parts, groups 4 (J % parts) on.
+struct MainJob { int row, c0, ngroups; };
+__host__ __device__ __forceinline__ MainJob main_job(int J, int parts, int G) {
+  MainJob m;
+  m.row = J / parts;
+  const int part = J - m.row * parts;
+  m.c0 = 128 * part;
+  m.ngroups = G - 4 * part < 4 ? G - 4 * part : 4;
+  return m;
+}
+
+// Main job: pixels cc = c0 + lane + 32k (k < NCOL) of one row, all loads in
 // flight before the first store.  `wait_stage` runs between the loads and
 // the stores (the stage may still be in use while the loads travel).
 template <int PREC, int E, int NCOL, class Wait>
-__device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJob &jb, long cstride,
-                                         int iw0, int W, int C, uint8_t *stage, int lo_off, int lane,
-                                         float &amax, Wait &&wait_stage) {
+__device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJob &jb, int c0,
+                                         long cstride, int iw0, int W, int C, uint8_t *stage,
+                                         int lo_off, int lane, float &amax, int s2sub,
+                                         Wait &&wait_stage) {
   float v[NCOL][E];
 #pragma unroll
-  for (int k = 0; k < NCOL; ++k) load_pixel<E>(x, jb, lane + 32 * k, cstride, iw0, W, C, v[k]);
+  for (int k = 0; k < NCOL; ++k) load_pixel<E>(x, jb, c0 + lane + 32 * k, cstride, iw0, W, C, v[k]);
   if (!wait_stage()) return false;
 #pragma unroll
   for (int k = 0; k < NCOL; ++k) {
-    const uint32_t o = jb.dst + (uint32_t)(lane + 32 * k) * 16u;
+    const uint32_t o = jb.dst + (uint32_t)col_px(c0 + lane + 32 * k, s2sub) * 16u;
     store_slice<PREC, E>(stage + o, stage + lo_off + o, v[k], amax);
   }
   return true;
@@ -572,7 +643,7 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL, int U>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial) {
@@ -618,12 +689,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   if (tid < q.KS) {
     uint32_t off16, lbo16;
     if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
-      const int t0 = 2 * tid;
-      const int s0 = tap_shift(t0, q.RIN, q.RS);
+      const int t0 = q.perm[2 * tid], t1 = q.perm[2 * tid + 1];
+      const int s0 = tap_shift(t0, q);
       off16 = (uint32_t)s0;
-      lbo16 = (t0 + 1 < q.TAPS) ? (uint32_t)(tap_shift(t0 + 1, q.RIN, q.RS) - s0) : 1u;
+      lbo16 = (t1 < q.TAPS) ? (uint32_t)(tap_shift(t1, q) - s0) : 1u;
     } else {           // slices: planes 0 and 1 of tap ks
-      off16 = (uint32_t)tap_shift(tid, q.RIN, q.RS);
+      off16 = (uint32_t)tap_shift(q.perm[tid], q);
       lbo16 = (uint32_t)(q.plane_bytes >> 4);
     }
     ctl->kdelta[tid] = (off16 & 0x3FFFu) | ((lbo16 & 0x3FFFu) << 16);
@@ -669,14 +740,19 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const long cstride = (long)p.D * HW;
     // A stage is filled by main jobs (one row: its full 32-pixel column
     // groups) and tail jobs (32 of the rows' remaining pixels each).
-    const int ncm = q.RS >> 5;
-    const int tail = q.RS - 32 * ncm;
-    const int mjobs = ncm ? jobs : 0;
+    const int G = q.LW >> 5;
+    // stride 1 loads at most 130 pixels a row: one main job, or none for
+    // rows shorter than 32 pixels
+    const int parts = S2 ? (G + 3) >> 2 : (G ? 1 : 0);
+    const int tail = q.LW - 32 * G;
+    const int mjobs = jobs * parts;
     const int njobs = mjobs + cdiv(jobs * tail, 32);
-    // Pixels past the staged rows are only read by discarded M rows; zero
-    // them once so those rows stay finite.
+    const int s2sub = S2 ? q.SUB : 0;
+    // Staged pixels no row job writes (past the staged rows; with stride 2
+    // also the odd-row sub-planes' last row) are only read by discarded M
+    // rows; zero them once so those rows stay finite.
     {
-      const int tail0 = nrows * q.RS;
+      const int tail0 = S2 ? 0 : nrows * q.RS;
       for (int st = 0; st < q.S; ++st)
         for (int pl = 0; pl < 2 * q.P; ++pl)
           for (int px = tail0 + pt; px < q.NPIX; px += kProdThreads)
@@ -693,9 +769,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q);
       StageSrc ss;
-      ss.od = up.od;
-      ss.oh0 = up.rt * U * q.R;  // first output row of the unit
-      ss.iw0 = up.ct * q.WT - p.pad;
+      const int st = p.stride;
+      ss.id0 = up.od * st - p.pad_d;
+      ss.ih0 = up.rt * U * q.R * st - p.pad;  // input row of the unit's first output row
+      ss.iw0 = up.ct * q.WT * st - p.pad;
       ss.xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = (int)(g % q.S);
@@ -736,27 +813,28 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         if (J < 0) J += kProdWarps;
         for (; ok && J < njobs; J += kProdWarps) {
           if (J < mjobs) {
-            const RowJob jb = row_job(J, ss, q, p, nrows, E);
-            switch (ncm) {
-              case 1: ok = fill_row<PREC, E, 1>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
-              case 2: ok = fill_row<PREC, E, 2>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
-              case 3: ok = fill_row<PREC, E, 3>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
-              default: ok = fill_row<PREC, E, 4>(p.x, jb, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, wait_stage); break;
+            const MainJob mj = main_job(J, parts, G);
+            const RowJob jb = row_job(mj.row, ss, q, p, nrows, E, S2);
+            switch (mj.ngroups) {
+              case 1: ok = fill_row<PREC, E, 1>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              case 2: ok = fill_row<PREC, E, 2>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              case 3: ok = fill_row<PREC, E, 3>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              default: ok = fill_row<PREC, E, 4>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
             }
           } else {
             // lane -> (row job, tail pixel) pair
             const int l = (J - mjobs) * 32 + lane;
             const int job = l / tail;
-            const int cc = 32 * ncm + (l - job * tail);
+            const int cc = 32 * G + (l - job * tail);
             float v[E];
             RowJob jb;
             if (job < jobs) {
-              jb = row_job(job, ss, q, p, nrows, E);
+              jb = row_job(job, ss, q, p, nrows, E, S2);
               load_pixel<E>(p.x, jb, cc, cstride, ss.iw0, p.W, p.C, v);
             }
             ok = wait_stage();
             if (ok && job < jobs) {
-              const uint32_t o = jb.dst + (uint32_t)cc * 16u;
+              const uint32_t o = jb.dst + (uint32_t)col_px(cc, s2sub) * 16u;
               store_slice<PREC, E>(stage + o, stage + lo_off + o, v, amax);
             }
           }
@@ -1074,10 +1152,10 @@ __global__ void selftest_wait_kernel(unsigned int *status, uint64_t limit_ns) {
 
 int g_num_sms = 0;
 
-template <int PREC, int CHAIN, bool POOL, int U>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                           float *partial, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U>;
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1094,18 +1172,18 @@ cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *
   return cudaGetLastError();
 }
 
-template <int PREC, int U>
+template <int PREC, int U, bool S2>
 cudaError_t launch_chain(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                          float *partial, cudaStream_t s) {
   switch (p.chain) {
-    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U>(p, q, bimg, partial, s);
+    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U, S2>(p, q, bimg, partial, s);
     case CHAIN_RELU_HARDSWISH:
-      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U, S2>(p, q, bimg, partial, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U, S2>(p, q, bimg, partial, s);
     case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U>(p, q, bimg, partial, s);
-    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U, S2>(p, q, bimg, partial, s);
+    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U, S2>(p, q, bimg, partial, s);
   }
 }
 
@@ -1113,8 +1191,13 @@ template <int PREC>
 cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                         float *partial, cudaStream_t s) {
   if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, s);
-  return q.U == 2 ? launch_chain<PREC, 2>(p, q, bimg, partial, s)
-                  : launch_chain<PREC, 1>(p, q, bimg, partial, s);
+  // stride 2 (even / odd sub-plane staging) is its own instance, so the
+  // stride-1 producer carries none of its index arithmetic
+  if (q.S2)
+    return q.U == 2 ? launch_chain<PREC, 2, true>(p, q, bimg, partial, s)
+                    : launch_chain<PREC, 1, true>(p, q, bimg, partial, s);
+  return q.U == 2 ? launch_chain<PREC, 2, false>(p, q, bimg, partial, s)
+                  : launch_chain<PREC, 1, false>(p, q, bimg, partial, s);
 }
 
 }  // namespace

@@ -117,8 +117,8 @@ typedef enum {
  * (floor), output (oh, ow) reading input rows oh*stride + kh - pad.
  * Supported: stride 1 or 2, kH = kW = 3, 0 <= pad <= 2, 1 <= C_in,
  * 1 <= C_out, H + 2 pad >= kH, W + 2 pad >= kW, and every tensor below 2^31
- * elements; stride 2 runs on the FFMA variant only (AUTO picks it; the
- * tensor-core variants return FC_ERR_UNSUPPORTED).  N = 0 is a valid empty
+ * elements; every variant takes stride 2 (the tensor-core variants stage
+ * the input as even/odd row x column sub-planes).  N = 0 is a valid empty
  * call (nothing is launched). */
 FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,
@@ -149,8 +149,8 @@ FC_API fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, i
 /* Conv3d + bias + elementwise epilogue chain; same ops as fc_conv2d_epi.
  * x [N][C_in][D][H][W]; w [C_out][C_in][kD][kH][kW];
  * y [N][C_out][Do][Ho][Wo], each extent (in + 2 pad - k) / stride + 1.
- * Supported: stride 1 or 2 (stride 2 on the FFMA variant only, as for
- * fc_conv2d_epi), kD = kH = kW = 3, 0 <= pad <= 2. */
+ * Supported: stride 1 or 2 (on every variant, as for fc_conv2d_epi),
+ * kD = kH = kW = 3, 0 <= pad <= 2. */
 FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
                         const float *w, int C_out, int kD, int kH, int kW,
                         int stride, int pad, const fc_epilogue *epi, float *y,

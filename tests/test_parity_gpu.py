@@ -354,47 +354,47 @@ def test_unfused_conv_then_tail_matches_fused_entry():
     _check(unfused, ref, "unfused")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("shape,pad,ops", [
     ((2, 8, 33, 37), 0, (("relu",), ("hardswish",))),
     ((1, 5, 20, 71), 1, (("leaky_relu", 0.2), ("clamp", -1.0, 1.0), ("gelu_erf",))),
     ((2, 16, 9, 12), 2, ()),
+    ((1, 8, 11, 300), 1, (("relu",),)),       # 128-column strips plus a tail
+    ((2, 64, 20, 150), 1, (("hardswish",),)),  # several channel chunks
 ])
-def test_conv2d_stride2(shape, pad, ops):
-    """Stride 2 (CUDA-core variant, chosen by AUTO) vs the oracle: odd and
-    even extents, pads 0-2, several tiles and ragged tails."""
-    st = synth.seeded(700 + pad)
+def test_conv2d_stride2(variant, shape, pad, ops):
+    """Stride 2 vs the oracle for every variant: odd and even extents, pads
+    0-2, row-packed tiles and column strips, ragged tails.  The tensor-core
+    variants stage the input in even/odd row x column sub-planes."""
+    st = synth.seeded(700 + pad + shape[1])
     N, C, H, W = shape
     x = st.normal(shape)
     w = st.uniform((70, C, 3, 3), 1.0 / np.sqrt(9.0 * C))
     b = st.uniform((70,), 0.1)
+    got = _run_conv_strided(variant, x, w, b, ops, pad, 2)
+    _check(got, oracle.conv_epi(x, w, b, ops, stride=2, pad=pad), f"{variant} stride2 {shape} pad {pad}")
+
+
+def _run_conv_strided(variant, x, w, b, ops, pad, stride):
     m = fc()
-    y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=2)
-    assert m.last_variant() == "ffma"
-    assert m.get_last_device_error() == 0
-    _check(y.cpu().numpy(), oracle.conv_epi(x, w, b, ops, stride=2, pad=pad), f"stride2 {shape} pad {pad}")
+    m.set_variant(variant)
+    try:
+        f = m.fc_conv2d_epi if x.ndim == 4 else m.fc_conv3d_epi
+        y = f(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=stride)
+        assert m.last_variant() == variant
+        assert m.get_last_device_error() == 0
+        return y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
 
 
-def test_conv3d_stride2():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_conv3d_stride2(variant):
     st = synth.seeded(710)
     x = st.normal((2, 8, 9, 12, 35))
     w = st.uniform((64, 8, 3, 3, 3), 1.0 / np.sqrt(216.0))
     b = st.uniform((64,), 0.1)
     s = st.normal((64,))
     ops = (("leaky_relu", 0.2), ("add_channel", s), ("clamp", -1.0, 1.0), ("gelu_erf",))
-    m = fc()
-    y = m.fc_conv3d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=1, stride=2)
-    assert m.get_last_device_error() == 0
-    _check(y.cpu().numpy(), oracle.conv_epi(x, w, b, ops, stride=2, pad=1), "conv3d stride 2")
-
-
-def test_stride2_rejected_by_tensor_core_variants():
-    m = fc()
-    x = _dev(np.zeros((1, 8, 16, 16), np.float32))
-    w = _dev(np.zeros((64, 8, 3, 3), np.float32))
-    for v in ("tc_tf32x3", "tc_f16x3"):
-        m.set_variant(v)
-        try:
-            with pytest.raises(m.FcError):
-                m.fc_conv2d_epi(x, w, None, (), stride=2)
-        finally:
-            m.set_variant("auto")
+    got = _run_conv_strided(variant, x, w, b, ops, 1, 2)
+    _check(got, oracle.conv_epi(x, w, b, ops, stride=2, pad=1), f"{variant} conv3d stride 2")
