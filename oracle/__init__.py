@@ -81,10 +81,11 @@ def _load():
             lib.or_apply_op.argtypes = [I, D, D, P, I, D]
             lib.or_conv_epi.restype = None
             lib.or_conv_epi.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I,
-                                        P, I, P, P, P, P, P]
+                                        I, P, I, P, P, P, P, P]
             lib.or_conv_epi_points.restype = None
             lib.or_conv_epi_points.argtypes = [P, I, I, I, I, I, P, I, I, I, I,
-                                               I, I, P, I, P, P, P, P, P, L, P]
+                                               I, I, I, P, I, P, P, P, P, P, L,
+                                               P]
             lib.or_convT2d.restype = None
             lib.or_convT2d.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P]
             lib.or_maxpool2d.restype = None
@@ -140,9 +141,9 @@ def apply_op(name, v, a=0.0, b=0.0, chan=None, co=0):
                            float(v))
 
 
-def conv_out_extent(n_in, k, stride=1, pad=0):
-    """Output extent of a cross-correlation: (n + 2p - k) // s + 1."""
-    return (n_in + 2 * pad - k) // stride + 1
+def conv_out_extent(n_in, k, stride=1, pad=0, dilation=1):
+    """Output extent of a cross-correlation: (n + 2p - d(k-1) - 1) // s + 1."""
+    return (n_in + 2 * pad - dilation * (k - 1) - 1) // stride + 1
 
 
 def convT_out_extent(n_in, k, stride=1, pad=0, out_pad=0):
@@ -150,9 +151,10 @@ def convT_out_extent(n_in, k, stride=1, pad=0, out_pad=0):
     return (n_in - 1) * stride - 2 * pad + k + out_pad
 
 
-def conv_epi(x, w, bias, ops=(), stride=1, pad=0):
+def conv_epi(x, w, bias, ops=(), stride=1, pad=0, dilation=1):
     """Conv2d (x [N,C,H,W], w [CO,C,kh,kw]) or Conv3d (x [N,C,D,H,W],
-    w [CO,C,kd,kh,kw]) + bias, then the elementwise chain.  Returns float64."""
+    w [CO,C,kd,kh,kw]) + bias, then the elementwise chain.  Output o reads
+    input o*stride + k*dilation - pad on every axis.  Returns float64."""
     lib = _load()
     x = _f32(x)
     w = _f32(w)
@@ -166,18 +168,18 @@ def conv_epi(x, w, bias, ops=(), stride=1, pad=0):
         N, C, D, H, W = x.shape
         CO, _, KD, KH, KW = w.shape
     pad_d = 0 if x.ndim == 4 else pad
-    Do = conv_out_extent(D, KD, stride, pad_d)
-    Ho = conv_out_extent(H, KH, stride, pad)
-    Wo = conv_out_extent(W, KW, stride, pad)
+    Do = conv_out_extent(D, KD, stride, pad_d, dilation)
+    Ho = conv_out_extent(H, KH, stride, pad, dilation)
+    Wo = conv_out_extent(W, KW, stride, pad, dilation)
     y = np.empty((N, CO, Do, Ho, Wo), dtype=np.float64)
     n, kinds, a, b, chan = _chain(ops, CO)
     lib.or_conv_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, stride,
-                    pad, _ptr(bias), n, _ptr(kinds), _ptr(a), _ptr(b),
+                    pad, dilation, _ptr(bias), n, _ptr(kinds), _ptr(a), _ptr(b),
                     _ptr(chan), _ptr(y))
     return y.reshape((N, CO, Ho, Wo)) if x.ndim == 4 else y
 
 
-def conv_epi_points(x, w, bias, ops, flat_idx, stride=1, pad=0):
+def conv_epi_points(x, w, bias, ops, flat_idx, stride=1, pad=0, dilation=1):
     """conv_epi evaluated at the given flat output indices only."""
     lib = _load()
     x = _f32(x)
@@ -194,7 +196,7 @@ def conv_epi_points(x, w, bias, ops, flat_idx, stride=1, pad=0):
     out = np.empty(idx.shape[0], dtype=np.float64)
     n, kinds, a, b, chan = _chain(ops, CO)
     lib.or_conv_epi_points(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW,
-                           stride, pad, _ptr(bias), n, _ptr(kinds), _ptr(a),
+                           stride, pad, dilation, _ptr(bias), n, _ptr(kinds), _ptr(a),
                            _ptr(b), _ptr(chan), _ptr(idx), idx.shape[0],
                            _ptr(out))
     return out

@@ -11,11 +11,15 @@
  * What each function follows (the pages are three POPCORNBENCH reasoning
  * traces; each is cited by its trace name and the paragraph topic):
  *  - or_conv: the definition of a PyTorch cross-correlation with bias,
- *    stride 1, no dilation, groups 1: Kimi-K2.6 l2_p57 trace, "Simplest
- *    kernel" paragraph (one output = bias + sum over c_in, kh, kw of
- *    input * weight) and the Kimi-K2.6 l2_p90 trace, conv3d FLOP paragraph
- *    (sum over C_in*Kd*Kh*Kw).  Output extent (H + 2p - k)/s + 1, which is
- *    H - k + 1 for the traces' padding 0.
+ *    groups 1: Kimi-K2.6 l2_p57 trace, "Simplest kernel" paragraph (one
+ *    output = bias + sum over c_in, kh, kw of input * weight) and the
+ *    Kimi-K2.6 l2_p90 trace, conv3d FLOP paragraph (sum over
+ *    C_in*Kd*Kh*Kw).  The traces' layers use stride 1, padding 0 and
+ *    dilation 1 (l2_p57, output-size paragraph); for the general layer,
+ *    output o reads input o*s + k*d - p along each axis, and the extent is
+ *    (H + 2p - d(k-1) - 1)/s + 1 (floor), the formula the l2_p10 trace
+ *    states for a pooling window with dilation d.  H - k + 1 for the
+ *    traces' own layers.
  *  - or_convT2d: the transposed convolution in SCATTER form: every input
  *    element x[n,ci,i,j] adds x * W[ci,co,kh,kw] to output position
  *    (i*s + kh - p, j*s + kw - p), positions outside the output dropped.
@@ -92,26 +96,26 @@ static double apply_chain(int nops, const int *kinds, const double *a,
   return v;
 }
 
-static inline int out_extent(int in, int k, int s, int p) {
-  return (in + 2 * p - k) / s + 1;
+static inline int out_extent(int in, int k, int s, int p, int d) {
+  return (in + 2 * p - d * (k - 1) - 1) / s + 1;
 }
 
 /* One conv output (cross-correlation + bias), summed in double. 2-D is the
  * case D = KD = 1. */
 static double conv_one(const float *x, int C, int D, int H, int W,
                        const float *w, int KD, int KH, int KW, int stride,
-                       int pad_d, int pad, const float *bias, int n, int co,
-                       int od, int oh, int ow) {
+                       int pad_d, int pad, int dil, const float *bias, int n,
+                       int co, int od, int oh, int ow) {
   double acc = bias ? (double)bias[co] : 0.0;
   for (int ci = 0; ci < C; ++ci)
     for (int kd = 0; kd < KD; ++kd) {
-      int id = od * stride + kd - pad_d;
+      int id = od * stride + kd * dil - pad_d;
       if (id < 0 || id >= D) continue;
       for (int kh = 0; kh < KH; ++kh) {
-        int ih = oh * stride + kh - pad;
+        int ih = oh * stride + kh * dil - pad;
         if (ih < 0 || ih >= H) continue;
         for (int kw = 0; kw < KW; ++kw) {
-          int iw = ow * stride + kw - pad;
+          int iw = ow * stride + kw * dil - pad;
           if (iw < 0 || iw >= W) continue;
           double xv = x[((((size_t)n * C + ci) * D + id) * H + ih) * W + iw];
           double wv = w[((((size_t)co * C + ci) * KD + kd) * KH + kh) * KW + kw];
@@ -126,13 +130,13 @@ static double conv_one(const float *x, int C, int D, int H, int W,
  * elementwise chain.  y: [N][CO][Do][Ho][Wo] doubles. */
 void or_conv_epi(const float *x, int N, int C, int D, int H, int W,
                  const float *w, int CO, int KD, int KH, int KW, int stride,
-                 int pad, const float *bias, int nops, const int *kinds,
-                 const double *a, const double *b, const float *chan,
-                 double *y) {
+                 int pad, int dil, const float *bias, int nops,
+                 const int *kinds, const double *a, const double *b,
+                 const float *chan, double *y) {
   int pad_d = (D == 1 && KD == 1) ? 0 : pad;
-  int Do = out_extent(D, KD, stride, pad_d);
-  int Ho = out_extent(H, KH, stride, pad);
-  int Wo = out_extent(W, KW, stride, pad);
+  int Do = out_extent(D, KD, stride, pad_d, dil);
+  int Ho = out_extent(H, KH, stride, pad, dil);
+  int Wo = out_extent(W, KW, stride, pad, dil);
   long plane = (long)Do * Ho * Wo;
 #pragma omp parallel for collapse(2) schedule(dynamic)
   for (int n = 0; n < N; ++n)
@@ -142,7 +146,7 @@ void or_conv_epi(const float *x, int N, int C, int D, int H, int W,
         for (int oh = 0; oh < Ho; ++oh)
           for (int ow = 0; ow < Wo; ++ow) {
             double v = conv_one(x, C, D, H, W, w, KD, KH, KW, stride, pad_d,
-                                pad, bias, n, co, od, oh, ow);
+                                pad, dil, bias, n, co, od, oh, ow);
             yp[((size_t)od * Ho + oh) * Wo + ow] =
                 apply_chain(nops, kinds, a, b, chan, CO, co, v);
           }
@@ -154,14 +158,14 @@ void or_conv_epi(const float *x, int N, int C, int D, int H, int W,
  * sample of their outputs. */
 void or_conv_epi_points(const float *x, int N, int C, int D, int H, int W,
                         const float *w, int CO, int KD, int KH, int KW,
-                        int stride, int pad, const float *bias, int nops,
-                        const int *kinds, const double *a, const double *b,
-                        const float *chan, const int64_t *idx, long npts,
-                        double *out) {
+                        int stride, int pad, int dil, const float *bias,
+                        int nops, const int *kinds, const double *a,
+                        const double *b, const float *chan, const int64_t *idx,
+                        long npts, double *out) {
   int pad_d = (D == 1 && KD == 1) ? 0 : pad;
-  int Do = out_extent(D, KD, stride, pad_d);
-  int Ho = out_extent(H, KH, stride, pad);
-  int Wo = out_extent(W, KW, stride, pad);
+  int Do = out_extent(D, KD, stride, pad_d, dil);
+  int Ho = out_extent(H, KH, stride, pad, dil);
+  int Wo = out_extent(W, KW, stride, pad, dil);
   (void)N;
 #pragma omp parallel for schedule(static)
   for (long i = 0; i < npts; ++i) {
@@ -171,8 +175,8 @@ void or_conv_epi_points(const float *x, int N, int C, int D, int H, int W,
     int od = (int)(t % Do); t /= Do;
     int co = (int)(t % CO); t /= CO;
     int n = (int)t;
-    double v = conv_one(x, C, D, H, W, w, KD, KH, KW, stride, pad_d, pad, bias,
-                        n, co, od, oh, ow);
+    double v = conv_one(x, C, D, H, W, w, KD, KH, KW, stride, pad_d, pad, dil,
+                        bias, n, co, od, oh, ow);
     out[i] = apply_chain(nops, kinds, a, b, chan, CO, co, v);
   }
 }

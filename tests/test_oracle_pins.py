@@ -215,6 +215,88 @@ def test_conv_stride2_delta_kernel_subsamples():
     np.testing.assert_array_equal(y3[0, 0], x3[0, 1, 2:7:2, 0:5:2, 1:7:2])
 
 
+def _brute_conv2d_dilated(x, w, b, stride, pad, dil):
+    """Independent loop for a dilated, strided conv: out (oh, ow) reads input
+    row oh*stride + kh*dil - pad and column ow*stride + kw*dil - pad; the
+    extent counts the outputs whose window start oh*stride - pad keeps the
+    last tap (k-1)*dil inside the padded input."""
+    N, C, H, W = x.shape
+    CO, _, K, _ = w.shape
+    span = (K - 1) * dil + 1
+    Ho = len([o for o in range(H + 2 * pad) if o * stride + span <= H + 2 * pad])
+    Wo = len([o for o in range(W + 2 * pad) if o * stride + span <= W + 2 * pad])
+    y = np.zeros((N, CO, Ho, Wo))
+    for n, co, oh, ow in np.ndindex(N, CO, Ho, Wo):
+        s = float(b[co])
+        for ci in range(C):
+            for kh in range(K):
+                for kw in range(K):
+                    ih, iw = oh * stride + kh * dil - pad, ow * stride + kw * dil - pad
+                    if 0 <= ih < H and 0 <= iw < W:
+                        s += float(x[n, ci, ih, iw]) * float(w[co, ci, kh, kw])
+        y[n, co, oh, ow] = s
+    return y
+
+
+def test_conv2d_dilation2_brute_force_and_extent():
+    st = _rng(13)
+    x = st.normal((2, 3, 11, 9))
+    w = st.uniform((4, 3, 3, 3), 0.5)
+    b = st.uniform((4,), 0.5)
+    for stride in (1, 2):
+        for pad in (0, 1, 2, 3, 4):
+            got = oracle.conv_epi(x, w, b, (), stride=stride, pad=pad, dilation=2)
+            ref = _brute_conv2d_dilated(x, w, b, stride, pad, 2)
+            assert got.shape == ref.shape
+            assert got.shape[2:] == (oracle.conv_out_extent(11, 3, stride, pad, 2),
+                                     oracle.conv_out_extent(9, 3, stride, pad, 2))
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    # the extent of a 3-tap window at dilation 2 (span 5) over 10 inputs, pad 0
+    assert oracle.conv_out_extent(10, 3, 1, 0, 2) == 6
+    assert oracle.conv_out_extent(10, 3, 2, 2, 2) == 5  # "same"-padded, stride 2
+
+
+def test_conv_dilation2_equals_zero_inserted_kernel():
+    """A 3-tap kernel at dilation 2 is the 5-tap kernel with zeros between
+    its taps at dilation 1 (2-D and 3-D; same terms in the same order)."""
+    st = _rng(14)
+    x = st.normal((2, 3, 10, 12))
+    w = st.uniform((4, 3, 3, 3), 0.5)
+    b = st.uniform((4,), 0.5)
+    w5 = np.zeros((4, 3, 5, 5), np.float32)
+    w5[:, :, ::2, ::2] = w
+    for stride, pad in ((1, 2), (2, 1), (1, 0)):
+        np.testing.assert_array_equal(
+            oracle.conv_epi(x, w, b, (), stride=stride, pad=pad, dilation=2),
+            oracle.conv_epi(x, w5, b, (), stride=stride, pad=pad))
+    x3 = st.normal((1, 2, 7, 8, 9))
+    w3 = st.uniform((3, 2, 3, 3, 3), 0.5)
+    w35 = np.zeros((3, 2, 5, 5, 5), np.float32)
+    w35[:, :, ::2, ::2, ::2] = w3
+    np.testing.assert_array_equal(
+        oracle.conv_epi(x3, w3, None, (), stride=1, pad=2, dilation=2),
+        oracle.conv_epi(x3, w35, None, (), stride=1, pad=2))
+
+
+def test_conv_dilation2_delta_kernel_shifts():
+    # tap (kh, kw) = (2, 0) at dilation 2, pad 2: y[i, j] = x[i + 2, j - 2]
+    st = _rng(15)
+    x = st.normal((1, 1, 8, 9))
+    w = np.zeros((1, 1, 3, 3), np.float32)
+    w[0, 0, 2, 0] = 1.0
+    y = oracle.conv_epi(x, w, None, (), pad=2, dilation=2)
+    ref = np.zeros((8, 9))
+    ref[:6, 2:] = x[0, 0, 2:, :7]
+    np.testing.assert_array_equal(y[0, 0], ref)
+    # 3-D, stride 2: tap (kd, kh, kw) = (1, 2, 1) at dilation 2, pad 0 picks
+    # x[2od + 2, 2oh + 4, 2ow + 2]
+    x3 = st.normal((1, 1, 9, 10, 11))
+    w3 = np.zeros((1, 1, 3, 3, 3), np.float32)
+    w3[0, 0, 1, 2, 1] = 1.0
+    y3 = oracle.conv_epi(x3, w3, None, (), stride=2, dilation=2)
+    np.testing.assert_array_equal(y3[0, 0], x3[0, 0, 2:7:2, 4:10:2, 2:9:2])
+
+
 def test_conv_all_ones_closed_form():
     b = np.array([0.5, -1.0], dtype=np.float32)
     y2 = oracle.conv_epi(np.ones((1, 8, 5, 5), np.float32),
