@@ -417,12 +417,16 @@ def run_ours(args):
     if not args.no_ablation:
         ablation = fusion_ablation(fc, d[5], flush, stream, per[5])
 
-    # widened path beyond the headline workloads: stride-2 conv2d on the
-    # conv2d workload's input (runs on the CUDA-core kernel)
+    # widened layer parameters beyond the headline workloads, on the conv2d
+    # workload's input: stride 2, and dilation 2 with "same" padding
     widened = None
     if not args.no_ablation:
-        widened = {"conv2d_stride2_relu_hardswish_128x8x128x128": strided_conv(
-            fc, d[3], flush, stream, peaks)}
+        widened = {
+            "conv2d_stride2_relu_hardswish_128x8x128x128": widened_conv(
+                fc, d[3], flush, stream, peaks, stride=2, pad=0, dilation=1),
+            "conv2d_dilation2_pad2_relu_hardswish_128x8x128x128": widened_conv(
+                fc, d[3], flush, stream, peaks, stride=1, pad=2, dilation=2),
+        }
 
     # end to end through the public API with host buffers
     e2e = None
@@ -494,16 +498,19 @@ def fusion_ablation(fc, d5, flush, stream, fused_ms_list, reps=10):
             "tail_gbs": tail_bytes / (mt * 1e-3) / 1e9, "conv_variant": conv_variant}
 
 
-def strided_conv(fc, d3, flush, stream, peaks, reps=20):
-    """Stride-2 conv2d + ReLU + HardSwish on x [128,8,128,128] -> y
-    [128,64,63,63], L2 flushed before each call; roofline = max(FLOPs at the
-    FFMA peak, bytes at HBM bandwidth)."""
+def widened_conv(fc, d3, flush, stream, peaks, stride, pad, dilation, reps=20):
+    """conv2d + ReLU + HardSwish on x [128,8,128,128] at the given stride,
+    padding and dilation (stride 2: y [128,64,63,63]; dilation 2, pad 2:
+    y [128,64,128,128]), L2 flushed before each call; roofline = max(FLOPs at
+    the used pipe's peak, bytes at HBM bandwidth)."""
     import torch
     x, w, b = d3["x"], d3["w"], d3["b"]
     N, C, H, W = x.shape
-    Ho, Wo = (H - 3) // 2 + 1, (W - 3) // 2 + 1
+    span = 2 * dilation + 1
+    Ho, Wo = (H + 2 * pad - span) // stride + 1, (W + 2 * pad - span) // stride + 1
     y = torch.empty((N, w.shape[0], Ho, Wo), dtype=torch.float32, device=x.device)
-    call = lambda: fc.fc_conv2d_epi(x, w, b, CHAIN_RH, y=y, stride=2)
+    call = lambda: fc.fc_conv2d_epi(x, w, b, CHAIN_RH, y=y, stride=stride, pad=pad,
+                                    dilation=dilation)
     call()
     variant = fc.last_variant()
     ts = []
@@ -516,7 +523,7 @@ def strided_conv(fc, d3, flush, stream, peaks, reps=20):
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
     if fc.get_last_device_error() != 0:
-        raise RuntimeError("device status word set in the strided conv")
+        raise RuntimeError("device status word set in the widened conv")
     ms = statistics.median(ts)
     flops = 2.0 * N * w.shape[0] * Ho * Wo * C * 9
     nbytes = 4.0 * (x.numel() + w.numel() + b.numel() + y.numel())

@@ -70,12 +70,12 @@ def lib():
             L = ctypes.CDLL(LIB_PATH)
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.fc_conv2d_epi.restype = I
-            L.fc_conv2d_epi.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P, P, S, P]
+            L.fc_conv2d_epi.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P, S, P]
             L.fc_conv2d_epi_noalloc.restype = I
-            L.fc_conv2d_epi_noalloc.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P, P]
+            L.fc_conv2d_epi_noalloc.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P]
             L.fc_conv3d_epi.restype = I
-            L.fc_conv3d_epi.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I, P, P,
-                                        P, S, P]
+            L.fc_conv3d_epi.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I, I, P,
+                                        P, P, S, P]
             L.fc_convT2d_pool_mean.restype = I
             L.fc_convT2d_pool_mean.argtypes = [P, I, I, I, I, P, I, I, I, I, I, P, P,
                                                P, S, P]
@@ -220,8 +220,14 @@ def profile_read(entry: int):
     return ms.value, n.value
 
 
-def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1):
-    """Conv2d(k=3, stride 1 or 2, pad) + bias + elementwise ops -> y [N,CO,Ho,Wo]."""
+def _extent(n_in, k, stride, pad, dilation):
+    return (n_in + 2 * pad - dilation * (k - 1) - 1) // stride + 1
+
+
+def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1,
+                  dilation=1):
+    """Conv2d(k=3, stride 1 or 2, pad, dilation 1 or 2) + bias + elementwise
+    ops -> y [N,CO,Ho,Wo]."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -229,7 +235,7 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
     CO, C2, KH, KW = w.shape
     if C2 != C:
         raise ValueError("weight C_in mismatch")
-    Ho, Wo = (H + 2 * pad - KH) // stride + 1, (W + 2 * pad - KW) // stride + 1
+    Ho, Wo = _extent(H, KH, stride, pad, dilation), _extent(W, KW, stride, pad, dilation)
     if y is None:
         y = torch.empty((N, CO, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -237,7 +243,7 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
         ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv2d_epi(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, int(stride), pad,
-                             ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                             int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
                              _stream_handle(stream))
     _check(st, "fc_conv2d_epi")
     del keep
@@ -258,15 +264,16 @@ def fc_conv2d_epi_noalloc(x, w, y, bias=None, ops=(), pad=0, stream=None):
     if C2 != C:
         raise ValueError("weight C_in mismatch")
     e, keep = make_epilogue(bias, ops)
-    st = lib().fc_conv2d_epi_noalloc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad,
+    st = lib().fc_conv2d_epi_noalloc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad, 1,
                                      ctypes.byref(e), _ptr(y), _stream_handle(stream))
     _check(st, "fc_conv2d_epi_noalloc")
     del keep
     return y
 
 
-def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1):
-    """Conv3d(k=3, stride 1 or 2, pad) + bias + elementwise ops."""
+def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1,
+                  dilation=1):
+    """Conv3d(k=3, stride 1 or 2, pad, dilation 1 or 2) + bias + elementwise ops."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -274,8 +281,8 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
     CO, C2, KD, KH, KW = w.shape
     if C2 != C:
         raise ValueError("weight C_in mismatch")
-    Do, Ho, Wo = ((D + 2 * pad - KD) // stride + 1, (H + 2 * pad - KH) // stride + 1,
-                  (W + 2 * pad - KW) // stride + 1)
+    Do, Ho, Wo = (_extent(D, KD, stride, pad, dilation), _extent(H, KH, stride, pad, dilation),
+                  _extent(W, KW, stride, pad, dilation))
     if y is None:
         y = torch.empty((N, CO, Do, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -283,8 +290,8 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
         ws = _workspace(workspace_bytes(1, (N, C, D, H, W, CO, KD, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv3d_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, int(stride),
-                             pad, ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
-                             _stream_handle(stream))
+                             pad, int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
+                             ws.numel(), _stream_handle(stream))
     _check(st, "fc_conv3d_epi")
     del keep
     return y

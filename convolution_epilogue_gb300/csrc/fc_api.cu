@@ -236,7 +236,8 @@ extern "C" {
 
 fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
                                 const float *w, int C_out, int kH, int kW, int stride,
-                                int pad, const fc_epilogue *epi, float *y, void *stream) {
+                                int pad, int dilation, const fc_epilogue *epi, float *y,
+                                void *stream) {
   // The shapes' workspace must fit the fixed array; anything larger is
   // refused before touching the device.
   const int dims[7] = {N, C_in, H, W, C_out, kH, pad};
@@ -249,20 +250,22 @@ fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
   if (s != FC_OK) return s;
   // The packed weights are rewritten in the array by every call before use,
   // so nothing in it has to start at zero.
-  return fc_conv2d_epi(x, N, C_in, H, W, w, C_out, kH, kW, stride, pad, epi, y, scratch,
-                       kNoAllocScratchBytes, stream);
+  return fc_conv2d_epi(x, N, C_in, H, W, w, C_out, kH, kW, stride, pad, dilation, epi, y,
+                       scratch, kNoAllocScratchBytes, stream);
 }
 
 fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,
-                        int pad, const fc_epilogue *epi, float *y, void *ws,
+                        int pad, int dilation, const fc_epilogue *epi, float *y, void *ws,
                         size_t ws_bytes, void *stream) {
   if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || kH < 1 || kW < 1 ||
-      stride < 1 || pad < 0)
+      stride < 1 || pad < 0 || dilation < 1)
     return FC_ERR_INVALID_ARG;
-  if (stride > 2 || kH != 3 || kW != 3 || pad > 2) return FC_ERR_UNSUPPORTED;
-  if (H + 2 * pad < kH || W + 2 * pad < kW) return FC_ERR_INVALID_ARG;
-  const int Ho = (H + 2 * pad - kH) / stride + 1, Wo = (W + 2 * pad - kW) / stride + 1;
+  if (stride > 2 || dilation > 2 || kH != 3 || kW != 3 || pad > 2 * dilation)
+    return FC_ERR_UNSUPPORTED;
+  const int spanH = dilation * (kH - 1) + 1, spanW = dilation * (kW - 1) + 1;
+  if (H + 2 * pad < spanH || W + 2 * pad < spanW) return FC_ERR_INVALID_ARG;
+  const int Ho = (H + 2 * pad - spanH) / stride + 1, Wo = (W + 2 * pad - spanW) / stride + 1;
   if (Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
   if (!fits_int32((long long)N * C_in * H * W) ||
       !fits_int32((long long)N * C_out * Ho * Wo) ||
@@ -279,6 +282,7 @@ fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
   p.CO = C_out; p.KD = 1; p.KH = kH; p.KW = kW;
   p.pad_d = 0; p.pad = pad;
   p.stride = stride;
+  p.dil = dilation;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 0;
@@ -287,16 +291,18 @@ fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
 
 fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
                         const float *w, int C_out, int kD, int kH, int kW,
-                        int stride, int pad, const fc_epilogue *epi, float *y,
-                        void *ws, size_t ws_bytes, void *stream) {
+                        int stride, int pad, int dilation, const fc_epilogue *epi,
+                        float *y, void *ws, size_t ws_bytes, void *stream) {
   if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 ||
-      kH < 1 || kW < 1 || stride < 1 || pad < 0)
+      kH < 1 || kW < 1 || stride < 1 || pad < 0 || dilation < 1)
     return FC_ERR_INVALID_ARG;
-  if (stride > 2 || kD != 3 || kH != 3 || kW != 3 || pad > 2)
+  if (stride > 2 || dilation > 2 || kD != 3 || kH != 3 || kW != 3 || pad > 2 * dilation)
     return FC_ERR_UNSUPPORTED;
-  if (D + 2 * pad < kD || H + 2 * pad < kH || W + 2 * pad < kW) return FC_ERR_INVALID_ARG;
-  const int Do = (D + 2 * pad - kD) / stride + 1, Ho = (H + 2 * pad - kH) / stride + 1,
-            Wo = (W + 2 * pad - kW) / stride + 1;
+  const int span = dilation * 2 + 1;  // kD = kH = kW = 3
+  if (D + 2 * pad < span || H + 2 * pad < span || W + 2 * pad < span)
+    return FC_ERR_INVALID_ARG;
+  const int Do = (D + 2 * pad - span) / stride + 1, Ho = (H + 2 * pad - span) / stride + 1,
+            Wo = (W + 2 * pad - span) / stride + 1;
   if (Do < 1 || Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
   if (!fits_int32((long long)N * C_in * D * H * W) ||
       !fits_int32((long long)N * C_out * Do * Ho * Wo) ||
@@ -313,6 +319,7 @@ fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
   p.CO = C_out; p.KD = kD; p.KH = kH; p.KW = kW;
   p.pad_d = pad; p.pad = pad;
   p.stride = stride;
+  p.dil = dilation;
   p.Do = Do; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 1;
@@ -348,6 +355,7 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   // the equivalent conv: swapped + flipped weights, padding k - 1 - p
   p.pad_d = 0; p.pad = k - 1 - pad;
   p.stride = 1;
+  p.dil = 1;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 1;
   p.pool = 1;
@@ -382,7 +390,8 @@ fc_status fc_pool_mean_tail(const float *x, int N, int C, int H, int W, int k, i
 size_t fc_workspace_bytes(int entry, const int *d) {
   if (!d) return 0;
   ConvProblem p{};
-  p.stride = 1;  // the workspace does not depend on the stride
+  p.stride = 1;  // the workspace depends on neither the stride nor the dilation
+  p.dil = 1;
   switch (entry) {
     case 0:
       p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];

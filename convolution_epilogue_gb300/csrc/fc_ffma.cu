@@ -54,16 +54,17 @@ __global__ void ffma_pack_weights(const float *__restrict__ w, int C, int CO,
   }
 }
 
-template <int KD, int PR, int PC, bool POOL, int CHAIN, int S>
+template <int KD, int PR, int PC, bool POOL, int CHAIN, int S, int DL>
 __global__ void __launch_bounds__(256)
 ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
                  float *__restrict__ partial, int n_th, int n_tw) {
   constexpr int K = 3;
   constexpr int TAPS = KD * K * K;
   constexpr int TW = 8 * PC, TH = 4 * PR;
-  // staged input extent of an output tile at stride S
-  constexpr int SW = (TW - 1) * S + K, SH = (TH - 1) * S + K;
-  static_assert(!POOL || S == 1, "the pooled path is stride 1");
+  // staged input extent of an output tile at stride S, dilation DL
+  constexpr int SPAN = (K - 1) * DL + 1;
+  constexpr int SW = (TW - 1) * S + SPAN, SH = (TH - 1) * S + SPAN;
+  static_assert(!POOL || (S == 1 && DL == 1), "the pooled path is stride 1, dilation 1");
   extern __shared__ __align__(16) float smem_f[];
   float (*s_w)[TAPS][kCoT] = reinterpret_cast<float (*)[TAPS][kCoT]>(smem_f);
   float (*s_in)[KD][SH][SW] =
@@ -101,7 +102,7 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
       int c = i % SW, r = (i / SW) % SH, kd = (i / (SW * SH)) % KD;
       int ci = i / (SW * SH * KD);
       int gci = ci0 + ci;
-      int id = od * S + kd - p.pad_d, ih = oh0 * S + r - p.pad, iw = ow0 * S + c - p.pad;
+      int id = od * S + kd * DL - p.pad_d, ih = oh0 * S + r - p.pad, iw = ow0 * S + c - p.pad;
       float v = 0.0f;
       if (gci < p.C && id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 &&
           iw < p.W)
@@ -134,16 +135,17 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
           }
 #pragma unroll
           for (int a = 0; a < PR; ++a) {
-            // input columns (gc*PC + c)*S + kw of staged row (gr*PR + a)*S + kh
-            float xin[(PC - 1) * S + K];
+            // input columns (gc*PC + c)*S + kw*DL of staged row
+            // (gr*PR + a)*S + kh*DL
+            float xin[(PC - 1) * S + SPAN];
 #pragma unroll
-            for (int q = 0; q < (PC - 1) * S + K; ++q)
-              xin[q] = s_in[ci][kd][(gr * PR + a) * S + kh][gc * PC * S + q];
+            for (int q = 0; q < (PC - 1) * S + SPAN; ++q)
+              xin[q] = s_in[ci][kd][(gr * PR + a) * S + kh * DL][gc * PC * S + q];
 #pragma unroll
             for (int kw = 0; kw < K; ++kw)
 #pragma unroll
               for (int c = 0; c < PC; ++c) {
-                float xv = xin[c * S + kw];
+                float xv = xin[c * S + kw * DL];
                 acc[a][c][0] = fmaf(xv, wv[kw][0].x, acc[a][c][0]);
                 acc[a][c][1] = fmaf(xv, wv[kw][0].y, acc[a][c][1]);
                 acc[a][c][2] = fmaf(xv, wv[kw][0].z, acc[a][c][2]);
@@ -247,7 +249,7 @@ pool_finish_kernel(const float *__restrict__ partial, int N, int CO, int T, doub
   }
 }
 
-template <int KD, int PR, int PC, bool POOL, int CHAIN, int S = 1>
+template <int KD, int PR, int PC, bool POOL, int CHAIN, int S = 1, int DL = 1>
 cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
                        float *partial, cudaStream_t s) {
   constexpr int TW = 8 * PC, TH = 4 * PR;
@@ -255,9 +257,10 @@ cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
   long blocks = (long)(COp / kCoT) * p.N * p.Do * n_th * n_tw;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+  constexpr int SPAN = 2 * DL + 1;
   constexpr size_t smem = sizeof(float) * (kCiT * KD * 9 * kCoT +
-                                           kCiT * KD * ((TH - 1) * S + 3) * ((TW - 1) * S + 3));
-  auto kern = ffma_conv_kernel<KD, PR, PC, POOL, CHAIN, S>;
+                                           kCiT * KD * ((TH - 1) * S + SPAN) * ((TW - 1) * S + SPAN));
+  auto kern = ffma_conv_kernel<KD, PR, PC, POOL, CHAIN, S, DL>;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -267,19 +270,30 @@ cudaError_t launch_one(const ConvProblem &p, const float *wp, int Cp, int COp,
   return cudaGetLastError();
 }
 
-template <int KD, int S>
+template <int KD, int S, int DL>
 cudaError_t launch_eltwise(const ConvProblem &p, const float *wp, int Cp, int COp,
                            cudaStream_t s) {
   switch (p.chain) {
-    case CHAIN_NONE: return launch_one<KD, 1, 4, false, CHAIN_NONE, S>(p, wp, Cp, COp, nullptr, s);
+    case CHAIN_NONE:
+      return launch_one<KD, 1, 4, false, CHAIN_NONE, S, DL>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_RELU_HARDSWISH:
-      return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH, S>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_RELU_HARDSWISH, S, DL>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU, S>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP_GELU, S, DL>(p, wp, Cp, COp, nullptr, s);
     case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP1_GELU, S>(p, wp, Cp, COp, nullptr, s);
-    default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC, S>(p, wp, Cp, COp, nullptr, s);
+      return launch_one<KD, 1, 4, false, CHAIN_LEAKY_ADD_CLAMP1_GELU, S, DL>(p, wp, Cp, COp, nullptr, s);
+    default: return launch_one<KD, 1, 4, false, CHAIN_GENERIC, S, DL>(p, wp, Cp, COp, nullptr, s);
   }
+}
+
+template <int KD>
+cudaError_t launch_eltwise_kd(const ConvProblem &p, const float *wp, int Cp, int COp,
+                              cudaStream_t s) {
+  if (p.stride == 2)
+    return p.dil == 2 ? launch_eltwise<KD, 2, 2>(p, wp, Cp, COp, s)
+                      : launch_eltwise<KD, 2, 1>(p, wp, Cp, COp, s);
+  return p.dil == 2 ? launch_eltwise<KD, 1, 2>(p, wp, Cp, COp, s)
+                    : launch_eltwise<KD, 1, 1>(p, wp, Cp, COp, s);
 }
 
 }  // namespace
@@ -318,12 +332,8 @@ cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
     *launches += 2;
     return e;
   }
-  if (p.stride == 2)
-    e = (p.KD == 1) ? launch_eltwise<1, 2>(p, wp, Cp, COp, s)
-                    : launch_eltwise<3, 2>(p, wp, Cp, COp, s);
-  else
-    e = (p.KD == 1) ? launch_eltwise<1, 1>(p, wp, Cp, COp, s)
-                    : launch_eltwise<3, 1>(p, wp, Cp, COp, s);
+  e = (p.KD == 1) ? launch_eltwise_kd<1>(p, wp, Cp, COp, s)
+                  : launch_eltwise_kd<3>(p, wp, Cp, COp, s);
   *launches += 1;
   return e;
 }

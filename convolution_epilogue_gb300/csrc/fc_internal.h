@@ -39,6 +39,7 @@ struct ConvProblem {
   int CO, KD, KH, KW;
   int pad_d, pad;  // zero padding on D and on H/W
   int stride;      // conv stride on every spatial axis (1 or 2)
+  int dil;         // conv dilation on every spatial axis (1 or 2)
   int Do, Ho, Wo;
   int wlayout;     // 0: conv [CO][C][KD][KH][KW]; 1: convT [C][CO][KH][KW]
   int pool;        // 1: 2x2 maxpool -> hardtanh -> mean -> tanh

@@ -119,9 +119,10 @@ struct TcPlan {
   // the input pixels loaded per row; DSL the staged pixels per depth slice.
   // Stride 2 (S2) stages each input slice deinterleaved into four
   // sub-planes (even/odd rows x even/odd columns) of SR x RS pixels (SUB
-  // each), so that tap (kh, kw) reads sub-plane (kh & 1, kw & 1) at a shift
-  // of (kh >> 1, kw >> 1) -- again one shifted descriptor start per tap.
-  int S2, LW, SR, SUB, DSL;
+  // each), so that tap (kh, kw) at input offset (a, b) = (kh, kw) * DIL
+  // reads sub-plane (a & 1, b & 1) at a shift of (a >> 1, b >> 1) -- again
+  // one shifted descriptor start per tap.  DIL is the dilation.
+  int S2, DIL, LW, SR, SUB, DSL;
   uint8_t perm[28];  // K order of the taps (paired taps: increasing shifts)
   int NPIX;
   int plane_bytes;
@@ -158,22 +159,20 @@ static_assert(offsetof(SmemCtl, bias) % 16 == 0 && offsetof(SmemCtl, addend) % 1
 static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 
 // Staged-pixel shift of tap t = (kd, kh, kw) from an M tile's first
-// pixel: stride 1 (kd*RIN + kh)*RS + kw; stride 2 sub-plane
-// (kh & 1, kw & 1) of depth slice kd, then (kh >> 1) rows and (kw >> 1)
-// columns.
+// pixel, with input offsets a = kh * DIL, b = kw * DIL: stride 1
+// kd*DSL + a*RS + b; stride 2 sub-plane (a & 1, b & 1) of depth slice kd,
+// then (a >> 1) rows and (b >> 1) columns.  (Depth slice kd is staged input
+// depth od*stride + kd*DIL - pad.)
 __host__ __device__ __forceinline__ int tap_shift(int t, const TcPlan &q) {
-  const int kd = t / 9, kh = (t / 3) % 3, kw = t % 3;
-  if (!q.S2) return kd * q.DSL + kh * q.RS + kw;
-  return kd * q.DSL + (2 * (kh & 1) + (kw & 1)) * q.SUB + (kh >> 1) * q.RS + (kw >> 1);
+  const int kd = t / 9, a = ((t / 3) % 3) * q.DIL, b = (t % 3) * q.DIL;
+  if (!q.S2) return kd * q.DSL + a * q.RS + b;
+  return kd * q.DSL + (2 * (a & 1) + (b & 1)) * q.SUB + (a >> 1) * q.RS + (b >> 1);
 }
 
-// Plan with `U` M tiles per unit (pooling needs 2).
-TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
-  TcPlan q{};
-  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
-  if (p.stride > 2 || (p.stride == 2 && p.pool)) return q;
-  if (p.pool && U != 2) return q;
-  if (p.pool && p.KD != 1) return q;
+// Channel chunks and K steps of a plan.  They do not depend on the
+// geometry, so neither does the weight image (nor the workspace): stride,
+// dilation and the spatial extents change only the staging.
+void plan_chunks(const ConvProblem &p, int prec, TcPlan &q) {
   q.prec = prec;
   q.E = prec ? 8 : 4;
   const int Cp8 = cdiv(p.C, 8) * 8;
@@ -184,8 +183,23 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.TAPS = p.KD * 9;
   q.pairtaps = (q.P == 1);
   q.KS = q.pairtaps ? cdiv(q.TAPS, 2) : q.TAPS;
+  q.COB = cdiv(p.CO, 64);
+  q.b_chunk_bytes = q.KS * kBStep;
+}
+
+// Plan with `U` M tiles per unit (pooling needs 2).
+TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
+  TcPlan q{};
+  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
+  if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
+  if (p.pool && U != 2) return q;
+  if (p.pool && p.KD != 1) return q;
+  plan_chunks(p, prec, q);
   q.S2 = p.stride == 2;
-  const int halo = q.S2 ? 1 : 2;  // staged columns past the tile's outputs
+  q.DIL = p.dil;
+  // staged columns past the tile's outputs: the last tap's column offset
+  // 2 DIL (stride 2: DIL in the half-width sub-planes)
+  const int halo = q.S2 ? q.DIL : 2 * q.DIL;
   const bool rowpack = (p.Wo + halo <= 128);
   if (rowpack) {
     q.RS = p.Wo + halo;
@@ -199,14 +213,14 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
     q.R = 1;
   }
   q.U = U;
-  if (!q.S2) {
-    q.RIN = q.U * q.R + 2;
+  if (!q.S2) {  // output rows u read input rows u + kh DIL: UR + 2 DIL rows
+    q.RIN = q.U * q.R + 2 * q.DIL;
     q.LW = q.RS;
     q.DSL = q.RIN * q.RS;
-  } else {  // output rows u read input rows 2u + kh: 2UR + 1 rows, 2 RS columns
-    q.RIN = 2 * q.U * q.R + 1;
-    q.LW = 2 * q.RS;
-    q.SR = q.U * q.R + 1;
+  } else {  // output rows u read input rows 2u + kh DIL: 2UR - 1 + 2 DIL rows
+    q.RIN = 2 * q.U * q.R - 1 + 2 * q.DIL;
+    q.LW = 2 * q.RS;  // of 2 RS columns
+    q.SR = q.U * q.R + q.DIL;  // even input rows (odd rows: one fewer)
     q.SUB = q.SR * q.RS;
     q.DSL = 4 * q.SUB;
   }
@@ -234,9 +248,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.NPIX = cdiv(npix, 8) * 8;
   q.plane_bytes = q.NPIX * 16;
   q.a_stage_bytes = 2 * q.P * q.plane_bytes;
-  q.COB = cdiv(p.CO, 64);
   if (q.COB * 64 > kMaxCoTc) return q;
-  q.b_chunk_bytes = q.KS * kBStep;
   q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.U * q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
   if (q.units >= (1L << 31)) return q;  // unit indices are 32-bit
@@ -489,7 +501,7 @@ __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, 
   const int sr = job - plane * nrows;
   const int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
   const int r = sr - kdp * q.RIN;
-  const int id = ss.id0 + kdp, ih = ss.ih0 + r;
+  const int id = ss.id0 + kdp * q.DIL, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
   jb.rowbase = ss.xn + ((long)id * p.H + ih) * p.W + ss.iw0;
   jb.cbase = ss.ci0 + plane * E;
@@ -1210,13 +1222,14 @@ cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaSt
 }
 
 size_t tc_weight_bytes(const ConvProblem &p) {
+  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return 0;
   size_t m = 0;
   for (int prec = 0; prec < 2; ++prec) {
-    TcPlan q = make_plan(p, prec);
-    if (q.ok) {
-      size_t b = (size_t)q.COB * q.NCH * q.b_chunk_bytes;
-      if (b > m) m = b;
-    }
+    TcPlan q{};
+    plan_chunks(p, prec, q);
+    if (q.COB * 64 > kMaxCoTc) continue;
+    const size_t b = (size_t)q.COB * q.NCH * q.b_chunk_bytes;
+    if (b > m) m = b;
   }
   return m;
 }

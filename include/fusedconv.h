@@ -113,17 +113,21 @@ typedef enum {
 /* Conv2d + bias + elementwise epilogue chain (any sequence of RELU,
  * HARDSWISH, LEAKY_RELU, ADD_CHANNEL, CLAMP, GELU_ERF, HARDTANH, TANH).
  * x [N][C_in][H][W]; w [C_out][C_in][kH][kW]; y [N][C_out][Ho][Wo] with
- * Ho = (H + 2 pad - kH) / stride + 1, Wo = (W + 2 pad - kW) / stride + 1
- * (floor), output (oh, ow) reading input rows oh*stride + kh - pad.
- * Supported: stride 1 or 2, kH = kW = 3, 0 <= pad <= 2, 1 <= C_in,
- * 1 <= C_out, H + 2 pad >= kH, W + 2 pad >= kW, and every tensor below 2^31
- * elements; every variant takes stride 2 (the tensor-core variants stage
- * the input as even/odd row x column sub-planes).  N = 0 is a valid empty
- * call (nothing is launched). */
+ * Ho = (H + 2 pad - dilation (kH - 1) - 1) / stride + 1 and Wo likewise
+ * (floor), output (oh, ow) reading input row oh*stride + kh*dilation - pad
+ * and column ow*stride + kw*dilation - pad (the dilated extent is the one
+ * trace "Kimi-K2.6__l2_p10" states for pooling windows; its l2_p57 trace
+ * names the layer's stride / padding / dilation defaults 1 / 0 / 1).
+ * Supported: stride 1 or 2, dilation 1 or 2, kH = kW = 3,
+ * 0 <= pad <= 2 dilation, 1 <= C_in, 1 <= C_out, H + 2 pad and W + 2 pad
+ * at least the dilated window 2 dilation + 1, and every tensor below 2^31
+ * elements; every variant takes every stride / dilation pair (the
+ * tensor-core variants stage stride 2 as even/odd row x column
+ * sub-planes).  N = 0 is a valid empty call (nothing is launched). */
 FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,
-                        int pad, const fc_epilogue *epi, float *y, void *ws,
-                        size_t ws_bytes, void *stream);
+                        int pad, int dilation, const fc_epilogue *epi, float *y,
+                        void *ws, size_t ws_bytes, void *stream);
 
 /* fc_conv2d_epi for callers that cannot allocate device memory (code run
  * from a host callback or an allocator hook, allocation-free real-time or
@@ -143,18 +147,20 @@ FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
  * the GPU -- on different streams or host threads -- race on it. */
 FC_API fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
                                        const float *w, int C_out, int kH, int kW,
-                                       int stride, int pad, const fc_epilogue *epi,
-                                       float *y, void *stream);
+                                       int stride, int pad, int dilation,
+                                       const fc_epilogue *epi, float *y, void *stream);
 
 /* Conv3d + bias + elementwise epilogue chain; same ops as fc_conv2d_epi.
  * x [N][C_in][D][H][W]; w [C_out][C_in][kD][kH][kW];
- * y [N][C_out][Do][Ho][Wo], each extent (in + 2 pad - k) / stride + 1.
- * Supported: stride 1 or 2 (on every variant, as for fc_conv2d_epi),
- * kD = kH = kW = 3, 0 <= pad <= 2. */
+ * y [N][C_out][Do][Ho][Wo], each extent
+ * (in + 2 pad - dilation (k - 1) - 1) / stride + 1, output (od, oh, ow)
+ * reading input od*stride + kd*dilation - pad on each axis.
+ * Supported: stride 1 or 2, dilation 1 or 2 (on every variant, as for
+ * fc_conv2d_epi), kD = kH = kW = 3, 0 <= pad <= 2 dilation. */
 FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
                         const float *w, int C_out, int kD, int kH, int kW,
-                        int stride, int pad, const fc_epilogue *epi, float *y,
-                        void *ws, size_t ws_bytes, void *stream);
+                        int stride, int pad, int dilation, const fc_epilogue *epi,
+                        float *y, void *ws, size_t ws_bytes, void *stream);
 
 /* ConvTranspose2d + bias -> MaxPool2d(2,2) -> Hardtanh[a,b] -> mean(H,W)
  * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];

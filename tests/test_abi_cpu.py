@@ -60,10 +60,10 @@ def _epi(ops=()):
 
 
 def _conv2d(L, N=1, C=8, H=8, W=8, CO=64, k=3, stride=1, pad=0, x=16, w=16,
-            y=16, ops=(), ws=256, ws_bytes=1 << 20):
+            y=16, ops=(), ws=256, ws_bytes=1 << 20, dilation=1):
     e, _ = _epi(ops)
     return L.fc_conv2d_epi(ctypes.c_void_p(x), N, C, H, W, ctypes.c_void_p(w), CO,
-                           k, k, stride, pad, ctypes.byref(e), ctypes.c_void_p(y),
+                           k, k, stride, pad, dilation, ctypes.byref(e), ctypes.c_void_p(y),
                            ctypes.c_void_p(ws), ws_bytes, None)
 
 
@@ -75,7 +75,12 @@ def test_host_validation_rejects_before_launch(L):
     assert _conv2d(L, stride=3) == UNSUP  # stride 1 and 2 are supported
     assert _conv2d(L, k=5) == UNSUP
     assert _conv2d(L, pad=3) == UNSUP
+    assert _conv2d(L, dilation=0) == INVALID
+    assert _conv2d(L, dilation=3) == UNSUP  # dilation 1 and 2 are supported
+    assert _conv2d(L, dilation=2, pad=5) == UNSUP  # pad at most 2 x dilation
     assert _conv2d(L, H=2) == INVALID  # Ho = 0
+    assert _conv2d(L, H=4, dilation=2) == INVALID  # window of 5 rows over 4
+    assert _conv2d(L, H=4, W=4, dilation=2, pad=1, N=0) == 0  # 6 padded rows: valid
     assert _conv2d(L, x=0) == INVALID  # NULL x
     assert _conv2d(L, x=18) == ALIGN
     assert _conv2d(L, ops=(("maxpool2x2",),)) == UNSUP

@@ -375,12 +375,13 @@ def test_conv2d_stride2(variant, shape, pad, ops):
     _check(got, oracle.conv_epi(x, w, b, ops, stride=2, pad=pad), f"{variant} stride2 {shape} pad {pad}")
 
 
-def _run_conv_strided(variant, x, w, b, ops, pad, stride):
+def _run_conv_strided(variant, x, w, b, ops, pad, stride, dilation=1):
     m = fc()
     m.set_variant(variant)
     try:
         f = m.fc_conv2d_epi if x.ndim == 4 else m.fc_conv3d_epi
-        y = f(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=stride)
+        y = f(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=stride,
+              dilation=dilation)
         assert m.last_variant() == variant
         assert m.get_last_device_error() == 0
         return y.cpu().numpy()
@@ -398,3 +399,68 @@ def test_conv3d_stride2(variant):
     ops = (("leaky_relu", 0.2), ("add_channel", s), ("clamp", -1.0, 1.0), ("gelu_erf",))
     got = _run_conv_strided(variant, x, w, b, ops, 1, 2)
     _check(got, oracle.conv_epi(x, w, b, ops, stride=2, pad=1), f"{variant} conv3d stride 2")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape,stride,pad,ops", [
+    ((2, 8, 33, 37), 1, 0, (("relu",), ("hardswish",))),
+    ((1, 5, 20, 71), 1, 3, (("leaky_relu", 0.2), ("clamp", -1.0, 1.0), ("gelu_erf",))),
+    ((1, 8, 11, 300), 1, 4, (("relu",),)),        # 128-column strips plus a tail
+    ((2, 64, 20, 150), 1, 2, (("hardswish",),)),  # several channel chunks
+    ((2, 8, 33, 37), 2, 2, (("relu",), ("hardswish",))),
+    ((1, 8, 15, 300), 2, 1, ()),
+    ((2, 16, 9, 12), 2, 4, (("tanh",),)),
+])
+def test_conv2d_dilation2(variant, shape, stride, pad, ops):
+    """Dilation 2 (strides 1 and 2, pads 0-4) vs the oracle for every
+    variant: row-packed tiles, column strips, ragged tails."""
+    st = synth.seeded(720 + pad + shape[1] + 10 * stride)
+    N, C, H, W = shape
+    x = st.normal(shape)
+    w = st.uniform((70, C, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((70,), 0.1)
+    got = _run_conv_strided(variant, x, w, b, ops, pad, stride, dilation=2)
+    ref = oracle.conv_epi(x, w, b, ops, stride=stride, pad=pad, dilation=2)
+    _check(got, ref, f"{variant} dilation 2 stride {stride} {shape} pad {pad}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape,stride,pad", [
+    ((2, 8, 9, 12, 35), 1, 2),
+    ((2, 8, 11, 12, 20), 2, 2),
+])
+def test_conv3d_dilation2(variant, shape, stride, pad):
+    st = synth.seeded(730 + stride)
+    x = st.normal(shape)
+    w = st.uniform((64, shape[1], 3, 3, 3), 1.0 / np.sqrt(27.0 * shape[1]))
+    b = st.uniform((64,), 0.1)
+    s = st.normal((64,))
+    ops = (("leaky_relu", 0.2), ("add_channel", s), ("clamp", -1.0, 1.0), ("gelu_erf",))
+    got = _run_conv_strided(variant, x, w, b, ops, pad, stride, dilation=2)
+    ref = oracle.conv_epi(x, w, b, ops, stride=stride, pad=pad, dilation=2)
+    _check(got, ref, f"{variant} conv3d dilation 2 stride {stride}")
+
+
+@pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
+@pytest.mark.parametrize("stride,pad,dilation", [(2, 0, 1), (1, 2, 2)])
+def test_widened_conv2d_full_size_sampled(variant, stride, pad, dilation):
+    """The widened layer parameters on the full conv2d workload input
+    [128,8,128,128], in the launch configuration the benchmark times, on
+    sampled outputs."""
+    inp = _full_inputs(3)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_conv2d_epi(_dev(inp["x"]), _dev(inp["w"]), _dev(inp["b"]), CHAIN_RH,
+                            stride=stride, pad=pad, dilation=dilation)
+        assert m.get_last_device_error() == 0
+        shape = tuple(y.shape)
+        e = oracle.conv_out_extent(128, 3, stride, pad, dilation)
+        assert shape == (128, 64, e, e)
+        idx = _sample_idx(shape, 4000, 30 + stride)
+        got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    ref = oracle.conv_epi_points(inp["x"], inp["w"], inp["b"], CHAIN_RH, idx, stride=stride,
+                                 pad=pad, dilation=dilation)
+    _check(got, ref, f"widened s{stride} p{pad} d{dilation} sampled [{variant}]")

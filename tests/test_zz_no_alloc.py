@@ -79,7 +79,7 @@ def test_noalloc_refuses_shapes_beyond_its_array():
     assert fc.workspace_bytes(0, (1, 256, 8, 8, 256, 3, 0)) > (1 << 20)
     e, _keep = fc.make_epilogue(None, ())
     st = L.fc_conv2d_epi_noalloc(ctypes.c_void_p(x.data_ptr()), 1, 256, 8, 8,
-                                 ctypes.c_void_p(w.data_ptr()), 256, 3, 3, 1, 0,
+                                 ctypes.c_void_p(w.data_ptr()), 256, 3, 3, 1, 0, 1,
                                  ctypes.byref(e), ctypes.c_void_p(y.data_ptr()), None)
     assert st == 4  # FC_ERR_WORKSPACE
     assert L.fc_status_string(st).decode().startswith("FC_ERR_WORKSPACE")
