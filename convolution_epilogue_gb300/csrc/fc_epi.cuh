@@ -96,6 +96,58 @@ __device__ __forceinline__ float apply_chain(const EpiDev &e, int co, float v,
   }
 }
 
+// The general chain on N consecutive output channels co0 .. co0 + N - 1 of
+// one pixel, v already carrying the bias.  The op loop is outside and the
+// values inside, so each op's kind and parameters are read and dispatched
+// once per N outputs instead of once per output.  Every value sees the same
+// ops in the same order as in apply_chain<CHAIN_GENERIC> (bit-identical
+// results).  Only the first `nco` channels exist (ADD_CHANNEL reads only
+// those; the caller stores only those).
+template <int N>
+__device__ __forceinline__ void apply_chain_generic_n(const EpiDev &e, int co0, int nco,
+                                                      float (&v)[N]) {
+#pragma unroll 1
+  for (int i = 0; i < e.n_ops; ++i) {
+    const float a = e.a[i], b = e.b[i];
+    switch (e.kind[i]) {
+      case FC_EPI_RELU:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = fmaxf(v[j], 0.0f);
+        break;
+      case FC_EPI_HARDSWISH:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = op_hardswish(v[j]);
+        break;
+      case FC_EPI_LEAKY_RELU:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = v[j] > 0.0f ? v[j] : a * v[j];
+        break;
+      case FC_EPI_ADD_CHANNEL: {
+        const float *ch = e.chan[i] + co0;
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+          if (j < nco) v[j] = v[j] + __ldg(ch + j);
+        break;
+      }
+      case FC_EPI_CLAMP:
+      case FC_EPI_HARDTANH:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = fminf(fmaxf(v[j], a), b);
+        break;
+      case FC_EPI_GELU_ERF:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = op_gelu_erf(v[j]);
+        break;
+      case FC_EPI_TANH:
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] = tanhf(v[j]);
+        break;
+      default:
+        break;
+    }
+  }
+}
+
 // Two adjacent channels of one pixel through the fused chains on the paired
 // fp32 pipe: y = chain(hi + scale * lo + bias).  Bit-identical to
 // apply_chain on each lane.  Only the two fixed chains.

@@ -1042,7 +1042,19 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             }
             float *yc = yp + (long)cc * cstride;
             if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
-              if constexpr (CHAIN == CHAIN_RELU_HARDSWISH || CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+              if constexpr (CHAIN == CHAIN_GENERIC) {  // op loop outside, 16 values inside
+                float v[16];
+  #pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, 16, v);
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  *yc = v[j];
+                  yc += cstride;
+                }
+              } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
+                                   CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
   #pragma unroll
                 for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
                   float o0, o1;
@@ -1062,13 +1074,26 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                 }
               }
             } else if (valid) {
+              if constexpr (CHAIN == CHAIN_GENERIC) {
+                float v[16];
   #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                if (cc + j < nco) {
-                  float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                  *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                for (int j = 0; j < 16; ++j)
+                  v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, v);
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (cc + j < nco) *yc = v[j];
+                  yc += cstride;
                 }
-                yc += cstride;
+              } else {
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (cc + j < nco) {
+                    float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                    *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                  }
+                  yc += cstride;
+                }
               }
             }
             RT_MARK(3);  // epilogue math + stores

@@ -464,3 +464,21 @@ def test_widened_conv2d_full_size_sampled(variant, stride, pad, dilation):
     ref = oracle.conv_epi_points(inp["x"], inp["w"], inp["b"], CHAIN_RH, idx, stride=stride,
                                  pad=pad, dilation=dilation)
     _check(got, ref, f"widened s{stride} p{pad} d{dilation} sampled [{variant}]")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", [(2, 8, 21, 40), (1, 8, 6, 7, 30)])
+def test_generic_chain_every_op(variant, shape):
+    """An op sequence outside the fixed chains, using every elementwise op
+    (per-channel add included), with 70 output channels so the last channel
+    group is partial."""
+    st = synth.seeded(740 + len(shape))
+    x = st.normal(shape)
+    C, taps = shape[1], 9 if len(shape) == 4 else 27
+    w = st.uniform((70, C) + (3,) * (len(shape) - 2), 1.0 / np.sqrt(taps * C))
+    b = st.uniform((70,), 0.1)
+    s = st.normal((70,))
+    ops = (("relu",), ("add_channel", s), ("leaky_relu", 0.3), ("hardtanh", -0.8, 0.9),
+           ("gelu_erf",), ("tanh",), ("hardswish",), ("clamp", -0.2, 0.6))
+    got = _run_conv_strided(variant, x, w, b, ops, 1, 1)
+    _check(got, oracle.conv_epi(x, w, b, ops, pad=1), f"{variant} generic chain {shape}")
