@@ -777,6 +777,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // the first ones.
     int rot = 0;
     uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
+    // ring positions kept as counters (no integer division in the loop):
+    // stage ps of phase pph; weight slot psb of phase psbph
+    int ps = 0, psb = 0;
+    uint32_t pph = 0, psbph = 0;
     RT_DECL
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q);
@@ -787,11 +791,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       ss.iw0 = up.ct * q.WT * st - p.pad;
       ss.xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
-        const int s = (int)(g % q.S);
+        const int s = ps;
         RT_MARK(0);
         if (!q.b_resident && pw == 0) {
-          const int sb = (int)(g % q.SB);
-          if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status, 0x11000000u | g)) {
+          const int sb = psb;
+          if (!wait_bar_warp(bars, B_EMPTY + sb, psbph ^ 1, abort_flag, p.status, 0x11000000u | g)) {
             ok = false;
             break;
           }
@@ -816,7 +820,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           if (waited) return true;
           waited = true;
           RT_MARK(2);
-          const bool w = wait_bar_warp(bars, A_EMPTY + s, ((g / q.S) & 1) ^ 1, abort_flag,
+          const bool w = wait_bar_warp(bars, A_EMPTY + s, pph ^ 1, abort_flag,
                                        p.status, 0x10000000u | g);
           RT_MARK(1);
           return w;
@@ -857,6 +861,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
         rot += njobs % kProdWarps;
         if (rot >= kProdWarps) rot -= kProdWarps;
+        if (++ps == q.S) { ps = 0; pph ^= 1; }
+        if (++psb == q.SB) { psb = 0; psbph ^= 1; }
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&a_full[s]);
@@ -884,13 +890,18 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const uint32_t lo_delta = (uint32_t)((q.P * q.plane_bytes) >> 4);  // hi -> lo planes
     const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile (pool)
     uint32_t g = 0, gb = 0, it = 0;
+    // ring positions as counters (no integer division in the issue loop):
+    // accumulator macc of phase mpar, stage ms of phase mph, weight slot msb
+    int macc = 0, ms = 0, msb = 0;
+    uint32_t mpar = 0, mph = 0, msbph = 0;
     bool ok = true;
     RT_DECL
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
-      const int acc = (int)(it % q.NACC);
-      const uint32_t acc_par = ((it / q.NACC) & 1) ^ 1;
+      const int acc = macc;
+      const uint32_t acc_par = mpar ^ 1;
+      if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
       RT_MARK(0);
       if constexpr (POOL) {  // the pooled epilogue takes both tiles at once
         if (!wait_bar_warp(bars, ACC_EMPTY + acc, acc_par, abort_flag, p.status, 0x21000000u | it)) break;
@@ -898,9 +909,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
       RT_MARK(1);  // waiting for a free accumulator
       for (int c = 0; c < q.NCH; ++c, ++g) {
-        const int s = (int)(g % q.S);
+        const int s = ms;
+        const uint32_t sph = mph;
+        if (++ms == q.S) { ms = 0; mph ^= 1; }
         RT_MARK(0);
-        if (!wait_bar_warp(bars, A_FULL + s, (g / q.S) & 1, abort_flag, p.status, 0x22000000u | g)) {
+        if (!wait_bar_warp(bars, A_FULL + s, sph, abort_flag, p.status, 0x22000000u | g)) {
           ok = false;
           break;
         }
@@ -909,8 +922,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         if (q.b_resident) {
           bbase = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
         } else {
-          sb = (int)(gb % q.SB);
-          if (!wait_bar_warp(bars, B_FULL + sb, (gb / q.SB) & 1, abort_flag, p.status, 0x23000000u | gb)) {
+          sb = msb;
+          if (!wait_bar_warp(bars, B_FULL + sb, msbph, abort_flag, p.status, 0x23000000u | gb)) {
             ok = false;
             break;
           }
@@ -961,7 +974,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           if (!q.b_resident) ptx::tc_commit(&b_empty[sb]);
         }
         __syncwarp();
-        if (!q.b_resident) ++gb;
+        if (!q.b_resident) {
+          ++gb;
+          if (++msb == q.SB) { msb = 0; msbph ^= 1; }
+        }
         RT_MARK(3);  // issuing MMAs
       }
       if (!ok) break;
@@ -985,11 +1001,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     const int m_row = m / q.RS, m_col = m - m_row * q.RS;  // staged row / column of m
     const float scale = PREC ? (1.0f / 2048.0f) : 1.0f;
     uint32_t it = 0;
+    int eacc = 0;  // accumulator eacc of phase epar, as counters
+    uint32_t epar = 0;
     RT_DECL
     for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const UnitPos up = decode_unit(u, q);
-      const int acc = (int)(it % q.NACC);
-      const uint32_t acc_par = (it / q.NACC) & 1;
+      const int acc = eacc;
+      const uint32_t acc_par = epar;
+      if (++eacc == q.NACC) { eacc = 0; epar ^= 1; }
       RT_MARK(0);
       if constexpr (POOL) {
         bool okw = wait_bar_warp(bars, ACC_FULL + acc, acc_par, abort_flag, p.status, 0x30000000u | it);
