@@ -345,11 +345,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bars, int idx, uint32_t parit
   }
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so a
-// warp never splits around .sync.aligned instructions or named barriers.
+// Warp-uniform bounded wait.  Every lane tests the barrier once (a phase
+// that has already completed costs one instruction and a vote); otherwise
+// lane 0 polls and the verdict is broadcast, so a warp never splits around
+// .sync.aligned instructions or named barriers.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t parity,
                                               volatile int *abort, unsigned int *status,
                                               uint32_t tag, uint64_t limit_ns = kWaitNs) {
+  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bars + idx, parity))) return true;
   int ok = 1;
   if ((threadIdx.x & 31) == 0)
     ok = wait_bar(bars, idx, parity, abort, status, tag, limit_ns) ? 1 : 0;
@@ -894,6 +897,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // accumulator macc of phase mpar, stage ms of phase mph, weight slot msb
     int macc = 0, ms = 0, msb = 0;
     uint32_t mpar = 0, mph = 0, msbph = 0;
+    // The tensor pipe queues only a few MMAs, so any stall of this warp
+    // between bursts idles it.  Right after issuing a chunk the warp tests
+    // (without blocking) the barriers the next chunk and the next unit will
+    // wait on, while the queued MMAs run; a barrier seen complete then needs
+    // no wait.
+    bool pre_full = false, pre_acc = false;
     bool ok = true;
     RT_DECL
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
@@ -903,17 +912,20 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       const uint32_t acc_par = mpar ^ 1;
       if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
       RT_MARK(0);
-      if constexpr (POOL) {  // the pooled epilogue takes both tiles at once
-        if (!wait_bar_warp(bars, ACC_EMPTY + acc, acc_par, abort_flag, p.status, 0x21000000u | it)) break;
-        ptx::tc_fence_after();
-      }
+      // One wait for the whole accumulator: the epilogue frees a unit's
+      // tiles in order (each warp arrives for tile t before tile t + 1), so
+      // the last tile's barrier implies the others.
+      if (!pre_acc && !wait_bar_warp(bars, ACC_EMPTY + (POOL ? acc : acc * U + U - 1), acc_par,
+                                     abort_flag, p.status, 0x21000000u | it))
+        break;
+      ptx::tc_fence_after();
       RT_MARK(1);  // waiting for a free accumulator
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = ms;
         const uint32_t sph = mph;
         if (++ms == q.S) { ms = 0; mph ^= 1; }
         RT_MARK(0);
-        if (!wait_bar_warp(bars, A_FULL + s, sph, abort_flag, p.status, 0x22000000u | g)) {
+        if (!pre_full && !wait_bar_warp(bars, A_FULL + s, sph, abort_flag, p.status, 0x22000000u | g)) {
           ok = false;
           break;
         }
@@ -941,17 +953,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           // both tiles per K step (measured faster for the pooled chunks)
           issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
         } else {
-          // Tile by tile, each with its own accumulator barriers: a tile's
-          // MMAs start once the epilogue has freed that tile, and the
-          // epilogue starts on a tile once its last chunk's MMAs are done.
-          bool okt = true;
+          // Tile by tile, each committed to its own accumulator-full barrier:
+          // the epilogue starts on a tile once its last chunk's MMAs are done.
 #pragma unroll 1
-          for (int t = 0; t < U && okt; ++t) {
+          for (int t = 0; t < U; ++t) {
             const int ab = acc * U + t;
-            if (c == 0) {
-              okt = wait_bar_warp(bars, ACC_EMPTY + ab, acc_par, abort_flag, p.status, 0x21000000u | it);
-              ptx::tc_fence_after();
-            }
             const uint32_t at = a_lo + (uint32_t)t * tile_delta, dt = dacc + (uint32_t)(t * 128);
             switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
               case 5: issue_chunk<PREC, 1, 5>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
@@ -964,11 +970,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               __syncwarp();
             }
           }
-          if (!okt) {
-            ok = false;
-            break;
-          }
         }
+        // look ahead while the MMAs just issued run
+        pre_full = __all_sync(0xffffffffu, ptx::mbar_test_wait(&a_full[ms], mph));
+        if (c == q.NCH - 1)
+          pre_acc = __all_sync(0xffffffffu, ptx::mbar_test_wait(
+                                                &acc_empty[POOL ? macc : macc * U + U - 1], mpar ^ 1));
         if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
           if (!q.b_resident) ptx::tc_commit(&b_empty[sb]);
