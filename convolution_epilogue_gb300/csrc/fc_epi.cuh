@@ -19,35 +19,33 @@ __device__ __forceinline__ float op_hardswish(float v) {
   return v * __saturatef(fmaf(v, 1.0f / 6.0f, 0.5f));
 }
 
-// GELU for |v| <= 1 from the Maclaurin series of erf,
-//   erf(z) = 2/sqrt(pi) sum_n (-1)^n z^(2n+1) / (n! (2n+1)).
-// With z = v / sqrt 2 and s = v^2 this gives
-//   GELU(v) = v/2 + v/2 erf(v / sqrt 2) = v/2 + s R(s),
-//   R(s) = sum_n d_n s^n,  d_n = (-1)^n / (sqrt(2 pi) 2^n n! (2n+1)),
-// evaluated by Horner in s and truncated after n = 7: for |v| <= 1 the first
-// omitted term is below 2.3e-10, far under fp32 rounding of the result.
-constexpr double kInvSqrt2Pi = 0.39894228040143267794;  // 1 / sqrt(2 pi)
-
-__host__ __device__ constexpr float gelu_series_d(int n) {
-  double d = kInvSqrt2Pi;
-  for (int k = 1; k <= n; ++k) d /= 2.0 * k;  // 2^n n!
-  return (float)(((n & 1) ? -d : d) / (2 * n + 1));
-}
+// GELU for |v| <= 1 (the fused conv3d chain clamps to [-1, 1] first):
+//   GELU(v) = v/2 + v/2 erf(v / sqrt 2) = v/2 + s R(s),   s = v^2,
+// with R(s) = (GELU(v) - v/2) / s an even, entire function of v, replaced on
+// s in [0, 1] by the degree-4 polynomial below: the minimax fit of the GELU
+// error s (R(s) - p(s)) by weighted least squares with Lawson's iteration,
+// computed by gen_gelu_poly.py next to this file.  Fit error 4e-9; in fp32
+// Horner form within 1e-7 of GELU on [-1, 1] (the result's own rounding
+// level), far inside the 1e-4 tolerance.
+constexpr float kGeluR0 = 0.39894208f, kGeluR1 = -0.06648772f, kGeluR2 = 0.00996112f,
+                kGeluR3 = -0.0011617212f, kGeluR4 = 9.097826e-05f;  // s^0 .. s^4
 
 __device__ __forceinline__ float op_gelu_small(float v) {
   const float s = v * v;
-  float r = gelu_series_d(7);
-#pragma unroll
-  for (int n = 6; n >= 0; --n) r = fmaf(r, s, gelu_series_d(n));
+  float r = fmaf(kGeluR4, s, kGeluR3);
+  r = fmaf(r, s, kGeluR2);
+  r = fmaf(r, s, kGeluR1);
+  r = fmaf(r, s, kGeluR0);
   return fmaf(s, r, 0.5f * v);
 }
 
 // The same for two values on the paired fp32 pipe (bit-identical per lane).
 __device__ __forceinline__ uint64_t op_gelu_small2(uint64_t v) {
   const uint64_t s = ptx::mul2(v, v);
-  uint64_t r = ptx::pk2(gelu_series_d(7), gelu_series_d(7));
-#pragma unroll
-  for (int n = 6; n >= 0; --n) r = ptx::fma2(r, s, ptx::pk2(gelu_series_d(n), gelu_series_d(n)));
+  uint64_t r = ptx::fma2(ptx::pk2(kGeluR4, kGeluR4), s, ptx::pk2(kGeluR3, kGeluR3));
+  r = ptx::fma2(r, s, ptx::pk2(kGeluR2, kGeluR2));
+  r = ptx::fma2(r, s, ptx::pk2(kGeluR1, kGeluR1));
+  r = ptx::fma2(r, s, ptx::pk2(kGeluR0, kGeluR0));
   return ptx::fma2(s, r, ptx::mul2(v, ptx::pk2(0.5f, 0.5f)));
 }
 
