@@ -518,6 +518,40 @@ def test_convT_pool_mean_odd_extent_floor():
                                atol=1e-14)
 
 
+def _brute_convT(x, w, b, s, p, op):
+    """Scatter loop for a transposed conv: x[ci, i, j] adds x * w[ci, co, kh, kw]
+    to output (i*s + kh - p, j*s + kw - p)."""
+    N, C, H, W = x.shape
+    CO, K = w.shape[1], w.shape[2]
+    Ho, Wo = (H - 1) * s - 2 * p + K + op, (W - 1) * s - 2 * p + K + op
+    y = np.zeros((N, CO, Ho, Wo)) + b.astype(np.float64)[None, :, None, None]
+    for n, ci, i, j in np.ndindex(N, C, H, W):
+        for co, kh, kw in np.ndindex(CO, K, K):
+            oi, oj = i * s + kh - p, j * s + kw - p
+            if 0 <= oi < Ho and 0 <= oj < Wo:
+                y[n, co, oi, oj] += float(x[n, ci, i, j]) * float(w[ci, co, kh, kw])
+    return y
+
+
+@pytest.mark.parametrize("op", [0, 1])
+def test_convT_stride2_pool_mean_composition(op):
+    """Stride-2 transposed conv (pad 1, output padding 0 or 1) -> 2x2 max
+    pool (floor extent) -> hardtanh -> mean -> tanh, against an independent
+    scatter loop and a numpy tail."""
+    st = _rng(18 + op)
+    x = st.normal((2, 3, 5, 6))
+    w = st.uniform((3, 4, 3, 3), 0.4)
+    b = st.uniform((4,), 0.3)
+    y = _brute_convT(x, w, b, 2, 1, op)
+    assert y.shape[2:] == ((5 - 1) * 2 + 1 + op, (6 - 1) * 2 + 1 + op)
+    Hp, Wp = y.shape[2] // 2, y.shape[3] // 2
+    pooled = y[:, :, :2 * Hp, :2 * Wp].reshape(2, 4, Hp, 2, Wp, 2).max(axis=(3, 5))
+    ref = np.tanh(np.clip(pooled, -1, 1).mean(axis=(2, 3)))
+    out = oracle.convT_pool_mean(x, w, b, stride=2, pad=1, out_pad=op)
+    np.testing.assert_allclose(out[:, :, 0, 0], ref, atol=1e-13)
+    np.testing.assert_allclose(oracle.convT2d(x, w, b, 2, 1, op), y, atol=1e-12)
+
+
 # ------------------------------------------------------------ the generator
 def test_synth_generator_is_deterministic_and_distributed():
     a = synth.make_inputs(1)
