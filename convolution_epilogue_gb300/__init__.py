@@ -302,9 +302,10 @@ def pool_mean_ops(lo=-1.0, hi=1.0):
 
 
 def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
-                         ws=None, stream=None):
-    """ConvTranspose2d(k=3, s=1, p=1) + bias -> maxpool 2x2 -> hardtanh ->
-    mean(H,W) -> tanh.  w: [C_in, C_out, 3, 3]; returns y [N, C_out, 1, 1]."""
+                         ws=None, stream=None, stride=1, out_pad=0):
+    """ConvTranspose2d(k=3, stride 1 or 2, p=1, out_pad) + bias -> maxpool
+    2x2 -> hardtanh -> mean(H,W) -> tanh.  w: [C_in, C_out, 3, 3]; returns
+    y [N, C_out, 1, 1]."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -318,7 +319,8 @@ def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
     if ws is None:
         ws = _workspace(workspace_bytes(2, (N, C, H, W, CO, K, pad)), x.device)
     e, keep = make_epilogue(bias, pool_mean_ops(*hardtanh))
-    st = lib().fc_convT2d_pool_mean(_ptr(x), N, C, H, W, _ptr(w), CO, K, 1, pad, 0,
+    st = lib().fc_convT2d_pool_mean(_ptr(x), N, C, H, W, _ptr(w), CO, K, int(stride), pad,
+                                    int(out_pad),
                                     ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
                                     _stream_handle(stream))
     _check(st, "fc_convT2d_pool_mean")

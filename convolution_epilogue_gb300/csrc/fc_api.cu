@@ -119,6 +119,7 @@ bool fits_int32(long long v) { return v >= 0 && v < (1LL << 31); }
 // benchmark's per-variant table): the tensor-core f16-split path wins once
 // there is enough work; tiny problems go to whichever finished first.
 int auto_variant(const ConvProblem &p) {
+  if (p.subpix) return tc_supported(p, 1) ? FC_VARIANT_TC_F16X3 : FC_VARIANT_TC_TF32X3;
   const double macs = (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
   if (tc_supported(p, 1) && macs >= 4.0e8) return FC_VARIANT_TC_F16X3;
   if (tc_supported(p, 0) && macs >= 4.0e8) return FC_VARIANT_TC_TF32X3;
@@ -136,7 +137,8 @@ fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
     return FC_ERR_WORKSPACE;
   int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : auto_variant(p);
   if ((v == FC_VARIANT_TC_TF32X3 && !tc_supported(p, 0)) ||
-      (v == FC_VARIANT_TC_F16X3 && !tc_supported(p, 1)))
+      (v == FC_VARIANT_TC_F16X3 && !tc_supported(p, 1)) ||
+      (v == FC_VARIANT_FFMA && p.subpix))  // the CUDA-core kernel has no parity-class form
     return FC_ERR_UNSUPPORTED;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int launches = 0;
@@ -334,8 +336,10 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || k < 1 || stride < 1 ||
       pad < 0 || out_pad < 0)
     return FC_ERR_INVALID_ARG;
-  if (stride != 1 || k != 3 || pad != 1 || out_pad != 0) return FC_ERR_UNSUPPORTED;
-  // transposed-conv output extent (H-1)*s - 2p + k + op = H for these values
+  if (k != 3 || pad != 1 || !((stride == 1 && out_pad == 0) || (stride == 2 && out_pad <= 1)))
+    return FC_ERR_UNSUPPORTED;
+  // transposed-conv output extent (H-1)*s - 2p + k + op: H at stride 1,
+  // 2H - 1 + op at stride 2
   const int Ho = (H - 1) * stride - 2 * pad + k + out_pad;
   const int Wo = (W - 1) * stride - 2 * pad + k + out_pad;
   if (Ho < 2 || Wo < 2) return FC_ERR_INVALID_ARG;
@@ -352,8 +356,14 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   p.x = x; p.w = w; p.y = y;
   p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
   p.CO = C_out; p.KD = 1; p.KH = k; p.KW = k;
-  // the equivalent conv: swapped + flipped weights, padding k - 1 - p
-  p.pad_d = 0; p.pad = k - 1 - pad;
+  if (stride == 1) {
+    // the equivalent conv: swapped + flipped weights, padding k - 1 - p
+    p.pad_d = 0; p.pad = k - 1 - pad;
+  } else {
+    // computed per output parity class on the input grid (tensor cores only)
+    p.pad_d = 0; p.pad = 0;
+    p.subpix = 1;
+  }
   p.stride = 1;
   p.dil = 1;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
@@ -415,7 +425,19 @@ size_t fc_workspace_bytes(int entry, const int *d) {
   }
   if (p.N < 0 || p.C < 1 || p.CO < 1 || p.KH < 1 || p.Ho < 1 || p.Wo < 1 || p.Do < 1)
     return 0;
-  return ws_layout(p).total;
+  size_t total = ws_layout(p).total;
+  if (entry == 2) {
+    // the size covers every supported stride: stride 2 (output padding 0
+    // or 1) has its own per-tile partials
+    for (int op = 0; op <= 1; ++op) {
+      ConvProblem q = p;
+      q.subpix = 1; q.pad = 0;
+      q.Ho = 2 * p.H - 1 + op; q.Wo = 2 * p.W - 1 + op;
+      const size_t t = ws_layout(q).total;
+      if (t > total) total = t;
+    }
+  }
+  return total;
 }
 
 fc_status fc_set_variant(int v) {

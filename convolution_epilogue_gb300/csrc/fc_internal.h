@@ -43,6 +43,10 @@ struct ConvProblem {
   int Do, Ho, Wo;
   int wlayout;     // 0: conv [CO][C][KD][KH][KW]; 1: convT [C][CO][KH][KW]
   int pool;        // 1: 2x2 maxpool -> hardtanh -> mean -> tanh
+  // 1: stride-2 transposed conv (k 3, pad 1) computed per output parity
+  // class on the input grid (x, w in transposed-conv form, no rewrite);
+  // Ho, Wo are then the transposed conv's output extents.
+  int subpix;
   float ht_lo, ht_hi;
   int chain;       // ChainId
   int entry;       // 0 conv2d, 1 conv3d, 2 convT-pool-mean (for profiling)

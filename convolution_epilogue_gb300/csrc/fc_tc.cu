@@ -124,6 +124,13 @@ struct TcPlan {
   // one shifted descriptor start per tap.  DIL is the dilation.
   int S2, DIL, LW, SR, SUB, DSL;
   uint8_t perm[28];  // K order of the taps (paired taps: increasing shifts)
+  // Stride-2 transposed conv by output parity class (SP): K step ks feeds
+  // class kcls[ks] & 3 (accumulator (kcls & 3) x 128 columns); bit 7 marks
+  // the class's first K step of a chunk.  skd[ks] is the step's A start |
+  // slice distance << 16 (16-byte units), computed here on the host.
+  int SP;
+  uint8_t kcls[28];
+  uint32_t skd[28];
   int NPIX;
   int plane_bytes;
   int a_stage_bytes;
@@ -149,6 +156,7 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort;
   uint32_t kdelta[28];  // per K step: A start (16-byte units) | slice distance << 16
+  uint32_t kcls[28];    // per K step (stride-2 transposed conv): class | first << 7
   alignas(16) float red[4][64];          // pool: per-warp partial sums
   alignas(16) float bias[kMaxCoTc];      // bias per output channel (0 without bias)
   alignas(16) float addend[kMaxCoTc];    // per-channel addend of the fused GELU chain
@@ -285,11 +293,127 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   return q;
 }
 
+// Stride-2 transposed conv (k 3, pad 1) + pool by output parity class.
+// Output (2i + a, 2j + b) of the transposed conv sums the taps (kh, kw)
+// with a + 1 - kh and b + 1 - kw even, each reading input
+// (i + (a + 1 - kh) / 2, j + (b + 1 - kw) / 2): class (0,0) has tap (1,1);
+// (0,1) taps (1,2), (1,0); (1,0) taps (2,1), (0,1); (1,1) the four corners.
+// The 2x2 pool window at (i, j) holds exactly the four classes at (i, j),
+// so a unit is one M tile of pooled pixels (R rows of WT pooled columns on
+// the input grid) with one accumulator per class, and the epilogue takes
+// the max over the four accumulators lane by lane.  Staging is a stride-1
+// input tile with a one-pixel halo (R + 1 rows, WT + 1 columns).
+TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
+  TcPlan q{};
+  if (!p.pool || p.KH != 3 || p.KW != 3 || p.KD != 1 || p.wlayout != 1) return q;
+  plan_chunks(p, prec, q);
+  q.SP = 1;
+  q.DIL = 1;
+  const int Hp = p.Ho / 2, Wp = p.Wo / 2;  // pooled extents
+  const bool rowpack = Wp + 1 <= 128;
+  if (rowpack) {
+    q.RS = Wp + 1;
+    q.WT = Wp;
+    q.n_ct = 1;
+    q.R = 128 / q.RS;
+  } else {
+    q.RS = 129;
+    q.WT = 128;
+    q.n_ct = cdiv(Wp, 128);
+    q.R = 1;
+  }
+  q.U = 1;
+  q.RIN = q.R + 1;
+  q.LW = q.RS;
+  q.DSL = q.RIN * q.RS;
+  // K slots class by class, each class's taps by increasing shift; with
+  // paired taps class (0,0) takes a zero-weight slot so no pair straddles
+  // two classes.  10 (paired) or 9 slots.
+  static const int kTaps[4][4] = {{4, -1, -1, -1}, {5, 3, -1, -1}, {7, 1, -1, -1}, {8, 6, 2, 0}};
+  static const int kNTaps[4] = {1, 2, 2, 4};
+  int slot = 0, shift[28];
+  int slot_cls[28];
+  for (int cls = 0; cls < 4; ++cls) {
+    const int a = cls >> 1, b = cls & 1;
+    for (int k = 0; k < kNTaps[cls]; ++k) {
+      const int tap = kTaps[cls][k], kh = tap / 3, kw = tap % 3;
+      q.perm[slot] = (uint8_t)tap;
+      shift[slot] = ((a + 1 - kh) / 2) * q.RS + (b + 1 - kw) / 2;
+      slot_cls[slot++] = cls;
+    }
+    if (q.pairtaps && (kNTaps[cls] & 1)) {
+      q.perm[slot] = 255;
+      shift[slot] = shift[slot - 1] + 1;  // any staged data: zero weights
+      slot_cls[slot++] = cls;
+    }
+  }
+  const int nslots = slot;
+  if (q.KS != (q.pairtaps ? nslots / 2 : nslots)) return q;
+  for (int t = nslots; t < 28; ++t) q.perm[t] = 255;
+  int prev = -1;
+  for (int ks = 0; ks < q.KS; ++ks) {
+    const int s0 = q.pairtaps ? 2 * ks : ks;
+    const int cls = slot_cls[s0];
+    q.kcls[ks] = (uint8_t)(cls | (cls != prev ? 0x80 : 0));
+    prev = cls;
+    uint32_t lbo;
+    if (q.pairtaps) {
+      lbo = (uint32_t)(shift[s0 + 1] - shift[s0]);  // > 0 (increasing shifts)
+    } else {
+      lbo = 0;  // filled in below once the plane size is known
+    }
+    q.skd[ks] = (uint32_t)shift[s0] | (lbo << 16);
+  }
+  int maxshift = 0;
+  for (int t = 0; t < nslots; ++t) maxshift = shift[t] > maxshift ? shift[t] : maxshift;
+  int npix = maxshift + 1 + 127 + 1;
+  if (npix < q.RIN * q.RS) npix = q.RIN * q.RS;
+  q.NPIX = cdiv(npix, 8) * 8;
+  q.plane_bytes = q.NPIX * 16;
+  if (!q.pairtaps)
+    for (int ks = 0; ks < q.KS; ++ks) q.skd[ks] |= (uint32_t)(q.plane_bytes >> 4) << 16;
+  q.a_stage_bytes = 2 * q.P * q.plane_bytes;
+  if (q.COB * 64 > kMaxCoTc) return q;
+  q.n_rt = cdiv(Hp, q.R);
+  q.units = (long)q.COB * p.N * q.n_rt * q.n_ct;
+  if (q.units >= (1L << 31)) return q;
+  q.fd_ct = make_fastdiv((uint32_t)q.n_ct);
+  q.fd_rt = make_fastdiv((uint32_t)q.n_rt);
+  q.fd_do = make_fastdiv(1u);
+  q.fd_n = make_fastdiv((uint32_t)p.N);
+  q.fd_cb = make_fastdiv((uint32_t)((long)p.N * q.n_rt * q.n_ct));
+  q.NACC = 1;
+  q.tmem_cols = 512;  // four class accumulators of 128 columns
+  const int misc = 512 + (int)sizeof(SmemCtl) + 256;
+  const long b_all = (long)q.COB * q.NCH * q.b_chunk_bytes;
+  int S = 0, resident = 0, SB = 0;
+  for (int s = 4; s >= 2 && !S; --s)
+    if ((long)s * q.a_stage_bytes + b_all + misc <= kMaxSmem) { S = s; resident = 1; }
+  if (!S)
+    for (int s = 4; s >= 1 && !S; --s)
+      if ((long)s * q.a_stage_bytes + 2L * q.b_chunk_bytes + misc <= kMaxSmem) { S = s; SB = 2; }
+  if (!S)
+    for (int s = 2; s >= 1 && !S; --s)
+      if ((long)s * q.a_stage_bytes + 1L * q.b_chunk_bytes + misc <= kMaxSmem) { S = s; SB = 1; }
+  if (!S) return q;
+  q.S = S;
+  q.b_resident = resident;
+  q.SB = resident ? 1 : SB;
+  q.off_b = S * q.a_stage_bytes;
+  q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
+  q.off_misc = q.off_bar + 512;
+  q.smem_bytes = q.off_bar + misc;
+  if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;
+  q.ok = 1;
+  return q;
+}
+
 // Pooling pairs two output rows per unit.  Without pooling a unit also
 // takes two M tiles (half the barrier hand-offs per MMA, fewer re-staged
 // halo rows) when the image has rows for both and shared memory still holds
 // at least three stages; otherwise one.
 TcPlan make_plan(const ConvProblem &p, int prec) {
+  if (p.subpix) return make_plan_subpix(p, prec);
   if (p.pool) return make_plan_u(p, prec, 2);
   TcPlan q2 = make_plan_u(p, prec, 2);
   if (q2.ok && q2.S >= 3 && p.Ho > q2.R) return q2;
@@ -426,7 +550,9 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
     if (tap < q.TAPS && ci < p.C && co < p.CO) {
       if (p.wlayout == 0) {
         w = p.w[((long)co * p.C + ci) * q.TAPS + tap];
-      } else {  // transposed conv: swap channel axes, flip both taps
+      } else if (q.SP) {  // transposed conv by parity class: W[ci][co][kh][kw] as is
+        w = p.w[((long)ci * p.CO + co) * 9 + tap];
+      } else {  // transposed conv as a conv: swap channel axes, flip both taps
         const int kh = tap / 3, kw = tap % 3;
         w = p.w[(((long)ci * p.CO + co) * 3 + (2 - kh)) * 3 + (2 - kw)];
       }
@@ -642,6 +768,39 @@ __device__ __forceinline__ void issue_chunk_loop(const uint32_t *kd_smem, int KS
   }
 }
 
+// Issues one chunk of the stride-2 transposed conv by parity class: K step
+// ks adds into accumulator (kcls[ks] & 3) x 128 columns; the class's first
+// K step of the unit's first chunk starts the accumulator (accumulate 0).
+template <int PREC>
+__device__ __forceinline__ void issue_subpix(const uint32_t *kd_smem, const uint32_t *kc_smem,
+                                             int KS, uint32_t a_lo, uint32_t b_lo, uint32_t dacc,
+                                             uint32_t lo_delta, bool first_chunk) {
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
+  const volatile uint32_t *kt = kd_smem;
+  const volatile uint32_t *kc = kc_smem;
+#pragma unroll 1
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t ah = a_lo + kt[ks];
+    const uint32_t cls = kc[ks];
+    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+    const uint32_t accum = (first_chunk && (cls & 0x80u)) ? 0u : 1u;
+    const uint32_t d = dacc + (cls & 3u) * 128u;
+    if (ptx::elect_one()) {
+      if constexpr (PREC == 0) {
+        ptx::mma_tf32(d, desc_hi | ah, bd, idesc1, accum);
+        ptx::mma_tf32(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
+      } else {
+        ptx::mma_f16(d, desc_hi | ah, bd, idesc1, accum);
+        ptx::mma_f16(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Sums v[0..15] over the 32 lanes of a warp: after the call lane l holds in
 // v[0] the total of the value v[(l >> 1) & 15] had on every lane.
 __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
@@ -658,13 +817,14 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial) {
   constexpr int E = PREC ? 8 : 4;
   static_assert(U == 1 || U == 2, "one or two M tiles per unit");
-  static_assert(!POOL || U == 2, "pooling takes two output rows per unit");
+  static_assert(!POOL || U == 2 || SP, "pooling takes two output rows per unit");
+  static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -701,7 +861,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (tid < q.KS) {
+  if (SP && tid < q.KS) {  // per-class K steps, laid out on the host
+    ctl->kdelta[tid] = q.skd[tid];
+    ctl->kcls[tid] = q.kcls[tid];
+  } else if (tid < q.KS) {
     uint32_t off16, lbo16;
     if (q.pairtaps) {  // slices: taps 2ks and 2ks+1 (a zero-weight slice past the last)
       const int t0 = q.perm[2 * tid], t1 = q.perm[2 * tid + 1];
@@ -951,7 +1114,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t first = c != 0;
         if constexpr (POOL) {
           // both tiles per K step (measured faster for the pooled chunks)
-          issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
+          if constexpr (SP)
+            issue_subpix<PREC>(ctl->kdelta, ctl->kcls, q.KS, a_lo, b_lo, dacc, lo_delta, c == 0);
+          else
+            issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
         } else {
           // Tile by tile, each committed to its own accumulator-full barrier:
           // the epilogue starts on a tile once its last chunk's MMAs are done.
@@ -1129,6 +1295,52 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           if (lane == 0) ptx::mbar_arrive(&acc_empty[acc * U + t]);
         }
         if (!okt) break;
+      } else if constexpr (SP) {
+        // lane m = pooled pixel (rt R + m_row, ct WT + m_col); the 2x2 window
+        // is the four class accumulators of that lane
+        const int pi = up.rt * q.R + m_row, pj = up.ct * q.WT + m_col;
+        const bool valid = m_row < q.R && m_col < q.WT && pi < p.Ho / 2 && pj < p.Wo / 2;
+#pragma unroll 1
+        for (int cc = 0; cc < 32; cc += 16) {
+          float mx[16], bv[16];
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(&bv[j]) =
+                *reinterpret_cast<const float4 *>(&ctl->bias[co_base + ch0 + cc + j]);
+#pragma unroll 1
+          for (int cls = 0; cls < 4; ++cls) {
+            uint32_t h[16], l[16];
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + ch0 + cc), h);
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + 64 + ch0 + cc), l);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float v = fmaf(scale, __uint_as_float(l[j]), __uint_as_float(h[j])) + bv[j];
+              mx[j] = cls ? fmaxf(mx[j], v) : v;
+            }
+          }
+          float part[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            part[j] = valid ? fminf(fmaxf(mx[j], p.ht_lo), p.ht_hi) : 0.0f;
+          lane_sum16(part, lane);
+          if ((lane & 1) == 0) ctl->red[quad][ch0 + cc + ((lane >> 1) & 15)] = part[0];
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+        epi_sync();
+        if (warp == 0) {
+          const int T = q.n_rt * q.n_ct;
+          const int t = up.rt * q.n_ct + up.ct;
+          float *dst = partial + ((long)up.n * T + t) * p.CO;
+          for (int j = lane; j < 64; j += 32) {
+            const int co = co_base + j;
+            if (co < p.CO)
+              dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
+          }
+        }
+        epi_sync();
       } else {
         const int c = m;  // one output row per M tile
         const int ow = up.ct * q.WT + c;
@@ -1215,10 +1427,10 @@ __global__ void selftest_wait_kernel(unsigned int *status, uint64_t limit_ns) {
 
 int g_num_sms = 0;
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                           float *partial, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2>;
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1253,6 +1465,7 @@ cudaError_t launch_chain(const ConvProblem &p, const TcPlan &q, const uint8_t *b
 template <int PREC>
 cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                         float *partial, cudaStream_t s) {
+  if (p.subpix) return launch_kernel<PREC, CHAIN_NONE, true, 1, false, true>(p, q, bimg, partial, s);
   if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, s);
   // stride 2 (even / odd sub-plane staging) is its own instance, so the
   // stride-1 producer carries none of its index arithmetic

@@ -165,10 +165,15 @@ FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, in
 /* ConvTranspose2d + bias -> MaxPool2d(2,2) -> Hardtanh[a,b] -> mean(H,W)
  * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];
  * y [N][C_out][1][1].  The epilogue chain must be exactly
- * MAXPOOL2X2, HARDTANH(a, b), MEAN_HW, TANH.  Supported: stride 1,
- * k = 3, pad 1, out_pad 0 (conv output extent Ho = H, Wo = W; H, W >= 2).
- * The mean is reduced in a fixed order (per-tile partials, then a second
- * kernel sums them in index order), so results are bitwise reproducible. */
+ * MAXPOOL2X2, HARDTANH(a, b), MEAN_HW, TANH.  Supported: k = 3, pad 1 and
+ *   stride 1, out_pad 0: conv output extent Ho = H, Wo = W (H, W >= 2);
+ *   stride 2, out_pad 0 or 1: Ho = 2H - 1 + out_pad (likewise Wo; the
+ *   output-size formula (H-1)s - 2p + k + op of trace "Kimi-K2.6__l2_p10"),
+ *   computed per output parity class on the tensor-core variants only
+ *   (FC_VARIANT_FFMA returns FC_ERR_UNSUPPORTED; AUTO picks tensor cores).
+ * The 2x2 pool takes the floor extent (Ho / 2, Wo / 2).  The mean is
+ * reduced in a fixed order (per-tile partials, then a second kernel sums
+ * them in index order), so results are bitwise reproducible. */
 FC_API fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
                                const float *w, int C_out, int k, int stride,
                                int pad, int out_pad, const fc_epilogue *epi,
@@ -176,7 +181,8 @@ FC_API fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, in
                                void *stream);
 
 /* Workspace bytes needed by one call.  entry: 0 = fc_conv2d_epi,
- * 1 = fc_conv3d_epi, 2 = fc_convT2d_pool_mean.  dims:
+ * 1 = fc_conv3d_epi, 2 = fc_convT2d_pool_mean (any supported stride and
+ * out_pad).  dims:
  *   entry 0: {N, C_in, H, W, C_out, k, pad}
  *   entry 1: {N, C_in, D, H, W, C_out, k, pad}
  *   entry 2: {N, C_in, H, W, C_out, k, pad}

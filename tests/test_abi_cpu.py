@@ -96,9 +96,13 @@ def test_pool_entry_requires_exact_chain(L):
     assert st == 2
     e, _ = _epi(fc.pool_mean_ops())
     st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
-                                4, 3, 2, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
+                                4, 3, 3, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
                                 ctypes.c_void_p(256), 1 << 20, None)
-    assert st == 2  # stride 2 is not supported
+    assert st == 2  # stride 3 is not supported (1 and 2 are)
+    st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
+                                4, 3, 1, 1, 1, ctypes.byref(e), ctypes.c_void_p(16),
+                                ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 2  # output padding 1 only with stride 2
 
 
 def test_no_cpu_fallback_without_gpu(L):

@@ -482,3 +482,75 @@ def test_generic_chain_every_op(variant, shape):
            ("gelu_erf",), ("tanh",), ("hardswish",), ("clamp", -0.2, 0.6))
     got = _run_conv_strided(variant, x, w, b, ops, 1, 1)
     _check(got, oracle.conv_epi(x, w, b, ops, pad=1), f"{variant} generic chain {shape}")
+
+
+# ------------------------------------------- stride-2 transposed conv + pool
+def _run_pool_s2(variant, x, w, b, op, ht=(-1.0, 1.0)):
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b) if b is not None else None,
+                                   hardtanh=ht, stride=2, out_pad=op)
+        if variant != "auto":
+            assert m.last_variant() == variant
+        assert m.get_last_device_error() == 0
+        return y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
+
+
+@pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
+@pytest.mark.parametrize("shape,op", [
+    ((2, 64, 16, 20, 64), 1),   # several pooled rows per tile
+    ((1, 8, 9, 33, 64), 0),     # C_in 8: paired taps; odd extents (floor pool)
+    ((2, 16, 12, 140, 70), 1),  # 128-column strips, C_out > 64
+    ((1, 3, 5, 7, 64), 0),      # C_in not a multiple of 8, tiny image
+    ((1, 8, 6, 127, 64), 1),    # one pooled row of 127 per tile
+])
+def test_convT_stride2_pool_mean(variant, shape, op):
+    """Stride-2 transposed conv (pad 1, output padding 0 or 1) + 2x2 max pool
+    + hardtanh + mean + tanh, computed per output parity class, against the
+    oracle's scatter-form transposed conv."""
+    N, C, H, W, CO = shape
+    st = synth.seeded(760 + C + op)
+    x = st.normal((N, C, H, W))
+    w = st.uniform((C, CO, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((CO,), 0.1)
+    ht = (-0.5, 0.7)
+    got = _run_pool_s2(variant, x, w, b, op, ht)
+    ref = oracle.convT_pool_mean(x, w, b, stride=2, pad=1, out_pad=op, hardtanh=ht)
+    _check(got, ref, f"{variant} convT stride 2 {shape} op {op}")
+
+
+def test_convT_stride2_refused_by_cuda_core_variant():
+    m = fc()
+    x = _dev(np.zeros((1, 8, 8, 8), np.float32))
+    w = _dev(np.zeros((8, 64, 3, 3), np.float32))
+    m.set_variant("ffma")
+    try:
+        with pytest.raises(m.FcError):
+            m.fc_convT2d_pool_mean(x, w, None, stride=2, out_pad=1)
+    finally:
+        m.set_variant("auto")
+
+
+@pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
+def test_convT_stride2_full_size_sampled(variant):
+    """x [128,64,128,128] -> transposed conv 256 x 256 (stride 2, output
+    padding 1) -> pooled 128 x 128 -> mean: sampled (n, c) outputs."""
+    inp = _full_inputs(5)
+    x = inp["x"][:, :, ::2, ::2].copy()  # 128 x 64 x 128 x 128 from the same draw
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_convT2d_pool_mean(_dev(x), _dev(inp["w"]), _dev(inp["b"]), stride=2, out_pad=1)
+        assert m.get_last_device_error() == 0
+        ynp = y.cpu().numpy().reshape(128, 64)
+    finally:
+        m.set_variant("auto")
+    rng = np.random.default_rng(7)
+    pairs = [(0, 0), (127, 63)] + [(int(rng.integers(128)), int(rng.integers(64)))
+                                   for _ in range(14)]
+    ref = oracle.convT_pool_mean_points(x, inp["w"], inp["b"], pairs, stride=2, pad=1, out_pad=1)
+    got = np.array([ynp[n, c] for n, c in pairs])
+    _check(got, ref, f"convT stride 2 sampled [{variant}]")
