@@ -426,6 +426,8 @@ def run_ours(args):
                 fc, d[3], flush, stream, peaks, stride=2, pad=0, dilation=1),
             "conv2d_dilation2_pad2_relu_hardswish_128x8x128x128": widened_conv(
                 fc, d[3], flush, stream, peaks, stride=1, pad=2, dilation=2),
+            "convT2d_stride2_outpad1_pool_mean_128x64x128x128": widened_convT_s2(
+                fc, d[5], flush, stream, peaks),
         }
 
     # end to end through the public API with host buffers
@@ -529,6 +531,43 @@ def widened_conv(fc, d3, flush, stream, peaks, stride, pad, dilation, reps=20):
     nbytes = 4.0 * (x.numel() + w.numel() + b.numel() + y.numel())
     pk, _, basis = pipe_peak_tflops(variant, peaks)
     t_roof = max(flops / (pk * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    return {"variant": variant, "ms_median": ms, "gflops": flops / (ms * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms, "peak_basis": basis}
+
+
+def widened_convT_s2(fc, d5, flush, stream, peaks, reps=20):
+    """Stride-2 transposed conv (k 3, pad 1, output padding 1) on x
+    [128,64,128,128] (every other row and column of the pooled workload's
+    input) -> 256 x 256 -> 2x2 max pool -> hardtanh -> mean -> tanh.  Useful
+    FLOPs = 2 x N x C_in x C_out x H x W x 9 (each input pixel meets each of
+    the 9 taps once); roofline = max(FLOPs at the used pipe's peak, bytes at
+    HBM bandwidth)."""
+    import torch
+    x = d5["x"][:, :, ::2, ::2].contiguous()
+    w, b = d5["w"], d5["b"]
+    N, C, H, W = x.shape
+    CO = w.shape[1]
+    y = torch.empty((N, CO, 1, 1), dtype=torch.float32, device=x.device)
+    call = lambda: fc.fc_convT2d_pool_mean(x, w, b, y=y, stride=2, out_pad=1)
+    call()
+    variant = fc.last_variant()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if fc.get_last_device_error() != 0:
+        raise RuntimeError("device status word set in the stride-2 transposed conv")
+    ms = statistics.median(ts)
+    flops = 2.0 * N * C * CO * H * W * 9
+    nbytes = 4.0 * (x.numel() + w.numel() + b.numel() + y.numel())
+    pk, _, basis = pipe_peak_tflops(variant, peaks)
+    t_roof = max(flops / (pk * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
+    del x
     return {"variant": variant, "ms_median": ms, "gflops": flops / (ms * 1e-3) / 1e9,
             "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms, "peak_basis": basis}
 
