@@ -131,6 +131,12 @@ struct TcPlan {
   int SP;
   uint8_t kcls[28];
   uint32_t skd[28];
+  // SP with a unit's chunks and weights all resident (NCH <= S): the MMAs
+  // of classes (0,0), (0,1) (half A, TMEM columns 0-255) run over every
+  // chunk before those of (1,0), (1,1) (half B, 256-511), each half with its
+  // own accumulator barriers, so the epilogue's work on one half overlaps
+  // the MMAs of the other.  KA = the K steps of half A.
+  int SPLIT, KA;
   int NPIX;
   int plane_bytes;
   int a_stage_bytes;
@@ -404,6 +410,8 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
   q.off_misc = q.off_bar + 512;
   q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;
+  q.KA = q.pairtaps ? 2 : 3;  // classes (0,0), (0,1): 1 + 2 taps
+  q.SPLIT = (q.b_resident && q.NCH <= q.S) ? 1 : 0;
   q.ok = 1;
   return q;
 }
@@ -771,18 +779,18 @@ __device__ __forceinline__ void issue_chunk_loop(const uint32_t *kd_smem, int KS
 // Issues one chunk of the stride-2 transposed conv by parity class: K step
 // ks adds into accumulator (kcls[ks] & 3) x 128 columns; the class's first
 // K step of the unit's first chunk starts the accumulator (accumulate 0).
-template <int PREC>
-__device__ __forceinline__ void issue_subpix(const uint32_t *kd_smem, const uint32_t *kc_smem,
-                                             int KS, uint32_t a_lo, uint32_t b_lo, uint32_t dacc,
+// Fully unrolled over KS (5 paired or 9 single K steps) with the step
+// tables in registers, so no shared-memory load sits between two bursts.
+template <int PREC, int K0, int K1>
+__device__ __forceinline__ void issue_subpix(const uint32_t (&kt)[28], const uint32_t (&kc)[9],
+                                             uint32_t a_lo, uint32_t b_lo, uint32_t dacc,
                                              uint32_t lo_delta, bool first_chunk) {
   constexpr uint32_t fmt = PREC ? 0u : 2u;
   constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
   constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
   constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
-  const volatile uint32_t *kt = kd_smem;
-  const volatile uint32_t *kc = kc_smem;
-#pragma unroll 1
-  for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+  for (int ks = K0; ks < K1; ++ks) {
     const uint32_t ah = a_lo + kt[ks];
     const uint32_t cls = kc[ks];
     const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
@@ -1053,6 +1061,9 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     uint32_t kdr[28];
 #pragma unroll
     for (int i = 0; i < 28; ++i) kdr[i] = ctl->kdelta[i];
+    uint32_t kcr[9];  // parity-class K steps (SP): class | first << 7
+#pragma unroll
+    for (int i = 0; i < 9; ++i) kcr[i] = SP ? ctl->kcls[i] : 0u;
     const uint32_t lo_delta = (uint32_t)((q.P * q.plane_bytes) >> 4);  // hi -> lo planes
     const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile (pool)
     uint32_t g = 0, gb = 0, it = 0;
@@ -1083,6 +1094,57 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         break;
       ptx::tc_fence_after();
       RT_MARK(1);  // waiting for a free accumulator
+      if constexpr (SP) {
+        if (q.SPLIT) {
+          // half A (classes (0,0), (0,1)) over every chunk, then half B; the
+          // generic wait above freed half A; a chunk's stage is released
+          // after its half-B MMAs
+          const int s0 = ms;
+          const uint32_t ph0 = mph;
+          int s = s0;
+          uint32_t ph = ph0;
+          for (int c = 0; ok && c < q.NCH; ++c) {
+            if (!(c == 0 && pre_full) &&
+                !wait_bar_warp(bars, A_FULL + s, ph, abort_flag, p.status, 0x22000000u | (g + c)))
+              ok = false;
+            ptx::tc_fence_after();
+            const uint32_t a_lo = ((sbase + (uint32_t)(s * q.a_stage_bytes)) >> 4) & 0x3FFFu;
+            const uint32_t bb = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
+            const uint32_t b_lo = ((bb >> 4) & 0x3FFFu) | ((2048u >> 4) << 16);
+            if (ok) {
+              if (q.KS == 5) issue_subpix<PREC, 0, 2>(kdr, kcr, a_lo, b_lo, tmem, lo_delta, c == 0);
+              else issue_subpix<PREC, 0, 3>(kdr, kcr, a_lo, b_lo, tmem, lo_delta, c == 0);
+            }
+            if (++s == q.S) { s = 0; ph ^= 1; }
+          }
+          if (!ok) break;
+          if (ptx::elect_one()) ptx::tc_commit(&acc_full[0]);
+          __syncwarp();
+          if (!wait_bar_warp(bars, ACC_EMPTY + 1, acc_par, abort_flag, p.status, 0x21100000u | it)) break;
+          ptx::tc_fence_after();
+          s = s0;
+          ph = ph0;
+          for (int c = 0; c < q.NCH; ++c) {
+            const uint32_t a_lo = ((sbase + (uint32_t)(s * q.a_stage_bytes)) >> 4) & 0x3FFFu;
+            const uint32_t bb = sbase + q.off_b + (uint32_t)(((long)cb * q.NCH + c) * q.b_chunk_bytes);
+            const uint32_t b_lo = ((bb >> 4) & 0x3FFFu) | ((2048u >> 4) << 16);
+            if (q.KS == 5) issue_subpix<PREC, 2, 5>(kdr, kcr, a_lo, b_lo, tmem, lo_delta, c == 0);
+            else issue_subpix<PREC, 3, 9>(kdr, kcr, a_lo, b_lo, tmem, lo_delta, c == 0);
+            if (ptx::elect_one()) ptx::tc_commit(&a_empty[s]);
+            __syncwarp();
+            if (++s == q.S) { s = 0; ph ^= 1; }
+          }
+          ms = s;
+          mph = ph;
+          g += (uint32_t)q.NCH;
+          pre_full = __all_sync(0xffffffffu, ptx::mbar_test_wait(&a_full[ms], mph));
+          pre_acc = __all_sync(0xffffffffu, ptx::mbar_test_wait(&acc_empty[0], mpar ^ 1));
+          if (ptx::elect_one()) ptx::tc_commit(&acc_full[1]);
+          __syncwarp();
+          RT_MARK(3);
+          continue;
+        }
+      }
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = ms;
         const uint32_t sph = mph;
@@ -1114,9 +1176,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t first = c != 0;
         if constexpr (POOL) {
           // both tiles per K step (measured faster for the pooled chunks)
-          if constexpr (SP)
-            issue_subpix<PREC>(ctl->kdelta, ctl->kcls, q.KS, a_lo, b_lo, dacc, lo_delta, c == 0);
-          else
+          if constexpr (SP) {
+            if (q.KS == 5) issue_subpix<PREC, 0, 5>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
+            else issue_subpix<PREC, 0, 9>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
+          } else
             issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
         } else {
           // Tile by tile, each committed to its own accumulator-full barrier:
@@ -1300,6 +1363,70 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         // is the four class accumulators of that lane
         const int pi = up.rt * q.R + m_row, pj = up.ct * q.WT + m_col;
         const bool valid = m_row < q.R && m_col < q.WT && pi < p.Ho / 2 && pj < p.Wo / 2;
+        if (q.SPLIT) {
+          // half A (classes (0,0), (0,1), columns 0-255) is ready (waited
+          // above); its max is kept while half B is computed
+          float keep[2][16];
+#pragma unroll
+          for (int g2 = 0; g2 < 2; ++g2) {
+            const int cc = g2 * 16;
+            uint32_t h0[16], l0[16], h1[16], l1[16];
+            ptx::tmem_ld16(tl + (uint32_t)(ch0 + cc), h0);
+            ptx::tmem_ld16(tl + (uint32_t)(64 + ch0 + cc), l0);
+            ptx::tmem_ld16(tl + (uint32_t)(128 + ch0 + cc), h1);
+            ptx::tmem_ld16(tl + (uint32_t)(192 + ch0 + cc), l1);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              keep[g2][j] = fmaxf(fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])),
+                                  fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])));
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[0]);
+          bool okw = wait_bar_warp(bars, ACC_FULL + 1, acc_par, abort_flag, p.status, 0x30100000u | it);
+          okw = epi_all(okw);
+          if (!okw) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int g2 = 0; g2 < 2; ++g2) {
+            const int cc = g2 * 16;
+            uint32_t h0[16], l0[16], h1[16], l1[16];
+            ptx::tmem_ld16(tl + (uint32_t)(256 + ch0 + cc), h0);
+            ptx::tmem_ld16(tl + (uint32_t)(320 + ch0 + cc), l0);
+            ptx::tmem_ld16(tl + (uint32_t)(384 + ch0 + cc), h1);
+            ptx::tmem_ld16(tl + (uint32_t)(448 + ch0 + cc), l1);
+            ptx::tmem_wait_ld();
+            float part[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              // bias is common to the four classes: added once after the max
+              const float v = fmaxf(keep[g2][j],
+                                    fmaxf(fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])),
+                                          fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j]))));
+              const float bias = ctl->bias[co_base + ch0 + cc + j];
+              part[j] = valid ? fminf(fmaxf(v + bias, p.ht_lo), p.ht_hi) : 0.0f;
+            }
+            lane_sum16(part, lane);
+            if ((lane & 1) == 0) ctl->red[quad][ch0 + cc + ((lane >> 1) & 15)] = part[0];
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[1]);
+          epi_sync();
+          if (warp == 0) {
+            const int T = q.n_rt * q.n_ct;
+            const int t = up.rt * q.n_ct + up.ct;
+            float *dst = partial + ((long)up.n * T + t) * p.CO;
+            for (int j = lane; j < 64; j += 32) {
+              const int co = co_base + j;
+              if (co < p.CO)
+                dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
+            }
+          }
+          epi_sync();
+          continue;
+        }
 #pragma unroll 1
         for (int cc = 0; cc < 32; cc += 16) {
           float mx[16], bv[16];
@@ -1308,14 +1435,18 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             *reinterpret_cast<float4 *>(&bv[j]) =
                 *reinterpret_cast<const float4 *>(&ctl->bias[co_base + ch0 + cc + j]);
 #pragma unroll 1
-          for (int cls = 0; cls < 4; ++cls) {
-            uint32_t h[16], l[16];
-            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + ch0 + cc), h);
-            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + 64 + ch0 + cc), l);
+          for (int cls = 0; cls < 4; cls += 2) {  // two classes per tensor-memory wait
+            uint32_t h0[16], l0[16], h1[16], l1[16];
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + ch0 + cc), h0);
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + 64 + ch0 + cc), l0);
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + 128 + ch0 + cc), h1);
+            ptx::tmem_ld16(tl + (uint32_t)(cls * 128 + 192 + ch0 + cc), l1);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float v = fmaf(scale, __uint_as_float(l[j]), __uint_as_float(h[j])) + bv[j];
+              const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bv[j];
+              const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bv[j];
+              const float v = fmaxf(v0, v1);
               mx[j] = cls ? fmaxf(mx[j], v) : v;
             }
           }
