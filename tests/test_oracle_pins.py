@@ -552,6 +552,27 @@ def test_convT_stride2_pool_mean_composition(op):
     np.testing.assert_allclose(oracle.convT2d(x, w, b, 2, 1, op), y, atol=1e-12)
 
 
+@pytest.mark.parametrize("pool", [(3, 2), (2, 1), (3, 3), (4, 2)])
+def test_convT_pool_mean_general_window(pool):
+    """Stride-1 transposed conv -> max pool of window k, stride s (floor
+    extent, overlapping when k > s) -> hardtanh -> mean -> tanh, against an
+    independent scatter loop and explicit window loops."""
+    k, s = pool
+    st = _rng(20 + k + s)
+    x = st.normal((2, 3, 9, 10))
+    w = st.uniform((3, 2, 3, 3), 0.4)
+    b = st.uniform((2,), 0.3)
+    y = _brute_convT(x, w, b, 1, 1, 0)
+    Hp, Wp = (y.shape[2] - k) // s + 1, (y.shape[3] - k) // s + 1
+    pooled = np.empty(y.shape[:2] + (Hp, Wp))
+    for i in range(Hp):
+        for j in range(Wp):
+            pooled[:, :, i, j] = y[:, :, i * s:i * s + k, j * s:j * s + k].max(axis=(2, 3))
+    ref = np.tanh(np.clip(pooled, -0.5, 0.8).mean(axis=(2, 3)))
+    out = oracle.convT_pool_mean(x, w, b, pool=pool, hardtanh=(-0.5, 0.8))
+    np.testing.assert_allclose(out[:, :, 0, 0], ref, atol=1e-13)
+
+
 # ------------------------------------------------------------ the generator
 def test_synth_generator_is_deterministic_and_distributed():
     a = synth.make_inputs(1)
