@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "FC_OK", 1: "FC_ERR_INVALID_ARG", 2: "FC_ERR_UNSUPPORTED",
                 3: "FC_ERR_ALIGNMENT", 4: "FC_ERR_WORKSPACE", 5: "FC_ERR_CUDA",
                 6: "FC_ERR_TIMEOUT", 7: "FC_ERR_RANGE"}
 EPI = {"relu": 1, "hardswish": 2, "leaky_relu": 3, "add_channel": 4, "clamp": 5,
-       "gelu_erf": 6, "maxpool2x2": 7, "hardtanh": 8, "mean_hw": 9, "tanh": 10}
+       "gelu_erf": 6, "maxpool2x2": 7, "hardtanh": 8, "mean_hw": 9, "tanh": 10,
+       "maxpool": 11}
 VARIANTS = {"auto": 0, "ffma": 1, "tc_tf32x3": 2, "tc_f16x3": 3}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 MAX_OPS = 8
@@ -146,7 +147,7 @@ def make_epilogue(bias, ops):
         e.ops[i].kind = EPI[name]
         if name == "leaky_relu":
             e.ops[i].a = float(op[1])
-        elif name in ("clamp", "hardtanh"):
+        elif name in ("clamp", "hardtanh", "maxpool"):
             e.ops[i].a, e.ops[i].b = float(op[1]), float(op[2])
         elif name == "add_channel":
             t = op[1]
@@ -297,15 +298,17 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
     return y
 
 
-def pool_mean_ops(lo=-1.0, hi=1.0):
-    return (("maxpool2x2",), ("hardtanh", lo, hi), ("mean_hw",), ("tanh",))
+def pool_mean_ops(lo=-1.0, hi=1.0, pool=(2, 2)):
+    """The pooled entry's chain; pool = (window, stride) of the max pool."""
+    mp = ("maxpool2x2",) if tuple(pool) == (2, 2) else ("maxpool", float(pool[0]), float(pool[1]))
+    return (mp, ("hardtanh", lo, hi), ("mean_hw",), ("tanh",))
 
 
 def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
-                         ws=None, stream=None, stride=1, out_pad=0):
+                         ws=None, stream=None, stride=1, out_pad=0, pool=(2, 2)):
     """ConvTranspose2d(k=3, stride 1 or 2, p=1, out_pad) + bias -> maxpool
-    2x2 -> hardtanh -> mean(H,W) -> tanh.  w: [C_in, C_out, 3, 3]; returns
-    y [N, C_out, 1, 1]."""
+    (window, stride) = pool -> hardtanh -> mean(H,W) -> tanh.
+    w: [C_in, C_out, 3, 3]; returns y [N, C_out, 1, 1]."""
     import torch
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
@@ -317,8 +320,12 @@ def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
         y = torch.empty((N, CO, 1, 1), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
     if ws is None:
-        ws = _workspace(workspace_bytes(2, (N, C, H, W, CO, K, pad)), x.device)
-    e, keep = make_epilogue(bias, pool_mean_ops(*hardtanh))
+        if tuple(pool) == (2, 2):
+            nb = workspace_bytes(2, (N, C, H, W, CO, K, pad))
+        else:
+            nb = workspace_bytes(3, (N, C, H, W, CO, K, pad, stride, out_pad, pool[0], pool[1]))
+        ws = _workspace(nb, x.device)
+    e, keep = make_epilogue(bias, pool_mean_ops(*hardtanh, pool=pool))
     st = lib().fc_convT2d_pool_mean(_ptr(x), N, C, H, W, _ptr(w), CO, K, int(stride), pad,
                                     int(out_pad),
                                     ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),

@@ -98,14 +98,27 @@ fc_status decode_eltwise(const fc_epilogue *epi, EpiDev *e, int *chain) {
 }
 
 // The pooled entry point accepts exactly MAXPOOL2X2, HARDTANH, MEAN_HW, TANH.
-fc_status decode_pool(const fc_epilogue *epi, EpiDev *e, float *lo, float *hi) {
+fc_status decode_pool(const fc_epilogue *epi, EpiDev *e, float *lo, float *hi, int *pk,
+                      int *ps) {
   memset(e, 0, sizeof(*e));
   if (!epi) return FC_ERR_INVALID_ARG;
   if (epi->bias && !aligned16(epi->bias)) return FC_ERR_ALIGNMENT;
   if (epi->n_ops != 4) return FC_ERR_UNSUPPORTED;
   const int want[4] = {FC_EPI_MAXPOOL2X2, FC_EPI_HARDTANH, FC_EPI_MEAN_HW, FC_EPI_TANH};
-  for (int i = 0; i < 4; ++i)
+  for (int i = 1; i < 4; ++i)
     if (epi->ops[i].kind != want[i]) return FC_ERR_UNSUPPORTED;
+  if (epi->ops[0].kind == FC_EPI_MAXPOOL2X2) {
+    *pk = *ps = 2;
+  } else if (epi->ops[0].kind == FC_EPI_MAXPOOL) {
+    const float a = epi->ops[0].a, b = epi->ops[0].b;
+    if (!(a >= 1.0f && a <= 4.0f && b >= 1.0f && b <= 4.0f) || a != (float)(int)a ||
+        b != (float)(int)b)
+      return FC_ERR_UNSUPPORTED;  // window and stride: integers 1 .. 4
+    *pk = (int)a;
+    *ps = (int)b;
+  } else {
+    return FC_ERR_UNSUPPORTED;
+  }
   if (!(epi->ops[1].a <= epi->ops[1].b)) return FC_ERR_INVALID_ARG;
   e->bias = epi->bias;
   *lo = epi->ops[1].a;
@@ -120,6 +133,7 @@ bool fits_int32(long long v) { return v >= 0 && v < (1LL << 31); }
 // there is enough work; tiny problems go to whichever finished first.
 int auto_variant(const ConvProblem &p) {
   if (p.subpix) return tc_supported(p, 1) ? FC_VARIANT_TC_F16X3 : FC_VARIANT_TC_TF32X3;
+  if (p.pool && (p.pk != 2 || p.ps != 2)) return FC_VARIANT_FFMA;  // general pool windows
   const double macs = (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
   if (tc_supported(p, 1) && macs >= 4.0e8) return FC_VARIANT_TC_F16X3;
   if (tc_supported(p, 0) && macs >= 4.0e8) return FC_VARIANT_TC_TF32X3;
@@ -348,8 +362,13 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
     return FC_ERR_UNSUPPORTED;
   ConvProblem p{};
   float lo = 0.f, hi = 0.f;
-  fc_status s = decode_pool(epi, &p.epi, &lo, &hi);
+  int pk = 2, ps = 2;
+  fc_status s = decode_pool(epi, &p.epi, &lo, &hi, &pk, &ps);
   if (s != FC_OK) return s;
+  if ((pk != 2 || ps != 2) && stride != 1) return FC_ERR_UNSUPPORTED;
+  if (Ho < pk || Wo < pk) return FC_ERR_INVALID_ARG;  // no full pooling window
+  p.pk = pk;
+  p.ps = ps;
   if (N == 0) return FC_OK;
   if (!x || !w || !y) return FC_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
@@ -418,7 +437,15 @@ size_t fc_workspace_bytes(int entry, const int *d) {
       p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
       p.KD = 1; p.KH = p.KW = d[5]; p.pad = p.KH - 1 - d[6];
       p.Do = 1; p.Ho = p.H - 1 - 2 * d[6] + p.KH; p.Wo = p.W - 1 - 2 * d[6] + p.KW;
-      p.pool = 1; p.wlayout = 1;
+      p.pool = 1; p.wlayout = 1; p.pk = p.ps = 2;
+      break;
+    case 3:  // {N, C_in, H, W, C_out, k, pad, stride 1, out_pad 0, pool k, pool s}
+      if (d[7] != 1 || d[8] != 0 || d[9] < 1 || d[10] < 1) return 0;
+      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
+      p.KD = 1; p.KH = p.KW = d[5]; p.pad = p.KH - 1 - d[6];
+      p.Do = 1; p.Ho = p.H - 1 - 2 * d[6] + p.KH; p.Wo = p.W - 1 - 2 * d[6] + p.KW;
+      p.pool = 1; p.wlayout = 1; p.pk = d[9]; p.ps = d[10];
+      if (p.Ho < p.pk || p.Wo < p.pk) return 0;
       break;
     default:
       return 0;

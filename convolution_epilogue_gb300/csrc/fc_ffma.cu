@@ -220,6 +220,153 @@ ffma_conv_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
 // in index order, the t of quarter q, and the four quarter sums are added in
 // the order 0, 1, 2, 3.  A fixed order, so the result does not depend on
 // scheduling.
+// General max-pool (window K, stride ps <= 4, floor extent) fused after a
+// stride-1 3x3 conv (a transposed conv arrives rewritten as one): the
+// general path of the Kimi-K2.6__l2_p10 trace's tail-kernel and max-pool
+// paragraphs, computed without writing the conv output.  A block owns a
+// 4 x 8 tile of pooled outputs and 64 output channels; thread (gr, gc)
+// computes the K x K conv outputs of its window (conv rows
+// (pi0 + gr) ps + a, columns (pj0 + gc) ps + b) for 8 channels from the
+// staged input halo, takes their max, adds the bias, clamps, and the warp
+// adds its 32 windows in a fixed butterfly order into one partial per
+// (image, tile, channel).  Overlapping windows (K > ps) recompute the
+// shared conv outputs.
+constexpr int kPoolTH = 4, kPoolTW = 8;
+
+template <int K>
+__global__ void __launch_bounds__(256)
+ffma_pool_general_kernel(ConvProblem p, const float *__restrict__ wp, int Cp, int COp,
+                         float *__restrict__ partial, int n_th, int n_tw, int Hp, int Wp) {
+  constexpr int TAPS = 9;
+  constexpr int SHM = (kPoolTH - 1) * 4 + K + 2, SWM = (kPoolTW - 1) * 4 + K + 2;
+  extern __shared__ __align__(16) float smem_g[];
+  float (*s_w)[TAPS][kCoT] = reinterpret_cast<float (*)[TAPS][kCoT]>(smem_g);
+  float (*s_in)[SHM][SWM] = reinterpret_cast<float (*)[SHM][SWM]>(smem_g + kCiT * TAPS * kCoT);
+  const int ps = p.ps;
+  const int SH = (kPoolTH - 1) * ps + K + 2, SW = (kPoolTW - 1) * ps + K + 2;
+
+  const int tid = threadIdx.x;
+  const int cg = tid >> 5, pg = tid & 31;
+  const int gr = pg >> 3, gc = pg & 7;
+  long b = blockIdx.x;
+  const int tw = (int)(b % n_tw); b /= n_tw;
+  const int th = (int)(b % n_th); b /= n_th;
+  const int n = (int)(b % p.N); b /= p.N;
+  const int cb = (int)b;
+  const int pi0 = th * kPoolTH, pj0 = tw * kPoolTW;
+  const int r0 = pi0 * ps, c0 = pj0 * ps;  // first conv row / column of the tile
+  const int HW = p.H * p.W;
+  const long x_n = (long)n * p.C * HW;
+
+  float acc[K][K][8];
+#pragma unroll
+  for (int a = 0; a < K; ++a)
+#pragma unroll
+    for (int c = 0; c < K; ++c)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[a][c][j] = 0.0f;
+
+  for (int ci0 = 0; ci0 < Cp; ci0 += kCiT) {
+    __syncthreads();
+    const int nin = kCiT * SH * SW;
+    for (int i = tid; i < nin; i += 256) {
+      const int c = i % SW, r = (i / SW) % SH, ci = i / (SW * SH);
+      const int gci = ci0 + ci;
+      const int ih = r0 + r - p.pad, iw = c0 + c - p.pad;
+      float v = 0.0f;
+      if (gci < p.C && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
+        v = __ldg(p.x + x_n + (long)gci * HW + (long)ih * p.W + iw);
+      s_in[ci][r][c] = v;
+    }
+    constexpr int NW4 = kCiT * TAPS * (kCoT / 4);
+    for (int i = tid; i < NW4; i += 256) {
+      const int c4 = i % (kCoT / 4), t = (i / (kCoT / 4)) % TAPS, ci = i / (TAPS * (kCoT / 4));
+      const float4 *src = reinterpret_cast<const float4 *>(
+          wp + ((long)(ci0 + ci) * TAPS + t) * COp + cb * kCoT);
+      reinterpret_cast<float4 *>(&s_w[ci][t][0])[c4] = __ldg(src + c4);
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int ci = 0; ci < kCiT; ++ci) {
+#pragma unroll
+      for (int kh = 0; kh < 3; ++kh) {
+        float4 wv[3][2];
+#pragma unroll
+        for (int kw = 0; kw < 3; ++kw) {
+          const float4 *ws4 = reinterpret_cast<const float4 *>(&s_w[ci][kh * 3 + kw][cg * 8]);
+          wv[kw][0] = ws4[0];
+          wv[kw][1] = ws4[1];
+        }
+#pragma unroll
+        for (int a = 0; a < K; ++a) {
+          float xin[K + 2];
+#pragma unroll
+          for (int q = 0; q < K + 2; ++q) xin[q] = s_in[ci][gr * ps + a + kh][gc * ps + q];
+#pragma unroll
+          for (int kw = 0; kw < 3; ++kw)
+#pragma unroll
+            for (int c = 0; c < K; ++c) {
+              const float xv = xin[c + kw];
+              acc[a][c][0] = fmaf(xv, wv[kw][0].x, acc[a][c][0]);
+              acc[a][c][1] = fmaf(xv, wv[kw][0].y, acc[a][c][1]);
+              acc[a][c][2] = fmaf(xv, wv[kw][0].z, acc[a][c][2]);
+              acc[a][c][3] = fmaf(xv, wv[kw][0].w, acc[a][c][3]);
+              acc[a][c][4] = fmaf(xv, wv[kw][1].x, acc[a][c][4]);
+              acc[a][c][5] = fmaf(xv, wv[kw][1].y, acc[a][c][5]);
+              acc[a][c][6] = fmaf(xv, wv[kw][1].z, acc[a][c][6]);
+              acc[a][c][7] = fmaf(xv, wv[kw][1].w, acc[a][c][7]);
+            }
+        }
+      }
+    }
+  }
+
+  const int co0 = cb * kCoT + cg * 8;
+  const bool valid = (pi0 + gr < Hp) && (pj0 + gc < Wp);
+  float part[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int co = co0 + j;
+    const float bias = (co < p.CO && p.epi.bias) ? __ldg(p.epi.bias + co) : 0.0f;
+    float m = acc[0][0][j];
+#pragma unroll
+    for (int a = 0; a < K; ++a)
+#pragma unroll
+      for (int c = 0; c < K; ++c) m = fmaxf(m, acc[a][c][j]);
+    m = fminf(fmaxf(m + bias, p.ht_lo), p.ht_hi);
+    part[j] = valid ? m : 0.0f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[j] += __shfl_xor_sync(0xffffffffu, part[j], off);
+  if (pg == 0) {
+    const int T = n_th * n_tw;
+    float *dst = partial + ((long)n * T + th * n_tw + tw) * p.CO;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (co0 + j < p.CO) dst[co0 + j] = part[j];
+  }
+}
+
+template <int K>
+cudaError_t launch_pool_general(const ConvProblem &p, const float *wp, int Cp, int COp,
+                                float *partial, int n_th, int n_tw, int Hp, int Wp,
+                                cudaStream_t s) {
+  constexpr int SHM = (kPoolTH - 1) * 4 + K + 2, SWM = (kPoolTW - 1) * 4 + K + 2;
+  constexpr size_t smem = sizeof(float) * (kCiT * 9 * kCoT + kCiT * SHM * SWM);
+  const long blocks = (long)(COp / kCoT) * p.N * n_th * n_tw;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+  auto kern = ffma_pool_general_kernel<K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_begin(s);
+  kern<<<(unsigned)blocks, 256, smem, s>>>(p, wp, Cp, COp, partial, n_th, n_tw, Hp, Wp);
+  prof_end(s, p.entry);
+  return cudaGetLastError();
+}
+
 constexpr int kFinishQ = 4;
 constexpr int kFinishThreads = 64 * kFinishQ;
 
@@ -298,13 +445,19 @@ cudaError_t launch_eltwise_kd(const ConvProblem &p, const float *wp, int Cp, int
 
 }  // namespace
 
+// Pooled extents (floor): (Ho - pk) / ps + 1.
+static int pooled_h(const ConvProblem &p) { return (p.Ho - p.pk) / p.ps + 1; }
+static int pooled_w(const ConvProblem &p) { return (p.Wo - p.pk) / p.ps + 1; }
+static bool pool_general(const ConvProblem &p) { return p.pk != 2 || p.ps != 2; }
+
 int ffma_pool_tiles_per_image(const ConvProblem &p) {
+  if (pool_general(p)) return ceil_div(pooled_h(p), kPoolTH) * ceil_div(pooled_w(p), kPoolTW);
   return ceil_div(p.Ho, 8) * ceil_div(p.Wo, 16);
 }
 
 cudaError_t pool_finish_launch(const ConvProblem &p, const float *partials,
                                int tiles_per_image, cudaStream_t s) {
-  int count = (p.Ho / 2) * (p.Wo / 2);
+  int count = pooled_h(p) * pooled_w(p);
   pool_finish_kernel<<<p.N, kFinishThreads, 0, s>>>(partials, p.N, p.CO, tiles_per_image,
                                                     1.0 / (double)count, p.y);
   return cudaGetLastError();
@@ -324,6 +477,21 @@ cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *launches = 1;
+  if (p.pool && pool_general(p)) {
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
+    const int Hp = pooled_h(p), Wp = pooled_w(p);
+    const int n_th = ceil_div(Hp, kPoolTH), n_tw = ceil_div(Wp, kPoolTW);
+    switch (p.pk) {
+      case 1: e = launch_pool_general<1>(p, wp, Cp, COp, partial, n_th, n_tw, Hp, Wp, s); break;
+      case 2: e = launch_pool_general<2>(p, wp, Cp, COp, partial, n_th, n_tw, Hp, Wp, s); break;
+      case 3: e = launch_pool_general<3>(p, wp, Cp, COp, partial, n_th, n_tw, Hp, Wp, s); break;
+      default: e = launch_pool_general<4>(p, wp, Cp, COp, partial, n_th, n_tw, Hp, Wp, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    e = pool_finish_launch(p, partial, n_th * n_tw, s);
+    *launches += 2;
+    return e;
+  }
   if (p.pool) {
     float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
     e = launch_one<1, 2, 2, true, CHAIN_NONE>(p, wp, Cp, COp, partial, s);

@@ -47,6 +47,7 @@ struct ConvProblem {
   // class on the input grid (x, w in transposed-conv form, no rewrite);
   // Ho, Wo are then the transposed conv's output extents.
   int subpix;
+  int pk, ps;      // pooled entry: max-pool window and stride (floor extent)
   float ht_lo, ht_hi;
   int chain;       // ChainId
   int entry;       // 0 conv2d, 1 conv3d, 2 convT-pool-mean (for profiling)

@@ -208,6 +208,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
   if (p.pool && U != 2) return q;
   if (p.pool && p.KD != 1) return q;
+  if (p.pool && (p.pk != 2 || p.ps != 2)) return q;  // 2x2 / 2 pool only
   plan_chunks(p, prec, q);
   q.S2 = p.stride == 2;
   q.DIL = p.dil;
@@ -312,6 +313,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
 TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
   TcPlan q{};
   if (!p.pool || p.KH != 3 || p.KW != 3 || p.KD != 1 || p.wlayout != 1) return q;
+  if (p.pk != 2 || p.ps != 2) return q;
   plan_chunks(p, prec, q);
   q.SP = 1;
   q.DIL = 1;

@@ -77,7 +77,9 @@ typedef enum {
   FC_EPI_MAXPOOL2X2 = 7,  /* 2x2 window, stride 2, floor extent */
   FC_EPI_HARDTANH = 8,    /* min(max(x, a), b) */
   FC_EPI_MEAN_HW = 9,     /* mean over the (pooled) H x W plane */
-  FC_EPI_TANH = 10        /* tanh(x) */
+  FC_EPI_TANH = 10,       /* tanh(x) */
+  FC_EPI_MAXPOOL = 11     /* window a x a, stride b (integers 1 .. 4), floor extent
+                             (H - a) / b + 1; pooled entry only */
 } fc_epi_kind;
 
 typedef struct {
@@ -162,10 +164,15 @@ FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, in
                         int stride, int pad, int dilation, const fc_epilogue *epi,
                         float *y, void *ws, size_t ws_bytes, void *stream);
 
-/* ConvTranspose2d + bias -> MaxPool2d(2,2) -> Hardtanh[a,b] -> mean(H,W)
+/* ConvTranspose2d + bias -> MaxPool2d -> Hardtanh[a,b] -> mean(H,W)
  * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];
  * y [N][C_out][1][1].  The epilogue chain must be exactly
- * MAXPOOL2X2, HARDTANH(a, b), MEAN_HW, TANH.  Supported: k = 3, pad 1 and
+ * MAXPOOL2X2 (or MAXPOOL(k_p, s_p)), HARDTANH(a, b), MEAN_HW, TANH.  A
+ * general window (k_p, s_p) other than 2 / 2 -- overlapping or not, floor
+ * extent, the general max-pool of trace "Kimi-K2.6__l2_p10" -- runs at
+ * stride 1 on the CUDA-core variant only (the tensor-core variants return
+ * FC_ERR_UNSUPPORTED; AUTO picks FFMA), the conv output never leaving the
+ * kernel.  Supported: k = 3, pad 1 and
  *   stride 1, out_pad 0: conv output extent Ho = H, Wo = W (H, W >= 2);
  *   stride 2, out_pad 0 or 1: Ho = 2H - 1 + out_pad (likewise Wo; the
  *   output-size formula (H-1)s - 2p + k + op of trace "Kimi-K2.6__l2_p10"),
@@ -182,10 +189,13 @@ FC_API fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, in
 
 /* Workspace bytes needed by one call.  entry: 0 = fc_conv2d_epi,
  * 1 = fc_conv3d_epi, 2 = fc_convT2d_pool_mean (any supported stride and
- * out_pad).  dims:
+ * out_pad, 2x2 pool), 3 = fc_convT2d_pool_mean with a general pool window.
+ * dims:
  *   entry 0: {N, C_in, H, W, C_out, k, pad}
  *   entry 1: {N, C_in, D, H, W, C_out, k, pad}
  *   entry 2: {N, C_in, H, W, C_out, k, pad}
+ *   entry 3: {N, C_in, H, W, C_out, k, pad, stride (1), out_pad (0),
+ *             pool window, pool stride}
  * The size covers every variant, so it does not depend on the selection.
  * Returns 0 for an invalid entry or NULL dims. */
 FC_API size_t fc_workspace_bytes(int entry, const int *dims);

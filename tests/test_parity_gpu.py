@@ -554,3 +554,47 @@ def test_convT_stride2_full_size_sampled(variant):
     ref = oracle.convT_pool_mean_points(x, inp["w"], inp["b"], pairs, stride=2, pad=1, out_pad=1)
     got = np.array([ynp[n, c] for n, c in pairs])
     _check(got, ref, f"convT stride 2 sampled [{variant}]")
+
+
+# ------------------------------------------- general max-pool windows (fused)
+@pytest.mark.parametrize("variant", ["auto", "ffma"])
+@pytest.mark.parametrize("shape,pool", [
+    ((2, 16, 17, 21, 64), (3, 2)),   # overlapping windows, odd extents
+    ((1, 8, 12, 40, 70), (2, 1)),    # stride 1: every conv output in 4 windows
+    ((2, 64, 13, 14, 64), (3, 3)),   # non-overlapping 3x3
+    ((1, 5, 9, 35, 64), (4, 2)),     # 4x4 windows, C_in not a multiple of 8
+    ((1, 8, 6, 7, 64), (1, 1)),      # window 1: plain mean of the clamped conv
+])
+def test_convT_general_pool_mean(variant, shape, pool):
+    """Transposed conv (stride 1, pad 1) + max pool of any window / stride
+    (floor extent) + hardtanh + mean + tanh in one pass, against the oracle."""
+    N, C, H, W, CO = shape
+    st = synth.seeded(780 + pool[0] * 4 + pool[1])
+    x = st.normal((N, C, H, W))
+    w = st.uniform((C, CO, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((CO,), 0.1)
+    ht = (-0.6, 0.9)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), hardtanh=ht, pool=pool)
+        assert m.last_variant() == "ffma"
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    ref = oracle.convT_pool_mean(x, w, b, pool=pool, hardtanh=ht)
+    _check(got, ref, f"{variant} general pool {pool} {shape}")
+
+
+def test_general_pool_refused_by_tensor_core_variants():
+    m = fc()
+    x = _dev(np.zeros((1, 8, 8, 8), np.float32))
+    w = _dev(np.zeros((8, 64, 3, 3), np.float32))
+    for v in ("tc_tf32x3", "tc_f16x3"):
+        m.set_variant(v)
+        try:
+            with pytest.raises(m.FcError):
+                m.fc_convT2d_pool_mean(x, w, None, pool=(3, 2))
+        finally:
+            m.set_variant("auto")
