@@ -428,6 +428,8 @@ def run_ours(args):
                 fc, d[3], flush, stream, peaks, stride=1, pad=2, dilation=2),
             "convT2d_stride2_outpad1_pool_mean_128x64x128x128": widened_convT_s2(
                 fc, d[5], flush, stream, peaks),
+            "convT2d_maxpool3s2_mean_16x64x256x256": widened_general_pool(
+                fc, d[5], flush, stream, peaks),
         }
 
     # end to end through the public API with host buffers
@@ -568,6 +570,41 @@ def widened_convT_s2(fc, d5, flush, stream, peaks, reps=20):
     pk, _, basis = pipe_peak_tflops(variant, peaks)
     t_roof = max(flops / (pk * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
     del x
+    return {"variant": variant, "ms_median": ms, "gflops": flops / (ms * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms, "peak_basis": basis}
+
+
+def widened_general_pool(fc, d5, flush, stream, peaks, reps=10):
+    """Transposed conv (stride 1) on 16 images of the pooled workload's input
+    [16,64,256,256] -> 3x3 max pool, stride 2 (overlapping, floor extent
+    127 x 127) -> hardtanh -> mean -> tanh, fused on the CUDA-core kernel.
+    Useful FLOPs = 2 x conv MACs (each conv output counted once; the kernel
+    recomputes the outputs shared by overlapping windows, 2.25x here)."""
+    import torch
+    x = d5["x"][:16]
+    w, b = d5["w"], d5["b"]
+    N, C, H, W = x.shape
+    CO = w.shape[1]
+    y = torch.empty((N, CO, 1, 1), dtype=torch.float32, device=x.device)
+    call = lambda: fc.fc_convT2d_pool_mean(x, w, b, y=y, pool=(3, 2))
+    call()
+    variant = fc.last_variant()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if fc.get_last_device_error() != 0:
+        raise RuntimeError("device status word set in the general-pool entry")
+    ms = statistics.median(ts)
+    flops = 2.0 * N * C * CO * H * W * 9
+    nbytes = 4.0 * (x.numel() + w.numel() + b.numel() + y.numel())
+    pk, _, basis = pipe_peak_tflops(variant, peaks)
+    t_roof = max(flops / (pk * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9))
     return {"variant": variant, "ms_median": ms, "gflops": flops / (ms * 1e-3) / 1e9,
             "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms, "peak_basis": basis}
 
