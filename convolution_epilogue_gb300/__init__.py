@@ -32,6 +32,7 @@ MAX_OPS = 8
 
 # every symbol include/fusedconv.h declares
 EXPORTS = ("fc_conv2d_epi", "fc_conv2d_epi_noalloc", "fc_conv3d_epi", "fc_convT2d_pool_mean",
+           "fc_conv2d_epi_nhwc", "fc_conv3d_epi_ndhwc",
            "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
@@ -72,6 +73,11 @@ def lib():
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.fc_conv2d_epi.restype = I
             L.fc_conv2d_epi.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P, S, P]
+            L.fc_conv2d_epi_nhwc.restype = I
+            L.fc_conv2d_epi_nhwc.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P, S, P]
+            L.fc_conv3d_epi_ndhwc.restype = I
+            L.fc_conv3d_epi_ndhwc.argtypes = [P, I, I, I, I, I, P, I, I, I, I, I, I, I, P,
+                                              P, P, S, P]
             L.fc_conv2d_epi_noalloc.restype = I
             L.fc_conv2d_epi_noalloc.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P]
             L.fc_conv3d_epi.restype = I
@@ -294,6 +300,57 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
                              pad, int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
                              ws.numel(), _stream_handle(stream))
     _check(st, "fc_conv3d_epi")
+    del keep
+    return y
+
+
+def fc_conv2d_epi_nhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1,
+                       dilation=1):
+    """Channels-last conv2d: x [N,H,W,C_in], w [C_out,C_in,3,3] -> y [N,Ho,Wo,C_out]."""
+    import torch
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    N, H, W, C = x.shape
+    CO, C2, KH, KW = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    Ho, Wo = _extent(H, KH, stride, pad, dilation), _extent(W, KW, stride, pad, dilation)
+    if y is None:
+        y = torch.empty((N, Ho, Wo, CO), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    if ws is None:
+        ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
+    e, keep = make_epilogue(bias, ops)
+    st = lib().fc_conv2d_epi_nhwc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, int(stride), pad,
+                                  int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                                  _stream_handle(stream))
+    _check(st, "fc_conv2d_epi_nhwc")
+    del keep
+    return y
+
+
+def fc_conv3d_epi_ndhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, stride=1,
+                        dilation=1):
+    """Channels-last conv3d: x [N,D,H,W,C_in], w [C_out,C_in,3,3,3] -> y [N,Do,Ho,Wo,C_out]."""
+    import torch
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
+    N, D, H, W, C = x.shape
+    CO, C2, KD, KH, KW = w.shape
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    Do, Ho, Wo = (_extent(D, KD, stride, pad, dilation), _extent(H, KH, stride, pad, dilation),
+                  _extent(W, KW, stride, pad, dilation))
+    if y is None:
+        y = torch.empty((N, Do, Ho, Wo, CO), dtype=torch.float32, device=x.device)
+    _require_cuda_f32("y", y)
+    if ws is None:
+        ws = _workspace(workspace_bytes(1, (N, C, D, H, W, CO, KD, pad)), x.device)
+    e, keep = make_epilogue(bias, ops)
+    st = lib().fc_conv3d_epi_ndhwc(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, int(stride),
+                                   pad, int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
+                                   ws.numel(), _stream_handle(stream))
+    _check(st, "fc_conv3d_epi_ndhwc")
     del keep
     return y
 

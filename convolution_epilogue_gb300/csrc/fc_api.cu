@@ -132,7 +132,7 @@ bool fits_int32(long long v) { return v >= 0 && v < (1LL << 31); }
 // benchmark's per-variant table): the tensor-core f16-split path wins once
 // there is enough work; tiny problems go to whichever finished first.
 int auto_variant(const ConvProblem &p) {
-  if (p.subpix) return tc_supported(p, 1) ? FC_VARIANT_TC_F16X3 : FC_VARIANT_TC_TF32X3;
+  if (p.subpix || p.cl) return tc_supported(p, 1) ? FC_VARIANT_TC_F16X3 : FC_VARIANT_TC_TF32X3;
   if (p.pool && (p.pk != 2 || p.ps != 2)) return FC_VARIANT_FFMA;  // general pool windows
   const double macs = (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
   if (tc_supported(p, 1) && macs >= 4.0e8) return FC_VARIANT_TC_F16X3;
@@ -152,7 +152,7 @@ fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
   int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : auto_variant(p);
   if ((v == FC_VARIANT_TC_TF32X3 && !tc_supported(p, 0)) ||
       (v == FC_VARIANT_TC_F16X3 && !tc_supported(p, 1)) ||
-      (v == FC_VARIANT_FFMA && p.subpix))  // the CUDA-core kernel has no parity-class form
+      (v == FC_VARIANT_FFMA && (p.subpix || p.cl)))  // no parity-class or channels-last form
     return FC_ERR_UNSUPPORTED;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int launches = 0;
@@ -270,10 +270,10 @@ fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
                        scratch, kNoAllocScratchBytes, stream);
 }
 
-fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
-                        const float *w, int C_out, int kH, int kW, int stride,
-                        int pad, int dilation, const fc_epilogue *epi, float *y, void *ws,
-                        size_t ws_bytes, void *stream) {
+static fc_status conv2d_impl(const float *x, int N, int C_in, int H, int W, const float *w,
+                             int C_out, int kH, int kW, int stride, int pad, int dilation,
+                             const fc_epilogue *epi, float *y, void *ws, size_t ws_bytes,
+                             void *stream, int cl) {
   if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || kH < 1 || kW < 1 ||
       stride < 1 || pad < 0 || dilation < 1)
     return FC_ERR_INVALID_ARG;
@@ -299,16 +299,32 @@ fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
   p.pad_d = 0; p.pad = pad;
   p.stride = stride;
   p.dil = dilation;
+  p.cl = cl;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 0;
   return run(p, ws, ws_bytes, stream);
 }
 
-fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
-                        const float *w, int C_out, int kD, int kH, int kW,
-                        int stride, int pad, int dilation, const fc_epilogue *epi,
+fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W, const float *w, int C_out,
+                        int kH, int kW, int stride, int pad, int dilation, const fc_epilogue *epi,
                         float *y, void *ws, size_t ws_bytes, void *stream) {
+  return conv2d_impl(x, N, C_in, H, W, w, C_out, kH, kW, stride, pad, dilation, epi, y, ws,
+                     ws_bytes, stream, 0);
+}
+
+fc_status fc_conv2d_epi_nhwc(const float *x, int N, int C_in, int H, int W, const float *w,
+                             int C_out, int kH, int kW, int stride, int pad, int dilation,
+                             const fc_epilogue *epi, float *y, void *ws, size_t ws_bytes,
+                             void *stream) {
+  return conv2d_impl(x, N, C_in, H, W, w, C_out, kH, kW, stride, pad, dilation, epi, y, ws,
+                     ws_bytes, stream, 1);
+}
+
+static fc_status conv3d_impl(const float *x, int N, int C_in, int D, int H, int W,
+                             const float *w, int C_out, int kD, int kH, int kW, int stride,
+                             int pad, int dilation, const fc_epilogue *epi, float *y, void *ws,
+                             size_t ws_bytes, void *stream, int cl) {
   if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 ||
       kH < 1 || kW < 1 || stride < 1 || pad < 0 || dilation < 1)
     return FC_ERR_INVALID_ARG;
@@ -336,10 +352,27 @@ fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
   p.pad_d = pad; p.pad = pad;
   p.stride = stride;
   p.dil = dilation;
+  p.cl = cl;
   p.Do = Do; p.Ho = Ho; p.Wo = Wo;
   p.wlayout = 0;
   p.entry = 1;
   return run(p, ws, ws_bytes, stream);
+}
+
+fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W, const float *w,
+                        int C_out, int kD, int kH, int kW, int stride, int pad, int dilation,
+                        const fc_epilogue *epi, float *y, void *ws, size_t ws_bytes,
+                        void *stream) {
+  return conv3d_impl(x, N, C_in, D, H, W, w, C_out, kD, kH, kW, stride, pad, dilation, epi, y,
+                     ws, ws_bytes, stream, 0);
+}
+
+fc_status fc_conv3d_epi_ndhwc(const float *x, int N, int C_in, int D, int H, int W,
+                              const float *w, int C_out, int kD, int kH, int kW, int stride,
+                              int pad, int dilation, const fc_epilogue *epi, float *y, void *ws,
+                              size_t ws_bytes, void *stream) {
+  return conv3d_impl(x, N, C_in, D, H, W, w, C_out, kD, kH, kW, stride, pad, dilation, epi, y,
+                     ws, ws_bytes, stream, 1);
 }
 
 fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,

@@ -48,6 +48,7 @@ struct ConvProblem {
   // Ho, Wo are then the transposed conv's output extents.
   int subpix;
   int pk, ps;      // pooled entry: max-pool window and stride (floor extent)
+  int cl;          // 1: x is N(D)HWC and y is N(Do)(Ho)(Wo)C_out (channels last)
   float ht_lo, ht_hi;
   int chain;       // ChainId
   int entry;       // 0 conv2d, 1 conv3d, 2 convT-pool-mean (for profiling)

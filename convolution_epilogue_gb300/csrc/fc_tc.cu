@@ -206,6 +206,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   TcPlan q{};
   if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
   if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
+  if (p.cl && (p.pool || p.stride != 1)) return q;  // channels-last: stride 1, no pool
   if (p.pool && U != 2) return q;
   if (p.pool && p.KD != 1) return q;
   if (p.pool && (p.pk != 2 || p.ps != 2)) return q;  // 2x2 / 2 pool only
@@ -633,7 +634,8 @@ struct StageSrc {
 // the RIN loaded per depth.  Its staged pixels start at jb.dst; the input
 // column cc lands at staged column col_px(cc) of that row.
 __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, const TcPlan &q,
-                                                   const ConvProblem &p, int nrows, int E, bool s2) {
+                                                   const ConvProblem &p, int nrows, int E, bool s2,
+                                                   bool cl = false) {
   RowJob jb;
   // a stage holds at most 2 slice planes of at most 3 depth slices
   const int plane = job >= nrows ? 1 : 0;
@@ -642,7 +644,8 @@ __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, 
   const int r = sr - kdp * q.RIN;
   const int id = ss.id0 + kdp * q.DIL, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
-  jb.rowbase = ss.xn + ((long)id * p.H + ih) * p.W + ss.iw0;
+  // channels-last input: pixels C floats apart, channels adjacent
+  jb.rowbase = ss.xn + (((long)id * p.H + ih) * p.W + ss.iw0) * (cl ? p.C : 1);
   jb.cbase = ss.ci0 + plane * E;
   // stride 2: even / odd rows go to sub-plane row r >> 1 of their parity
   const int row_px = s2 ? 2 * (r & 1) * q.SUB + (r >> 1) * q.RS : r * q.RS;
@@ -657,14 +660,32 @@ __host__ __device__ __forceinline__ int col_px(int cc, int s2sub) {
 }
 
 // Loads E channels of staged pixel cc of a row (zero outside the image).
-template <int E>
+// Channels-first input: one load per channel plane (cstride apart).
+// Channels-last (CL): the E channels are adjacent, read as float4 vectors
+// when C is a multiple of 4 (then every slice starts 16-byte aligned).
+template <int E, bool CL = false>
 __device__ __forceinline__ void load_pixel(const float *__restrict__ x, const RowJob &jb, int cc,
                                            long cstride, int iw0, int W, int C, float (&v)[E]) {
   const bool colok = jb.ok && iw0 + cc >= 0 && iw0 + cc < W;
+  if constexpr (CL) {
+    const float *px = x + jb.rowbase + (long)cc * C + jb.cbase;
+    if ((C & 3) == 0 && jb.cbase + E <= C) {
 #pragma unroll
-  for (int e = 0; e < E; ++e)
-    v[e] = (colok && jb.cbase + e < C) ? __ldg(x + jb.rowbase + cc + (long)(jb.cbase + e) * cstride)
-                                        : 0.0f;
+      for (int e = 0; e < E; e += 4) {
+        const float4 f = colok ? __ldg(reinterpret_cast<const float4 *>(px + e))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[e] = f.x; v[e + 1] = f.y; v[e + 2] = f.z; v[e + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = (colok && jb.cbase + e < C) ? __ldg(px + e) : 0.0f;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      v[e] = (colok && jb.cbase + e < C) ? __ldg(x + jb.rowbase + cc + (long)(jb.cbase + e) * cstride)
+                                          : 0.0f;
+  }
 }
 
 // A loaded row of LW pixels has G = LW / 32 full 32-pixel groups, taken by
@@ -684,14 +705,15 @@ __host__ __device__ __forceinline__ MainJob main_job(int J, int parts, int G) {
 // Main job: pixels cc = c0 + lane + 32k (k < NCOL) of one row, all loads in
 // flight before the first store.  `wait_stage` runs between the loads and
 // the stores (the stage may still be in use while the loads travel).
-template <int PREC, int E, int NCOL, class Wait>
+template <int PREC, int E, int NCOL, bool CL, class Wait>
 __device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJob &jb, int c0,
                                          long cstride, int iw0, int W, int C, uint8_t *stage,
                                          int lo_off, int lane, float &amax, int s2sub,
                                          Wait &&wait_stage) {
   float v[NCOL][E];
 #pragma unroll
-  for (int k = 0; k < NCOL; ++k) load_pixel<E>(x, jb, c0 + lane + 32 * k, cstride, iw0, W, C, v[k]);
+  for (int k = 0; k < NCOL; ++k)
+    load_pixel<E, CL>(x, jb, c0 + lane + 32 * k, cstride, iw0, W, C, v[k]);
   if (!wait_stage()) return false;
 #pragma unroll
   for (int k = 0; k < NCOL; ++k) {
@@ -827,7 +849,7 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial) {
@@ -835,6 +857,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   static_assert(U == 1 || U == 2, "one or two M tiles per unit");
   static_assert(!POOL || U == 2 || SP, "pooling takes two output rows per unit");
   static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
+  static_assert(!CL || (!POOL && !S2), "channels-last: stride-1 elementwise entries");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1006,12 +1029,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         for (; ok && J < njobs; J += kProdWarps) {
           if (J < mjobs) {
             const MainJob mj = main_job(J, parts, G);
-            const RowJob jb = row_job(mj.row, ss, q, p, nrows, E, S2);
+            const RowJob jb = row_job(mj.row, ss, q, p, nrows, E, S2, CL);
             switch (mj.ngroups) {
-              case 1: ok = fill_row<PREC, E, 1>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
-              case 2: ok = fill_row<PREC, E, 2>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
-              case 3: ok = fill_row<PREC, E, 3>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
-              default: ok = fill_row<PREC, E, 4>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              case 1: ok = fill_row<PREC, E, 1, CL>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              case 2: ok = fill_row<PREC, E, 2, CL>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              case 3: ok = fill_row<PREC, E, 3, CL>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
+              default: ok = fill_row<PREC, E, 4, CL>(p.x, jb, mj.c0, cstride, ss.iw0, p.W, p.C, stage, lo_off, lane, amax, s2sub, wait_stage); break;
             }
           } else {
             // lane -> (row job, tail pixel) pair
@@ -1021,8 +1044,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             float v[E];
             RowJob jb;
             if (job < jobs) {
-              jb = row_job(job, ss, q, p, nrows, E, S2);
-              load_pixel<E>(p.x, jb, cc, cstride, ss.iw0, p.W, p.C, v);
+              jb = row_job(job, ss, q, p, nrows, E, S2, CL);
+              load_pixel<E, CL>(p.x, jb, cc, cstride, ss.iw0, p.W, p.C, v);
             }
             ok = wait_stage();
             if (ok && job < jobs) {
@@ -1297,59 +1320,96 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               else
                 av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
             }
-            float *yc = yp + (long)cc * cstride;
-            if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
-              if constexpr (CHAIN == CHAIN_GENERIC) {  // op loop outside, 16 values inside
-                float v[16];
+            if constexpr (CL) {
+              // channels-last output: this pixel's 16 channels are adjacent
+              if (valid) {
+                float o[16];
+                if constexpr (CHAIN == CHAIN_GENERIC) {
   #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, 16, v);
+                  for (int j = 0; j < 16; ++j)
+                    o[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, o);
+                } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
+                                     CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
   #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  *yc = v[j];
-                  yc += cstride;
+                  for (int j = 0; j < 16; j += 2)
+                    apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
+                                        __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
+                                        bv[j + 1], av[j], av[j + 1], o[j], o[j + 1]);
+                } else {
+  #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    const float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                    o[j] = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                  }
                 }
-              } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
-                                   CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+                float *yc = p.y + ((((long)up.n * p.Do + up.od) * p.Ho + oh) * p.Wo + ow) * p.CO +
+                            co_base + ch0 + cc;
+                if (cc + 16 <= nco && (p.CO & 3) == 0) {  // 16-byte aligned vectors
   #pragma unroll
-                for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
-                  float o0, o1;
-                  apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
-                                      __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
-                                      bv[j + 1], av[j], av[j + 1], o0, o1);
-                  yc[0] = o0;
-                  yc[cstride] = o1;
-                  yc += 2 * cstride;
-                }
-              } else {
+                  for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4 *>(yc + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+                } else {
   #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                  *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-                  yc += cstride;
+                  for (int j = 0; j < 16; ++j)
+                    if (cc + j < nco) yc[j] = o[j];
                 }
               }
-            } else if (valid) {
-              if constexpr (CHAIN == CHAIN_GENERIC) {
-                float v[16];
-  #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, v);
-  #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (cc + j < nco) *yc = v[j];
-                  yc += cstride;
-                }
-              } else {
-  #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (cc + j < nco) {
+            } else {
+              float *yc = yp + (long)cc * cstride;
+              if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
+                if constexpr (CHAIN == CHAIN_GENERIC) {  // op loop outside, 16 values inside
+                  float v[16];
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, 16, v);
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    *yc = v[j];
+                    yc += cstride;
+                  }
+                } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
+                                     CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+    #pragma unroll
+                  for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
+                    float o0, o1;
+                    apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
+                                        __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
+                                        bv[j + 1], av[j], av[j + 1], o0, o1);
+                    yc[0] = o0;
+                    yc[cstride] = o1;
+                    yc += 2 * cstride;
+                  }
+                } else {
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
                     float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
                     *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                    yc += cstride;
                   }
-                  yc += cstride;
+                }
+              } else if (valid) {
+                if constexpr (CHAIN == CHAIN_GENERIC) {
+                  float v[16];
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, v);
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    if (cc + j < nco) *yc = v[j];
+                    yc += cstride;
+                  }
+                } else {
+    #pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    if (cc + j < nco) {
+                      float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
+                      *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
+                    }
+                    yc += cstride;
+                  }
                 }
               }
             }
@@ -1560,10 +1620,10 @@ __global__ void selftest_wait_kernel(unsigned int *status, uint64_t limit_ns) {
 
 int g_num_sms = 0;
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false, bool CL = false>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                           float *partial, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP>;
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP, CL>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1580,18 +1640,18 @@ cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *
   return cudaGetLastError();
 }
 
-template <int PREC, int U, bool S2>
+template <int PREC, int U, bool S2, bool CL = false>
 cudaError_t launch_chain(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                          float *partial, cudaStream_t s) {
   switch (p.chain) {
-    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U, S2>(p, q, bimg, partial, s);
+    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U, S2, false, CL>(p, q, bimg, partial, s);
     case CHAIN_RELU_HARDSWISH:
-      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U, S2>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U, S2, false, CL>(p, q, bimg, partial, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U, S2>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U, S2, false, CL>(p, q, bimg, partial, s);
     case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U, S2>(p, q, bimg, partial, s);
-    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U, S2>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U, S2, false, CL>(p, q, bimg, partial, s);
+    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U, S2, false, CL>(p, q, bimg, partial, s);
   }
 }
 
@@ -1605,6 +1665,9 @@ cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bi
   if (q.S2)
     return q.U == 2 ? launch_chain<PREC, 2, true>(p, q, bimg, partial, s)
                     : launch_chain<PREC, 1, true>(p, q, bimg, partial, s);
+  if (p.cl)  // channels-last input and output: its own instances
+    return q.U == 2 ? launch_chain<PREC, 2, false, true>(p, q, bimg, partial, s)
+                    : launch_chain<PREC, 1, false, true>(p, q, bimg, partial, s);
   return q.U == 2 ? launch_chain<PREC, 2, false>(p, q, bimg, partial, s)
                   : launch_chain<PREC, 1, false>(p, q, bimg, partial, s);
 }

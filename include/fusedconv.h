@@ -164,6 +164,25 @@ FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, in
                         int stride, int pad, int dilation, const fc_epilogue *epi,
                         float *y, void *ws, size_t ws_bytes, void *stream);
 
+/* Channels-last forms of fc_conv2d_epi / fc_conv3d_epi: the same
+ * arguments (sizes as N, C_in, [D,] H, W; weights [C_out][C_in][k...] as
+ * there), but x is [N][H][W][C_in] ([N][D][H][W][C_in]) and y is
+ * [N][Ho][Wo][C_out] ([N][Do][Ho][Wo][C_out]).  A pixel's channels are then
+ * adjacent, so the kernel reads them (and writes its outputs) as 16-byte
+ * vectors when C_in (C_out) is a multiple of 4.  Tensor-core variants only
+ * (FC_VARIANT_FFMA returns FC_ERR_UNSUPPORTED; AUTO picks the tensor
+ * cores); stride 1 (dilation 1 or 2, pads as above); stride 2 returns
+ * FC_ERR_UNSUPPORTED.  Workspace: fc_workspace_bytes(0 or 1, ...) as for
+ * the channels-first calls. */
+FC_API fc_status fc_conv2d_epi_nhwc(const float *x, int N, int C_in, int H, int W,
+                                    const float *w, int C_out, int kH, int kW, int stride,
+                                    int pad, int dilation, const fc_epilogue *epi, float *y,
+                                    void *ws, size_t ws_bytes, void *stream);
+FC_API fc_status fc_conv3d_epi_ndhwc(const float *x, int N, int C_in, int D, int H, int W,
+                                     const float *w, int C_out, int kD, int kH, int kW,
+                                     int stride, int pad, int dilation, const fc_epilogue *epi,
+                                     float *y, void *ws, size_t ws_bytes, void *stream);
+
 /* ConvTranspose2d + bias -> MaxPool2d -> Hardtanh[a,b] -> mean(H,W)
  * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];
  * y [N][C_out][1][1].  The epilogue chain must be exactly

@@ -598,3 +598,67 @@ def test_general_pool_refused_by_tensor_core_variants():
                 m.fc_convT2d_pool_mean(x, w, None, pool=(3, 2))
         finally:
             m.set_variant("auto")
+
+
+# ------------------------------------------------ channels-last (N(D)HWC)
+@pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
+@pytest.mark.parametrize("shape,pad,dil,chain", [
+    ((2, 8, 33, 37, 64), 0, 1, "rh"),
+    ((1, 12, 17, 20, 70), 1, 1, "gelu"),      # C_in, C_out not multiples of 4 / 64
+    ((1, 16, 9, 150, 64), 2, 2, "generic"),   # strips, dilation 2
+    ((2, 64, 10, 30, 64), 1, 1, "none"),      # several channel chunks
+])
+def test_conv2d_channels_last(variant, shape, pad, dil, chain):
+    N, C, H, W, CO = shape
+    st = synth.seeded(790 + C + pad)
+    x = st.normal((N, C, H, W))
+    w = st.uniform((CO, C, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((CO,), 0.1)
+    ops = _chain(chain, CO, st)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        xl = torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 3, 1))).cuda()
+        y = m.fc_conv2d_epi_nhwc(xl, _dev(w), _dev(b), _ops_torch(ops), pad=pad, dilation=dil)
+        if variant != "auto":
+            assert m.last_variant() == variant
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy().transpose(0, 3, 1, 2)
+    finally:
+        m.set_variant("auto")
+    _check(got, oracle.conv_epi(x, w, b, ops, pad=pad, dilation=dil),
+           f"{variant} channels-last conv2d {shape}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "tc_f16x3"])
+def test_conv3d_channels_last(variant):
+    st = synth.seeded(795)
+    x = st.normal((2, 8, 6, 10, 30))
+    w = st.uniform((64, 8, 3, 3, 3), 1.0 / np.sqrt(216.0))
+    b = st.uniform((64,), 0.1)
+    s = st.normal((64,))
+    ops = chain_gelu(s)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        xl = torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 3, 4, 1))).cuda()
+        y = m.fc_conv3d_epi_ndhwc(xl, _dev(w), _dev(b), _ops_torch(ops), pad=1)
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy().transpose(0, 4, 1, 2, 3)
+    finally:
+        m.set_variant("auto")
+    _check(got, oracle.conv_epi(x, w, b, ops, pad=1), f"{variant} channels-last conv3d")
+
+
+def test_channels_last_refused_by_cuda_core_and_stride2():
+    m = fc()
+    x = torch.zeros((1, 8, 8, 8), device="cuda")
+    w = _dev(np.zeros((64, 8, 3, 3), np.float32))
+    m.set_variant("ffma")
+    try:
+        with pytest.raises(m.FcError):
+            m.fc_conv2d_epi_nhwc(x, w, None, ())
+    finally:
+        m.set_variant("auto")
+    with pytest.raises(m.FcError):
+        m.fc_conv2d_epi_nhwc(x, w, None, (), stride=2)
