@@ -85,9 +85,6 @@ NCU_TRAFFIC = {
     (5, "tc_f16x3"): {"src": "9ae71122429f537e", "bytes": 2179293184},
     # full-size capture; the tail of y is still in L2 when the launch ends
     (3, "tc_f16x3"): {"src": "9ae71122429f537e", "bytes": 527911680},
-},
-    # full-size capture; the tail of y is still in L2 when the launch ends
-    (3, "tc_f16x3"): {"src": "79bff196e7213315", "bytes": 528308992},
 }
 
 KERNEL_SOURCES = ("fc_tc.cu", "fc_tc_ptx.cuh", "fc_epi.cuh", "fc_internal.h")
