@@ -97,7 +97,8 @@ fc_status decode_eltwise(const fc_epilogue *epi, EpiDev *e, int *chain) {
   return FC_OK;
 }
 
-// The pooled entry point accepts exactly MAXPOOL2X2, HARDTANH, MEAN_HW, TANH.
+// The pooled entry point accepts exactly MAXPOOL2X2 (or MAXPOOL(k, s)),
+// HARDTANH, MEAN_HW, TANH.
 fc_status decode_pool(const fc_epilogue *epi, EpiDev *e, float *lo, float *hi, int *pk,
                       int *ps) {
   memset(e, 0, sizeof(*e));

@@ -142,3 +142,24 @@ def test_pool_mean_tail_host_validation(L):
     assert call(lo=1.0, hi=-1.0) == INVALID
     assert call(x=0) == INVALID          # NULL with N > 0
     assert call(N=0) == 0                # nothing to do
+
+
+def test_general_pool_chain_validation(L):
+    """The pooled entry's general max pool: window and stride integers in
+    1..4, stride-1 transposed conv only; the op is refused by the elementwise
+    entries.  All rejected on the host before any device work."""
+    UNSUP = 2
+    assert _conv2d(L, ops=(("maxpool", 3.0, 2.0),)) == UNSUP
+
+    def pool_call(pool, stride=1, out_pad=0):
+        e, _ = _epi(fc.pool_mean_ops(pool=pool))
+        return L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
+                                      4, 3, stride, 1, out_pad, ctypes.byref(e),
+                                      ctypes.c_void_p(16), ctypes.c_void_p(256), 1 << 20, None)
+    assert pool_call((5, 2)) == UNSUP      # window above 4
+    assert pool_call((3, 0)) == UNSUP      # stride below 1
+    assert pool_call((2.5, 2)) == UNSUP    # not an integer
+    assert pool_call((3, 2), stride=2, out_pad=1) == UNSUP  # general pool at stride 2
+    # workspace entry 3 (general pool) covers its per-tile partials
+    assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 1, 0, 3, 2)) > 0
+    assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 2, 1, 3, 2)) == 0  # stride 2: no
