@@ -662,3 +662,58 @@ def test_channels_last_refused_by_cuda_core_and_stride2():
         m.set_variant("auto")
     with pytest.raises(m.FcError):
         m.fc_conv2d_epi_nhwc(x, w, None, (), stride=2)
+
+
+# ------------------------------------------------------------ size limits
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_very_wide_rows_sampled(variant):
+    """Rows of 2048 outputs: 16 tensor-core column strips plus a ragged one."""
+    st = synth.seeded(800)
+    x = st.normal((1, 8, 5, 2050))
+    w = st.uniform((64, 8, 3, 3), 1.0 / np.sqrt(72.0))
+    b = st.uniform((64,), 0.1)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), CHAIN_RH, pad=1)
+        assert m.get_last_device_error() == 0
+        shape = tuple(y.shape)
+        idx = _sample_idx(shape, 3000, 800)
+        got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    ref = oracle.conv_epi_points(x, w, b, CHAIN_RH, idx, pad=1)
+    _check(got, ref, f"{variant} wide rows")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_largest_channel_block(variant):
+    """C_in 256 (16 fp16 chunks) and C_out 512, the most output channels the
+    tensor-core kernel stages: the weights no longer fit shared memory and
+    stream through the weight ring."""
+    st = synth.seeded(801)
+    x = st.normal((1, 256, 6, 40))
+    w = st.uniform((512, 256, 3, 3), 1.0 / np.sqrt(2304.0))
+    b = st.uniform((512,), 0.1)
+    got = _run_conv(variant, x, w, b, (("relu",),), pad=1)
+    _check(got, oracle.conv_epi(x, w, b, (("relu",),), pad=1), f"{variant} C 256 -> 512")
+
+
+def test_output_channels_beyond_the_tensor_core_block():
+    """C_out 520 > 512: the tensor-core variants refuse (FC_ERR_UNSUPPORTED),
+    AUTO runs the CUDA-core kernel."""
+    st = synth.seeded(802)
+    x = st.normal((1, 8, 7, 9))
+    w = st.uniform((520, 8, 3, 3), 1.0 / np.sqrt(72.0))
+    b = st.uniform((520,), 0.1)
+    m = fc()
+    for v in ("tc_tf32x3", "tc_f16x3"):
+        m.set_variant(v)
+        try:
+            with pytest.raises(m.FcError):
+                m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), ())
+        finally:
+            m.set_variant("auto")
+    y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), ())
+    assert m.last_variant() == "ffma"
+    _check(y.cpu().numpy(), oracle.conv_epi(x, w, b, ()), "C_out 520 auto")
