@@ -1,7 +1,8 @@
 /*
- * fusedconv.h -- C ABI of libfusedconv: dense 2-D / 3-D convolutions and a
- * stride-1 transposed convolution with their elementwise and reduction
- * epilogues fused into the same kernel, for one NVIDIA GB300 (sm_103a).
+ * fusedconv.h -- C ABI of libfusedconv: dense 2-D / 3-D convolutions
+ * (stride 1 or 2, dilation 1 or 2) and a transposed convolution (stride 1
+ * or 2) with their elementwise and reduction epilogues fused into the same
+ * kernel, for one NVIDIA GB300 (sm_103a).
  *
  * Sources of the operations (three POPCORNBENCH reasoning traces):
  *  - fc_conv2d_epi: trace "Kimi-K2.6__l2_p57", problem statement and
@@ -15,11 +16,15 @@
  *    ConvTranspose2d(k 3, stride 1, padding 1) (bias) -> MaxPool2d(2, 2) ->
  *    Hardtanh[-1, 1] -> mean over (H, W) keepdim -> tanh.  Computed as a
  *    plain convolution with swapped channel axes, both taps flipped and
- *    padding k - 1 - p (the trace's transposed-conv equivalence paragraph).
+ *    padding k - 1 - p (the trace's transposed-conv equivalence paragraph);
+ *    at stride 2 per output parity class (the taps each class reads) on the
+ *    input grid; the trace's general max-pool paragraph for other pool
+ *    windows.
  *
  * Conventions for every entry point
  *  - All tensor pointers are DEVICE pointers to contiguous fp32 arrays in
- *    PyTorch's default layouts: x NCHW / NCDHW; conv weights
+ *    PyTorch's default layouts: x NCHW / NCDHW (NHWC / NDHWC for the
+ *    _nhwc / _ndhwc entry points, which also write y channels-last); conv weights
  *    [C_out][C_in][kD][kH][kW]; transposed-conv weights [C_in][C_out][k][k];
  *    bias [C_out]; per-channel tensors of epilogue ops [C_out].  The caller
  *    owns every buffer; the library allocates nothing.
