@@ -261,6 +261,16 @@ def run_reference(args):
     return 0
 
 
+def aggregate_replicas(my_ms, world, steps, flops_step, max_over_ranks=None):
+    """Whole-job throughput of `world` independent replicas (weak scaling):
+    every rank runs the same `steps` steps of `flops_step` FLOPs; the job
+    takes as long as its slowest rank, so the time is the max over ranks of
+    each rank's summed step time (ms) and the value counts every rank's work.
+    Returns (job ms, GFLOP/s)."""
+    tot_ms = max_over_ranks(my_ms) if (world > 1 and max_over_ranks is not None) else my_ms
+    return tot_ms, world * flops_step * steps / (tot_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ GPU side
 def run_ours(args):
     import torch
@@ -352,14 +362,15 @@ def run_ours(args):
             step_ms[k] += ts[k]
         per[w] = ts
     my_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
+
+    def max_over_ranks(v):
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
-    else:
-        tot_ms = my_ms
+        return float(t.item())
+
     flops_step = sum(2 * macs_of(w) for w in WORKLOADS)
-    value = world * flops_step * args.steps / (tot_ms * 1e-3) / 1e9
+    tot_ms, value = aggregate_replicas(my_ms, world, args.steps, flops_step,
+                                       max_over_ranks if world > 1 else None)
 
     # dominant kernel: the main kernel with the largest summed time
     entry_of = {3: 0, 4: 1, 5: 2}
