@@ -132,6 +132,41 @@ def _require_cuda_f32(name, t):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _dims(name, t, ndim):
+    """Shape of a tensor argument, checked for its rank (any device: shapes
+    are checked before anything touches the GPU)."""
+    shape = tuple(getattr(t, "shape", ()))
+    if len(shape) != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {shape}")
+    return shape
+
+
+def _check_out(name, t, shape):
+    """A caller-provided output must have exactly the shape the call
+    writes: the kernels write every element of that shape, so a smaller
+    tensor would be written past its end."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; this call writes {tuple(shape)}")
+
+
+def _check_vec(name, t, n):
+    if t is not None and tuple(t.shape) != (n,) and int(t.numel()) != n:
+        raise ValueError(f"{name} must hold {n} values (one per output channel), "
+                         f"got shape {tuple(t.shape)}")
+
+
+def _check_ops(ops, cout):
+    for op in ops:
+        if op[0] not in EPI:
+            raise ValueError(f"unknown epilogue op {op[0]!r}")
+        if op[0] == "add_channel":
+            _check_vec("add_channel tensor", op[1], cout)
+
+
+def _ws_bytes(ws):
+    return int(ws.numel()) * int(ws.element_size())
+
+
 def _stream_handle(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -140,6 +175,8 @@ def _stream_handle(stream):
 
 def make_epilogue(bias, ops):
     """Build the C epilogue descriptor; returns (struct, keepalive list)."""
+    if bias is not None:
+        _require_cuda_f32("bias", bias)
     e = _Epilogue()
     keep = []
     e.bias = None if bias is None else bias.data_ptr()
@@ -236,13 +273,16 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
     """Conv2d(k=3, stride 1 or 2, pad, dilation 1 or 2) + bias + elementwise
     ops -> y [N,CO,Ho,Wo]."""
     import torch
-    _require_cuda_f32("x", x)
-    _require_cuda_f32("w", w)
-    N, C, H, W = x.shape
-    CO, C2, KH, KW = w.shape
+    N, C, H, W = _dims("x", x, 4)
+    CO, C2, KH, KW = _dims("w", w, 4)
     if C2 != C:
         raise ValueError("weight C_in mismatch")
     Ho, Wo = _extent(H, KH, stride, pad, dilation), _extent(W, KW, stride, pad, dilation)
+    _check_out("y", y, (N, CO, Ho, Wo))
+    _check_vec("bias", bias, CO)
+    _check_ops(ops, CO)
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
     if y is None:
         y = torch.empty((N, CO, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -250,7 +290,7 @@ def fc_conv2d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
         ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv2d_epi(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, int(stride), pad,
-                             int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                             int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws), _ws_bytes(ws),
                              _stream_handle(stream))
     _check(st, "fc_conv2d_epi")
     del keep
@@ -261,15 +301,18 @@ def fc_conv2d_epi_noalloc(x, w, y, bias=None, ops=(), pad=0, stream=None):
     """fc_conv2d_epi without a workspace argument, for callers that cannot
     allocate device memory: the library uses its own fixed 1 MiB device
     array (shared by all calls on a device; overlapping calls race).  The
-    caller passes every tensor, including the output y; nothing is
-    allocated here."""
+    caller passes every tensor, including the output y, whose shape must be
+    the call's output shape; nothing is allocated here."""
+    N, C, H, W = _dims("x", x, 4)
+    CO, C2, KH, KW = _dims("w", w, 4)
+    if C2 != C:
+        raise ValueError("weight C_in mismatch")
+    _check_out("y", y, (N, CO, _extent(H, KH, 1, pad, 1), _extent(W, KW, 1, pad, 1)))
+    _check_vec("bias", bias, CO)
+    _check_ops(ops, CO)
     _require_cuda_f32("x", x)
     _require_cuda_f32("w", w)
     _require_cuda_f32("y", y)
-    N, C, H, W = x.shape
-    CO, C2, KH, KW = w.shape
-    if C2 != C:
-        raise ValueError("weight C_in mismatch")
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv2d_epi_noalloc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, 1, pad, 1,
                                      ctypes.byref(e), _ptr(y), _stream_handle(stream))
@@ -282,14 +325,17 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
                   dilation=1):
     """Conv3d(k=3, stride 1 or 2, pad, dilation 1 or 2) + bias + elementwise ops."""
     import torch
-    _require_cuda_f32("x", x)
-    _require_cuda_f32("w", w)
-    N, C, D, H, W = x.shape
-    CO, C2, KD, KH, KW = w.shape
+    N, C, D, H, W = _dims("x", x, 5)
+    CO, C2, KD, KH, KW = _dims("w", w, 5)
     if C2 != C:
         raise ValueError("weight C_in mismatch")
     Do, Ho, Wo = (_extent(D, KD, stride, pad, dilation), _extent(H, KH, stride, pad, dilation),
                   _extent(W, KW, stride, pad, dilation))
+    _check_out("y", y, (N, CO, Do, Ho, Wo))
+    _check_vec("bias", bias, CO)
+    _check_ops(ops, CO)
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
     if y is None:
         y = torch.empty((N, CO, Do, Ho, Wo), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -298,7 +344,7 @@ def fc_conv3d_epi(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=None, 
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv3d_epi(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, int(stride),
                              pad, int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
-                             ws.numel(), _stream_handle(stream))
+                             _ws_bytes(ws), _stream_handle(stream))
     _check(st, "fc_conv3d_epi")
     del keep
     return y
@@ -308,13 +354,16 @@ def fc_conv2d_epi_nhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=N
                        dilation=1):
     """Channels-last conv2d: x [N,H,W,C_in], w [C_out,C_in,3,3] -> y [N,Ho,Wo,C_out]."""
     import torch
-    _require_cuda_f32("x", x)
-    _require_cuda_f32("w", w)
-    N, H, W, C = x.shape
-    CO, C2, KH, KW = w.shape
+    N, H, W, C = _dims("x", x, 4)
+    CO, C2, KH, KW = _dims("w", w, 4)
     if C2 != C:
         raise ValueError("weight C_in mismatch")
     Ho, Wo = _extent(H, KH, stride, pad, dilation), _extent(W, KW, stride, pad, dilation)
+    _check_out("y", y, (N, Ho, Wo, CO))
+    _check_vec("bias", bias, CO)
+    _check_ops(ops, CO)
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
     if y is None:
         y = torch.empty((N, Ho, Wo, CO), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -322,8 +371,8 @@ def fc_conv2d_epi_nhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=N
         ws = _workspace(workspace_bytes(0, (N, C, H, W, CO, KH, pad)), x.device)
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv2d_epi_nhwc(_ptr(x), N, C, H, W, _ptr(w), CO, KH, KW, int(stride), pad,
-                                  int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
-                                  _stream_handle(stream))
+                                  int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
+                                  _ws_bytes(ws), _stream_handle(stream))
     _check(st, "fc_conv2d_epi_nhwc")
     del keep
     return y
@@ -333,14 +382,17 @@ def fc_conv3d_epi_ndhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=
                         dilation=1):
     """Channels-last conv3d: x [N,D,H,W,C_in], w [C_out,C_in,3,3,3] -> y [N,Do,Ho,Wo,C_out]."""
     import torch
-    _require_cuda_f32("x", x)
-    _require_cuda_f32("w", w)
-    N, D, H, W, C = x.shape
-    CO, C2, KD, KH, KW = w.shape
+    N, D, H, W, C = _dims("x", x, 5)
+    CO, C2, KD, KH, KW = _dims("w", w, 5)
     if C2 != C:
         raise ValueError("weight C_in mismatch")
     Do, Ho, Wo = (_extent(D, KD, stride, pad, dilation), _extent(H, KH, stride, pad, dilation),
                   _extent(W, KW, stride, pad, dilation))
+    _check_out("y", y, (N, Do, Ho, Wo, CO))
+    _check_vec("bias", bias, CO)
+    _check_ops(ops, CO)
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
     if y is None:
         y = torch.empty((N, Do, Ho, Wo, CO), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -349,7 +401,7 @@ def fc_conv3d_epi_ndhwc(x, w, bias=None, ops=(), pad=0, y=None, ws=None, stream=
     e, keep = make_epilogue(bias, ops)
     st = lib().fc_conv3d_epi_ndhwc(_ptr(x), N, C, D, H, W, _ptr(w), CO, KD, KH, KW, int(stride),
                                    pad, int(dilation), ctypes.byref(e), _ptr(y), _ptr(ws),
-                                   ws.numel(), _stream_handle(stream))
+                                   _ws_bytes(ws), _stream_handle(stream))
     _check(st, "fc_conv3d_epi_ndhwc")
     del keep
     return y
@@ -367,12 +419,14 @@ def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
     (window, stride) = pool -> hardtanh -> mean(H,W) -> tanh.
     w: [C_in, C_out, 3, 3]; returns y [N, C_out, 1, 1]."""
     import torch
-    _require_cuda_f32("x", x)
-    _require_cuda_f32("w", w)
-    N, C, H, W = x.shape
-    C2, CO, K, _ = w.shape
+    N, C, H, W = _dims("x", x, 4)
+    C2, CO, K, _ = _dims("w", w, 4)
     if C2 != C:
         raise ValueError("weight C_in mismatch")
+    _check_out("y", y, (N, CO, 1, 1))
+    _check_vec("bias", bias, CO)
+    _require_cuda_f32("x", x)
+    _require_cuda_f32("w", w)
     if y is None:
         y = torch.empty((N, CO, 1, 1), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -385,7 +439,7 @@ def fc_convT2d_pool_mean(x, w, bias=None, hardtanh=(-1.0, 1.0), pad=1, y=None,
     e, keep = make_epilogue(bias, pool_mean_ops(*hardtanh, pool=pool))
     st = lib().fc_convT2d_pool_mean(_ptr(x), N, C, H, W, _ptr(w), CO, K, int(stride), pad,
                                     int(out_pad),
-                                    ctypes.byref(e), _ptr(y), _ptr(ws), ws.numel(),
+                                    ctypes.byref(e), _ptr(y), _ptr(ws), _ws_bytes(ws),
                                     _stream_handle(stream))
     _check(st, "fc_convT2d_pool_mean")
     del keep
@@ -396,8 +450,9 @@ def fc_pool_mean_tail(x, k=2, s=2, hardtanh=(-1.0, 1.0), y=None, stream=None):
     """MaxPool(k, s) -> hardtanh -> mean(H, W) -> tanh on a conv output
     x [N, C, H, W]; returns y [N, C, 1, 1]."""
     import torch
+    N, C, H, W = _dims("x", x, 4)
+    _check_out("y", y, (N, C, 1, 1))
     _require_cuda_f32("x", x)
-    N, C, H, W = x.shape
     if y is None:
         y = torch.empty((N, C, 1, 1), dtype=torch.float32, device=x.device)
     _require_cuda_f32("y", y)
@@ -405,4 +460,3 @@ def fc_pool_mean_tail(x, k=2, s=2, hardtanh=(-1.0, 1.0), y=None, stream=None):
                                    float(hardtanh[1]), _ptr(y), _stream_handle(stream)),
            "fc_pool_mean_tail")
     return y
-

@@ -44,22 +44,6 @@
 #include "fc_internal.h"
 #include "fc_tc_ptx.cuh"
 
-// Optional per-role cycle accounting for performance experiments (off in
-// the library build): each role's first thread accumulates clock64 deltas
-// into named buckets, written per CTA to fc_tc_role_cycles at exit.
-#ifdef FC_ROLE_TIMING
-#define RT_DECL unsigned long long rt_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; \
-  unsigned long long rt_t0 = clock64();
-#define RT_MARK(i) do { const unsigned long long t_ = clock64(); rt_[i] += t_ - rt_t0; rt_t0 = t_; } while (0)
-#define RT_STORE(role) do { if ((threadIdx.x & 31) == 0 && (role) >= 0) for (int i_ = 0; i_ < 8; ++i_) \
-  fc_tc_role_cycles[(blockIdx.x * 3 + (role)) * 8 + i_] = rt_[i_]; } while (0)
-__device__ unsigned long long fc_tc_role_cycles[1024 * 3 * 8];
-#else
-#define RT_DECL
-#define RT_MARK(i) do {} while (0)
-#define RT_STORE(role) do {} while (0)
-#endif
-
 namespace fc {
 
 namespace {
@@ -980,7 +964,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // stage ps of phase pph; weight slot psb of phase psbph
     int ps = 0, psb = 0;
     uint32_t pph = 0, psbph = 0;
-    RT_DECL
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const UnitPos up = decode_unit(u, q);
       StageSrc ss;
@@ -991,7 +974,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       ss.xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = ps;
-        RT_MARK(0);
         if (!q.b_resident && pw == 0) {
           const int sb = psb;
           if (!wait_bar_warp(bars, B_EMPTY + sb, psbph ^ 1, abort_flag, p.status, 0x11000000u | g)) {
@@ -1018,10 +1000,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         auto wait_stage = [&]() -> bool {
           if (waited) return true;
           waited = true;
-          RT_MARK(2);
           const bool w = wait_bar_warp(bars, A_EMPTY + s, pph ^ 1, abort_flag,
                                        p.status, 0x10000000u | g);
-          RT_MARK(1);
           return w;
         };
         int J = pw - rot;
@@ -1065,10 +1045,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&a_full[s]);
-        RT_MARK(2);  // filling the stage
       }
     }
-    RT_STORE(warp == kProdWarp0 ? 2 : -1);
     if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
     // drain outstanding weight copies before the CTA can exit
     if (pt == 0 && q.b_resident) wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
@@ -1103,14 +1081,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     // no wait.
     bool pre_full = false, pre_acc = false;
     bool ok = true;
-    RT_DECL
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
     for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
       const int acc = macc;
       const uint32_t acc_par = mpar ^ 1;
       if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
-      RT_MARK(0);
       // One wait for the whole accumulator: the epilogue frees a unit's
       // tiles in order (each warp arrives for tile t before tile t + 1), so
       // the last tile's barrier implies the others.
@@ -1118,7 +1094,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                                      abort_flag, p.status, 0x21000000u | it))
         break;
       ptx::tc_fence_after();
-      RT_MARK(1);  // waiting for a free accumulator
       if constexpr (SP) {
         if (q.SPLIT) {
           // half A (classes (0,0), (0,1)) over every chunk, then half B; the
@@ -1166,7 +1141,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           pre_acc = __all_sync(0xffffffffu, ptx::mbar_test_wait(&acc_empty[0], mpar ^ 1));
           if (ptx::elect_one()) ptx::tc_commit(&acc_full[1]);
           __syncwarp();
-          RT_MARK(3);
           continue;
         }
       }
@@ -1174,7 +1148,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const int s = ms;
         const uint32_t sph = mph;
         if (++ms == q.S) { ms = 0; mph ^= 1; }
-        RT_MARK(0);
         if (!pre_full && !wait_bar_warp(bars, A_FULL + s, sph, abort_flag, p.status, 0x22000000u | g)) {
           ok = false;
           break;
@@ -1192,7 +1165,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           bbase = sbase + q.off_b + (uint32_t)(sb * q.b_chunk_bytes);
         }
         ptx::tc_fence_after();
-        RT_MARK(2);  // waiting for a filled stage
         // low descriptor words of this stage / weight chunk (start address
         // and leading byte offset); the high word is the same for all
         const uint32_t a_lo = ((sbase + (uint32_t)(s * q.a_stage_bytes)) >> 4) & 0x3FFFu;
@@ -1239,7 +1211,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ++gb;
           if (++msb == q.SB) { msb = 0; msbph ^= 1; }
         }
-        RT_MARK(3);  // issuing MMAs
       }
       if (!ok) break;
       if constexpr (POOL) {
@@ -1251,8 +1222,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     if (ptx::elect_one()) ptx::tc_commit(drain);
     __syncwarp();
     wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u);
-    RT_MARK(4);
-    RT_STORE(1);
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lane quadrant w % 4 (one output pixel per lane) and
@@ -1264,20 +1233,17 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     uint32_t it = 0;
     int eacc = 0;  // accumulator eacc of phase epar, as counters
     uint32_t epar = 0;
-    RT_DECL
     for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
       const UnitPos up = decode_unit(u, q);
       const int acc = eacc;
       const uint32_t acc_par = epar;
       if (++eacc == q.NACC) { eacc = 0; epar ^= 1; }
-      RT_MARK(0);
       if constexpr (POOL) {
         bool okw = wait_bar_warp(bars, ACC_FULL + acc, acc_par, abort_flag, p.status, 0x30000000u | it);
         okw = epi_all(okw);
         if (!okw) break;
         ptx::tc_fence_after();
       }
-      RT_MARK(1);  // waiting for a finished accumulator
       const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
       const int co_base = up.cb * 64;
       const int ch0 = half * 32;  // first channel (within the block) of this warp
@@ -1304,11 +1270,9 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   #pragma unroll 1
           for (int cc = 0; cc < 32; cc += 16) {
             uint32_t hi[16], lo[16];
-            RT_MARK(0);
             ptx::tmem_ld16(tl + col0 + cc, hi);
             ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
             ptx::tmem_wait_ld();
-            RT_MARK(2);  // tensor-memory loads
             float bv[16], av[16];
             const float *sb = &ctl->bias[co_base + ch0 + cc];
             const float *sa = &ctl->addend[co_base + ch0 + cc];
@@ -1413,7 +1377,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                 }
               }
             }
-            RT_MARK(3);  // epilogue math + stores
           }
           ptx::tc_fence_before();
           __syncwarp();
@@ -1585,7 +1548,6 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         epi_sync();
       }
     }
-    RT_STORE(warp == 0 ? 0 : -1);
   }
 
   ptx::tc_fence_before();
@@ -1728,13 +1690,3 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
 }
 
 }  // namespace fc
-
-#ifdef FC_ROLE_TIMING
-extern "C" __attribute__((visibility("default"))) int fc_debug_role_cycles(unsigned long long *out,
-                                                                            int n) {
-  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-  if (n > 1024 * 3 * 8) n = 1024 * 3 * 8;
-  return cudaMemcpyFromSymbol(out, fc_tc_role_cycles, sizeof(unsigned long long) * n) == cudaSuccess
-             ? n : -1;
-}
-#endif

@@ -163,3 +163,44 @@ def test_general_pool_chain_validation(L):
     # workspace entry 3 (general pool) covers its per-tile partials
     assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 1, 0, 3, 2)) > 0
     assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 2, 1, 3, 2)) == 0  # stride 2: no
+
+
+def test_binding_refuses_wrong_output_shapes_before_any_launch():
+    """A caller-provided y (or bias / per-channel tensor) whose shape is not
+    the one the call writes is refused by the binding with ValueError before
+    it checks devices or calls the library: the kernels write every element
+    of the call's output shape, so a smaller tensor would be overrun."""
+    import torch
+    x = torch.zeros((2, 8, 10, 12))
+    w = torch.zeros((64, 8, 3, 3))
+    bad = torch.zeros((2, 64, 10, 12))  # pad-1 extents, called with pad 0
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi(x, w, None, (), pad=0, y=bad)
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi_noalloc(x, w, bad, None, (), pad=0)
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi(x, w, torch.zeros(32), (), pad=1)  # bias of 32 for C_out 64
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi(x, w, None, (("add_channel", torch.zeros(63)),), pad=1)
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi(x, w, None, (), stride=2, y=torch.zeros((2, 64, 5, 5)))
+    x3 = torch.zeros((1, 8, 5, 6, 7))
+    w3 = torch.zeros((16, 8, 3, 3, 3))
+    with pytest.raises(ValueError):
+        fc.fc_conv3d_epi(x3, w3, None, (), y=torch.zeros((1, 16, 3, 4, 6)))
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi_nhwc(torch.zeros((1, 10, 12, 8)), w, None, (),
+                              y=torch.zeros((1, 64, 8, 10)))  # channels-first y
+    with pytest.raises(ValueError):
+        fc.fc_conv3d_epi_ndhwc(torch.zeros((1, 5, 6, 7, 8)), w3, None, (),
+                               y=torch.zeros((1, 3, 4, 5, 15)))
+    wt = torch.zeros((8, 64, 3, 3))
+    with pytest.raises(ValueError):
+        fc.fc_convT2d_pool_mean(x, wt, None, y=torch.zeros((2, 63, 1, 1)))
+    with pytest.raises(ValueError):
+        fc.fc_pool_mean_tail(torch.zeros((2, 4, 8, 8)), y=torch.zeros((2, 4)))
+    with pytest.raises(ValueError):
+        fc.fc_conv2d_epi(torch.zeros((2, 8, 10)), w, None, ())  # rank 3 x
+    # the right shapes get past the shape checks to the device checks
+    with pytest.raises(TypeError):
+        fc.fc_conv2d_epi(x, w, None, (), pad=1, y=bad)

@@ -7,7 +7,9 @@ trace, problem statement).
 * ragged shapes (several tiles plus a ragged tail, C_out not a multiple of
   64, odd extents, padding) for every variant and chain;
 * full-size workloads 3-5, in the launch configuration the benchmark times,
-  on sampled outputs that the oracle computes one by one.
+  on every output (the oracle runs once per workload on all host cores);
+* widened forms at full size on sampled outputs the oracle computes one by
+  one.
 """
 import numpy as np
 import pytest
@@ -230,29 +232,72 @@ def _sample_idx(shape, n, seed):
     return np.concatenate([idx, np.array(extra)])
 
 
+_REF = {}
+
+
+def _full_ref(wid):
+    """The oracle's result for every output of a full-size workload,
+    computed once per session (float64)."""
+    if wid not in _REF:
+        inp = _full_inputs(wid)
+        if wid == 3:
+            _REF[wid] = oracle.conv_epi(inp["x"], inp["w"], inp["b"], CHAIN_RH)
+        elif wid == 4:
+            _REF[wid] = oracle.conv_epi(inp["x"], inp["w"], inp["b"],
+                                        chain_gelu(inp["s"].reshape(-1)))
+        else:
+            _REF[wid] = oracle.convT_pool_mean(inp["x"], inp["w"], inp["b"])
+    return _REF[wid]
+
+
+def _check_whole(got, ref, what, chunk=1 << 24):
+    """Element-by-element allclose over every output, in chunks (the
+    full-size outputs hold up to 441 M values).  Returns the largest
+    tolerance use max |g - o| / (atol + rtol |o|)."""
+    g = np.asarray(got).reshape(-1)
+    r = np.asarray(ref).reshape(-1)
+    assert g.size == r.size, f"{what}: {g.size} outputs vs {r.size} in the oracle"
+    worst = 0.0
+    for c in range(0, g.size, chunk):
+        gc = g[c:c + chunk].astype(np.float64)
+        rc = r[c:c + chunk]
+        use = np.abs(gc - rc) / (ATOL + RTOL * np.abs(rc))
+        m = float(np.nanmax(use)) if use.size else 0.0
+        if not np.all(use <= 1.0):  # NaN fails too
+            i = int(np.argmax(np.where(np.isnan(use), np.inf, use)))
+            raise AssertionError(
+                f"{what}: {(~(use <= 1.0)).sum()} outputs in chunk at {c} outside "
+                f"atol=rtol=1e-4; worst flat index {c + i}: gpu={gc[i]!r} oracle={rc[i]!r}")
+        worst = max(worst, m)
+    return worst
+
+
 @pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
-def test_workload3_full_size_sampled(variant):
+def test_workload3_full_size_every_output(variant):
+    """conv2d [128,8,128,128] + ReLU + HardSwish: all 130 M outputs against
+    the oracle, in the launch configuration the benchmark times."""
     inp = _full_inputs(3)
+    ref = _full_ref(3)
     m = fc()
     m.set_variant(variant)
     try:
         y = m.fc_conv2d_epi(_dev(inp["x"]), _dev(inp["w"]), _dev(inp["b"]), CHAIN_RH)
         assert m.get_last_device_error() == 0
-        shape = tuple(y.shape)
-        assert shape == (128, 64, 126, 126)
-        idx = _sample_idx(shape, 4000, 3)
-        got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
-        ynp = None
+        assert tuple(y.shape) == (128, 64, 126, 126)
+        got = y.cpu().numpy()
+        del y
     finally:
         m.set_variant("auto")
-    ref = oracle.conv_epi_points(inp["x"], inp["w"], inp["b"], CHAIN_RH, idx)
-    _check(got, ref, f"workload 3 sampled [{variant}]")
-    del ynp
+    use = _check_whole(got, ref, f"workload 3 every output [{variant}]")
+    print(f"workload 3 [{variant}] max tolerance use {use:.4f}")
 
 
 @pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
-def test_workload4_full_size_sampled(variant):
+def test_workload4_full_size_every_output(variant):
+    """conv3d [128,8,16,64,64] + LeakyReLU + add + clamp + GELU: all 441 M
+    outputs against the oracle."""
     inp = _full_inputs(4)
+    ref = _full_ref(4)
     m = fc()
     m.set_variant(variant)
     s = inp["s"].reshape(-1)
@@ -260,35 +305,52 @@ def test_workload4_full_size_sampled(variant):
         y = m.fc_conv3d_epi(_dev(inp["x"]), _dev(inp["w"]), _dev(inp["b"]),
                             _ops_torch(chain_gelu(s)))
         assert m.get_last_device_error() == 0
-        shape = tuple(y.shape)
-        assert shape == (128, 64, 14, 62, 62)
-        idx = _sample_idx(shape, 4000, 4)
-        got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+        assert tuple(y.shape) == (128, 64, 14, 62, 62)
+        got = y.cpu().numpy()
+        del y
     finally:
         m.set_variant("auto")
-    ref = oracle.conv_epi_points(inp["x"], inp["w"], inp["b"], chain_gelu(s), idx)
-    _check(got, ref, f"workload 4 sampled [{variant}]")
+    use = _check_whole(got, ref, f"workload 4 every output [{variant}]")
+    print(f"workload 4 [{variant}] max tolerance use {use:.4f}")
 
 
 @pytest.mark.parametrize("variant", ["auto"] + VARIANTS)
-def test_workload5_full_size_sampled(variant):
+def test_workload5_full_size_every_output(variant):
+    """Transposed conv [128,64,256,256] -> pool -> hardtanh -> mean -> tanh:
+    all 8192 (n, c) outputs against the oracle."""
     inp = _full_inputs(5)
+    ref = _full_ref(5)
     m = fc()
     m.set_variant(variant)
     try:
         y = m.fc_convT2d_pool_mean(_dev(inp["x"]), _dev(inp["w"]), _dev(inp["b"]))
         assert m.get_last_device_error() == 0
-        ynp = y.cpu().numpy().reshape(128, 64)
+        got = y.cpu().numpy()
     finally:
         m.set_variant("auto")
-    rng = np.random.default_rng(5)
-    pairs = [(0, 0), (127, 63)] + [(int(rng.integers(128)), int(rng.integers(64)))
-                                   for _ in range(14)]
-    ref = oracle.convT_pool_mean_points(inp["x"], inp["w"], inp["b"], pairs)
-    got = np.array([ynp[n, c] for n, c in pairs])
-    _check(got, ref, f"workload 5 sampled [{variant}]")
-    # every output is finite and inside tanh's range for clamped means
-    assert np.all(np.abs(ynp) <= np.tanh(1.0) + 1e-6)
+    use = _check_whole(got, ref, f"workload 5 every output [{variant}]")
+    print(f"workload 5 [{variant}] max tolerance use {use:.4f}")
+    # every output is inside tanh's range for clamped means
+    assert np.all(np.abs(got) <= np.tanh(1.0) + 1e-6)
+
+
+def test_workload5_deterministic_over_ten_calls():
+    """The pooled mean is reduced in a fixed order (per-tile partials, then
+    an index-order sum): ten calls on the full-size workload give bitwise
+    the same 8192 outputs, on every variant."""
+    inp = _full_inputs(5)
+    m = fc()
+    x, w, b = _dev(inp["x"]), _dev(inp["w"]), _dev(inp["b"])
+    for v in ["auto"] + VARIANTS:
+        m.set_variant(v)
+        try:
+            first = m.fc_convT2d_pool_mean(x, w, b).cpu().numpy()
+            for _ in range(9):
+                again = m.fc_convT2d_pool_mean(x, w, b).cpu().numpy()
+                np.testing.assert_array_equal(again, first, err_msg=f"[{v}]")
+            assert m.get_last_device_error() == 0
+        finally:
+            m.set_variant("auto")
 
 
 def test_f16_split_range_boundary():
