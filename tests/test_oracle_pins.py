@@ -297,6 +297,50 @@ def test_conv_dilation2_delta_kernel_shifts():
     np.testing.assert_array_equal(y3[0, 0], x3[0, 0, 2:7:2, 4:10:2, 2:9:2])
 
 
+@pytest.mark.parametrize("k,stride,pad,dil", [
+    (1, 1, 0, 1), (1, 3, 1, 1), (5, 1, 2, 1), (5, 3, 4, 2), (7, 1, 3, 1), (7, 4, 6, 3),
+    (4, 2, 1, 1), (2, 1, 0, 4), (3, 3, 2, 3), (6, 4, 5, 1)])
+def test_conv2d_general_layer_brute_force(k, stride, pad, dil):
+    """Kernel sizes 1..7 (odd and even), strides and dilations 1..4 and
+    paddings, against the independent loop: out (oh, ow) reads input
+    oh*stride + kh*dil - pad, extent (n + 2p - d(k-1) - 1)//s + 1."""
+    st = _rng(40 + k + 10 * stride + 100 * dil)
+    x = st.normal((2, 3, 13, 16))
+    w = st.uniform((4, 3, k, k), 0.4)
+    b = st.uniform((4,), 0.4)
+    got = oracle.conv_epi(x, w, b, (), stride=stride, pad=pad, dilation=dil)
+    ref = _brute_conv2d_dilated(x, w, b, stride, pad, dil)
+    assert got.shape == ref.shape
+    assert got.shape[2:] == (oracle.conv_out_extent(13, k, stride, pad, dil),
+                             oracle.conv_out_extent(16, k, stride, pad, dil))
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_conv_general_kernel_delta_and_pointwise():
+    """Closed forms at other kernel sizes: a 1x1 kernel is a matrix product
+    over channels at every pixel; a 7x7 delta tap at (kh, kw) with pad 3
+    shifts the input by (kh - 3, kw - 3); a 5x5x5 3-D delta at stride 2
+    subsamples."""
+    st = _rng(50)
+    x = st.normal((2, 5, 6, 7))
+    w = st.uniform((3, 5, 1, 1), 0.5)
+    y = oracle.conv_epi(x, w, None, ())
+    ref = np.einsum("oc,nchw->nohw", w[:, :, 0, 0].astype(np.float64), x.astype(np.float64))
+    np.testing.assert_allclose(y, ref, atol=1e-12)
+    w7 = np.zeros((1, 1, 7, 7), np.float32)
+    w7[0, 0, 1, 5] = 1.0
+    x1 = st.normal((1, 1, 9, 10))
+    y7 = oracle.conv_epi(x1, w7, None, (), pad=3)
+    ref7 = np.zeros((9, 10))
+    ref7[2:, :8] = x1[0, 0, :7, 2:]
+    np.testing.assert_array_equal(y7[0, 0], ref7)
+    x3 = st.normal((1, 1, 11, 12, 13))
+    w5 = np.zeros((1, 1, 5, 5, 5), np.float32)
+    w5[0, 0, 4, 0, 2] = 1.0
+    y3 = oracle.conv_epi(x3, w5, None, (), stride=2)
+    np.testing.assert_array_equal(y3[0, 0], x3[0, 0, 4:11:2, 0:8:2, 2:11:2])
+
+
 def test_conv_all_ones_closed_form():
     b = np.array([0.5, -1.0], dtype=np.float32)
     y2 = oracle.conv_epi(np.ones((1, 8, 5, 5), np.float32),
@@ -550,6 +594,29 @@ def test_convT_stride2_pool_mean_composition(op):
     out = oracle.convT_pool_mean(x, w, b, stride=2, pad=1, out_pad=op)
     np.testing.assert_allclose(out[:, :, 0, 0], ref, atol=1e-13)
     np.testing.assert_allclose(oracle.convT2d(x, w, b, 2, 1, op), y, atol=1e-12)
+
+
+@pytest.mark.parametrize("k,s,p,op", [(3, 3, 1, 2), (3, 4, 0, 3), (3, 2, 0, 1), (3, 2, 2, 0),
+                                      (5, 2, 2, 1), (1, 3, 0, 0), (7, 1, 3, 0), (4, 2, 1, 0),
+                                      (5, 1, 0, 0)])
+def test_convT_general_layer_scatter_and_pool_mean(k, s, p, op):
+    """The transposed conv at other kernel sizes, strides 1..4, paddings and
+    output paddings below the stride, against the independent scatter loop
+    (extent (H-1)s - 2p + k + op); then the 2x2 pool chain against a numpy
+    tail on that loop's output."""
+    st = _rng(60 + k + 10 * s + 100 * p + 1000 * op)
+    x = st.normal((2, 3, 5, 6))
+    w = st.uniform((3, 4, k, k), 0.4)
+    b = st.uniform((4,), 0.3)
+    y = _brute_convT(x, w, b, s, p, op)
+    assert y.shape[2:] == (oracle.convT_out_extent(5, k, s, p, op),
+                           oracle.convT_out_extent(6, k, s, p, op))
+    np.testing.assert_allclose(oracle.convT2d(x, w, b, s, p, op), y, atol=1e-12)
+    Hp, Wp = y.shape[2] // 2, y.shape[3] // 2
+    pooled = y[:, :, :2 * Hp, :2 * Wp].reshape(2, 4, Hp, 2, Wp, 2).max(axis=(3, 5))
+    ref = np.tanh(np.clip(pooled, -1, 1).mean(axis=(2, 3)))
+    out = oracle.convT_pool_mean(x, w, b, stride=s, pad=p, out_pad=op)
+    np.testing.assert_allclose(out[:, :, 0, 0], ref, atol=1e-13)
 
 
 @pytest.mark.parametrize("pool", [(3, 2), (2, 1), (3, 3), (4, 2)])
