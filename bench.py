@@ -309,6 +309,7 @@ def run_ours(args):
         dist.barrier()
     fc.lib()
     fc.set_variant(args.variant)
+    fc.set_staging(args.staging)
     peaks = load_peaks()
     stream = torch.cuda.current_stream(dev)
 
@@ -483,6 +484,7 @@ def run_ours(args):
             "config": {"workload": " + ".join(synth.WORKLOADS[w]["name"] for w in WORKLOADS),
                        "l2": "flushed by a 256 MiB write before every workload call (outside events)",
                        "variants": {synth.WORKLOADS[w]["name"]: variants[w] for w in WORKLOADS},
+                       "staging": args.staging,
                        "per_workload": per_cfg,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof, "clocks": clocks, "gpu_launches": n_launch,
@@ -729,6 +731,147 @@ def measure_e2e(args, fc, host, dev, stream, chain4_host, chunk=16):
             "pipeline": f"chunks of {chunk} images on copy-in / compute / copy-out streams"}
 
 
+# ------------------------------------------------------- variant table
+# (entry, dims) per shape: entry 0 conv2d / 1 conv3d with
+# (N, C, [D,] H, W, CO, k, stride, pad, dilation, channels_last), entry 2
+# the pooled transposed conv with (N, C, H, W, CO, k, stride, pad, out_pad,
+# pool window, pool stride).  The five workloads, smaller and larger
+# neighbours, other channel counts, and the widened forms.
+TABLE_SHAPES = (
+    [(0, (n, c, h, w, co, 3, 1, 0, 1, 0)) for (n, c, h, w, co) in [
+        (4, 8, 32, 32, 64), (2, 3, 9, 37, 10), (16, 8, 64, 64, 64), (32, 8, 128, 128, 64),
+        (128, 8, 128, 128, 64), (1, 64, 32, 32, 64), (8, 64, 64, 64, 64), (2, 16, 128, 128, 128),
+        (1, 256, 16, 16, 256), (64, 32, 64, 64, 64)]]
+    + [(0, (n, c, h, w, co, 3, 2, 0, 1, 0)) for (n, c, h, w, co) in [
+        (4, 8, 32, 32, 64), (128, 8, 128, 128, 64), (8, 64, 64, 64, 64)]]
+    + [(0, (n, c, h, w, co, 3, 1, 2, 2, 0)) for (n, c, h, w, co) in [
+        (4, 8, 32, 32, 64), (128, 8, 128, 128, 64)]]
+    + [(0, (n, c, h, w, co, 3, 1, 1, 1, 1)) for (n, c, h, w, co) in [
+        (4, 8, 32, 32, 64), (128, 8, 128, 128, 64), (8, 64, 64, 64, 64)]]
+    + [(1, (n, c, d, h, w, co, 3, 1, 0, 1, 0)) for (n, c, d, h, w, co) in [
+        (1, 8, 5, 10, 12, 64), (8, 8, 16, 64, 64, 64), (128, 8, 16, 64, 64, 64),
+        (2, 16, 8, 32, 32, 32), (4, 64, 8, 16, 16, 64)]]
+    + [(1, (8, 8, 16, 64, 64, 64, 3, 2, 1, 1, 0)), (1, (8, 8, 16, 64, 64, 64, 3, 1, 1, 1, 1))]
+    + [(2, (n, c, h, w, co, 3, 1, 1, 0, 2, 2)) for (n, c, h, w, co) in [
+        (2, 64, 32, 32, 64), (16, 64, 64, 64, 64), (128, 64, 256, 256, 64), (2, 5, 7, 10, 3),
+        (4, 16, 64, 64, 64)]]
+    + [(2, (2, 64, 16, 20, 64, 3, 2, 1, 1, 2, 2)), (2, (128, 64, 128, 128, 64, 3, 2, 1, 1, 2, 2))]
+    + [(2, (16, 64, 256, 256, 64, 3, 1, 1, 0, 3, 2)), (2, (2, 16, 17, 21, 64, 3, 1, 1, 0, 3, 2))]
+)
+# candidates in the table's column order
+TABLE_COLS = (("ffma", "loads"), ("tc_tf32x3", "loads"), ("tc_tf32x3", "tma"),
+              ("tc_f16x3", "loads"), ("tc_f16x3", "tma"))
+
+
+def _table_case(fc, dev, entry, dims):
+    """Device tensors and a call for one table shape; MACs as the library
+    counts them for its selection."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    rnd = lambda *sh: torch.randn(*sh, generator=g).to(dev)
+    if entry in (0, 1):
+        if entry == 0:
+            N, C, H, W, CO, k, st, pad, dil, cl = dims
+            D = 1
+        else:
+            N, C, D, H, W, CO, k, st, pad, dil, cl = dims
+        ext = lambda n: (n + 2 * pad - dil * (k - 1) - 1) // st + 1
+        Do = ext(D) if entry == 1 else 1
+        Ho, Wo = ext(H), ext(W)
+        xs = (N, C, H, W) if entry == 0 else (N, C, D, H, W)
+        if cl:
+            xs = (xs[0],) + xs[2:] + (C,)
+        x = rnd(*xs)
+        w = rnd(*((CO, C) + (k,) * (2 if entry == 0 else 3))) * 0.1
+        b = rnd(CO) * 0.1
+        ops = (("relu",), ("hardswish",)) if entry == 0 else (
+            ("leaky_relu", 0.2), ("add_channel", rnd(CO)), ("clamp", -1.0, 1.0), ("gelu_erf",))
+        f = {(0, 0): fc.fc_conv2d_epi, (0, 1): fc.fc_conv2d_epi_nhwc,
+             (1, 0): fc.fc_conv3d_epi, (1, 1): fc.fc_conv3d_epi_ndhwc}[(entry, cl)]
+        call = lambda: f(x, w, b, ops, pad=pad, stride=st, dilation=dil)
+        macs = N * CO * Do * Ho * Wo * C * (k ** (2 if entry == 0 else 3))
+        key = dict(entry=entry, k=k, stride=st, dil=dil, cl=cl, pool_general=0, C=C, CO=CO)
+    else:
+        N, C, H, W, CO, k, st, pad, op, pk, ps = dims
+        x = rnd(N, C, H, W)
+        w = rnd(C, CO, k, k) * 0.05
+        b = rnd(CO) * 0.1
+        call = lambda: fc.fc_convT2d_pool_mean(x, w, b, stride=st, pad=pad, out_pad=op,
+                                               pool=(pk, ps))
+        if st == 2 and k == 3 and pad == 1 and (pk, ps) == (2, 2):  # per parity class
+            macs = N * C * CO * H * W * k * k
+        else:
+            Ho, Wo = (H - 1) * st - 2 * pad + k + op, (W - 1) * st - 2 * pad + k + op
+            macs = N * CO * Ho * Wo * C * k * k
+        key = dict(entry=2, k=k, stride=st, dil=1, cl=0, pool_general=int((pk, ps) != (2, 2)),
+                   C=C, CO=CO)
+    key["macs"] = float(macs)
+    return call, key
+
+
+def run_variant_table(args):
+    """Times every (variant, input staging) pair on TABLE_SHAPES (median
+    main-kernel time from the library's own event pairs, L2 flushed before
+    each call) and writes the table the automatic choice compiles in."""
+    import torch
+    import convolution_epilogue_gb300 as fc
+    from convolution_epilogue_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    entry_prof = {0: 0, 1: 1, 2: 2}
+    rows = []
+    for entry, dims in TABLE_SHAPES:
+        call, key = _table_case(fc, dev, entry, dims)
+        ms = []
+        for variant, staging in TABLE_COLS:
+            fc.set_variant(variant)
+            fc.set_staging(staging)
+            try:
+                call()
+                torch.cuda.synchronize()
+            except fc.FcError:
+                ms.append(-1.0)
+                continue
+            if variant != "ffma" and fc.last_staging() != staging:
+                ms.append(-1.0)  # this plan cannot stage that way
+                continue
+            times = []
+            for _ in range(args.table_reps):
+                flush.zero_()
+                fc.profile_reset()
+                fc.profile_enable(True)
+                call()
+                fc.profile_enable(False)
+                t, n = fc.profile_read(entry_prof[entry])
+                times.append(t / max(n, 1))
+            if fc.get_last_device_error() != 0:
+                raise RuntimeError(f"device status word set at {dims} [{variant}/{staging}]")
+            ms.append(float(statistics.median(times)))
+        fc.set_variant("auto")
+        fc.set_staging("auto")
+        rows.append(dict(key, dims=list(dims), ms=ms))
+        print(json.dumps(rows[-1]), flush=True)
+    out = {"columns": [f"{v}/{s}" for v, s in TABLE_COLS], "rows": rows,
+           "gpu": torch.cuda.get_device_name(0)}
+    with open(args.variant_table, "w") as f:
+        json.dump(out, f, indent=1)
+    with open(os.path.splitext(args.variant_table)[0] + ".h", "w") as f:
+        f.write(variant_table_header(out))
+    return 0
+
+
+def variant_table_header(tab) -> str:
+    """The C table for fc_variant_table.h from a measured table."""
+    lines = []
+    for r in tab["rows"]:
+        ms = ", ".join(f"{m:.5f}f" if m >= 0 else "-1.f" for m in r["ms"])
+        lines.append(f"    {{{r['entry']}, {r['k']}, {r['stride']}, {r['dil']}, {r['cl']}, "
+                     f"{r['pool_general']}, {r['macs']:.1f}, {r['C']}, {r['CO']}, {{{ms}}}}},"
+                     f"  // {r['dims']}")
+    return "\n".join(lines) + "\n"
+
+
 def run_profile_case(args):
     """Run one workload (optionally at a smaller batch) `--profile-reps`
     times through the public API and exit: the command profilers wrap."""
@@ -742,6 +885,7 @@ def run_profile_case(args):
     inp = synth.make_inputs(wid, first_images=nb)
     d = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
     fc.set_variant(args.variant)
+    fc.set_staging(args.staging)
     for _ in range(args.profile_reps):
         if spec["kind"] == "conv2d":
             y = fc.fc_conv2d_epi(d["x"], d["w"], d["b"], CHAIN_RH)
@@ -766,11 +910,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tc_tf32x3", "tc_f16x3"])
+    ap.add_argument("--staging", default="auto", choices=["auto", "tma", "loads"],
+                    help="input staging of the tensor-core variants")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--cpu-scale", type=int, default=128)
     ap.add_argument("--ref-scale", type=int, default=2)
+    ap.add_argument("--variant-table", default="",
+                    help="time every variant / staging on the table's shapes; write JSON and .h here")
+    ap.add_argument("--table-reps", type=int, default=7)
     ap.add_argument("--profile-workload", type=int, default=0,
                     help="run only this workload (1..5) --profile-reps times, for profilers")
     ap.add_argument("--profile-batch", type=int, default=0)
@@ -778,6 +927,8 @@ def main():
     args = ap.parse_args()
     if args.profile_workload:
         return run_profile_case(args)
+    if args.variant_table:
+        return run_variant_table(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -33,7 +33,8 @@ MAX_OPS = 8
 # every symbol include/fusedconv.h declares
 EXPORTS = ("fc_conv2d_epi", "fc_conv2d_epi_noalloc", "fc_conv3d_epi", "fc_convT2d_pool_mean",
            "fc_conv2d_epi_nhwc", "fc_conv3d_epi_ndhwc",
-           "fc_workspace_bytes", "fc_set_variant", "fc_last_variant",
+           "fc_workspace_bytes", "fc_set_variant", "fc_set_staging", "fc_select_variant",
+           "fc_last_variant", "fc_last_staging",
            "fc_last_launch_count", "fc_status_string",
            "fc_get_last_device_error", "fc_version", "fc_profile_enable",
            "fc_profile_read", "fc_profile_reset", "fc_wait_report",
@@ -90,7 +91,12 @@ def lib():
             L.fc_workspace_bytes.argtypes = [I, ctypes.POINTER(I)]
             L.fc_set_variant.restype = I
             L.fc_set_variant.argtypes = [I]
+            L.fc_set_staging.restype = I
+            L.fc_set_staging.argtypes = [I]
+            L.fc_select_variant.restype = I
+            L.fc_select_variant.argtypes = [I, ctypes.POINTER(I)]
             L.fc_last_variant.restype = I
+            L.fc_last_staging.restype = I
             L.fc_last_launch_count.restype = I
             L.fc_status_string.restype = ctypes.c_char_p
             L.fc_status_string.argtypes = [I]
@@ -212,6 +218,27 @@ def _workspace(nbytes, device):
 
 def set_variant(name: str = "auto"):
     _check(lib().fc_set_variant(VARIANTS[name]), "fc_set_variant")
+
+
+def select_variant(entry: int, dims) -> str:
+    """The variant a call would run for a problem (fc_select_variant);
+    "none" for an invalid or unsupported one.  Needs no device."""
+    arr = (ctypes.c_int * len(dims))(*[int(d) for d in dims])
+    return VARIANT_NAMES.get(int(lib().fc_select_variant(int(entry), arr)), "none")
+
+
+STAGING = {"auto": -1, "loads": 0, "tma": 1}
+
+
+def set_staging(mode: str = "auto"):
+    """Input staging of the tensor-core variants: "auto" (chosen per shape
+    from the measured table), "tma" (tensor copies where the plan allows
+    them) or "loads" (producer register loads)."""
+    _check(lib().fc_set_staging(STAGING[mode]), "fc_set_staging")
+
+
+def last_staging() -> str:
+    return "tma" if lib().fc_last_staging() == 1 else "loads"
 
 
 def last_variant() -> str:

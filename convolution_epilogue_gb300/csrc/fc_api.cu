@@ -2,10 +2,12 @@
 // variant selection, workspace layout and launches.  Nothing here computes
 // a conv value; every step of the path runs in the kernels.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
 #include "fc_internal.h"
+#include "fc_variant_table.h"
 
 namespace fc {
 
@@ -22,8 +24,13 @@ constexpr int kMaxDevices = 64;
 unsigned int *g_status_ptr[kMaxDevices];
 
 int g_variant_override = FC_VARIANT_AUTO;
+// Input staging of the tensor-core variants: -1 chosen per shape with the
+// variant (measured table), 0 register loads, 1 tensor copies where the
+// plan allows them.
+int g_staging_override = -1;
 thread_local int t_last_variant = 0;
 thread_local int t_last_launches = 0;
+thread_local int t_last_staging = 0;
 
 // ---- benchmark profiling: event pairs around main kernels
 constexpr int kMaxProf = 4096;
@@ -129,16 +136,73 @@ fc_status decode_pool(const fc_epilogue *epi, EpiDev *e, float *lo, float *hi, i
 
 bool fits_int32(long long v) { return v >= 0 && v < (1LL << 31); }
 
-// Automatic variant choice from measured times on GB300 (see the
-// benchmark's per-variant table): the tensor-core f16-split path wins once
-// there is enough work; tiny problems go to whichever finished first.
-int auto_variant(const ConvProblem &p) {
+bool variant_supported(const ConvProblem &p, int v) {
+  if (v == FC_VARIANT_TC_TF32X3) return !p.gen && tc_supported(p, 0);
+  if (v == FC_VARIANT_TC_F16X3) return !p.gen && tc_supported(p, 1);
+  if (v == FC_VARIANT_FFMA)  // the fixed-size kernels, else the general one (no channels-last form)
+    return !p.cl && (ffma_fixed_supported(p) || ffma_gen_channel_chunk(p) > 0);
+  return false;
+}
+
+// Built-in rule, used when the measured table has no row of the problem's
+// category: the tensor-core f16-split path once there is enough work.
+int rule_variant(const ConvProblem &p) {
+  if (p.gen) return FC_VARIANT_FFMA;
   if (p.subpix || p.cl) return tc_supported(p, 1) ? FC_VARIANT_TC_F16X3 : FC_VARIANT_TC_TF32X3;
   if (p.pool && (p.pk != 2 || p.ps != 2)) return FC_VARIANT_FFMA;  // general pool windows
   const double macs = (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
   if (tc_supported(p, 1) && macs >= 4.0e8) return FC_VARIANT_TC_F16X3;
   if (tc_supported(p, 0) && macs >= 4.0e8) return FC_VARIANT_TC_TF32X3;
   return FC_VARIANT_FFMA;
+}
+
+double problem_macs(const ConvProblem &p) {
+  if (p.subpix)  // stride-2 transposed conv: each input pixel meets each tap once
+    return (double)p.N * p.C * p.CO * p.H * p.W * p.KH * p.KW;
+  return (double)p.N * p.CO * p.Do * p.Ho * p.Wo * p.C * p.KD * p.KH * p.KW;
+}
+
+// Automatic choice from measured times (fc_variant_table.h): among the
+// table rows of the problem's category (entry point, kernel size, stride,
+// dilation, layout, pool window), the one nearest in log2 MACs and log2
+// channel counts; its (variant, staging) pairs in order of measured time,
+// the first the problem supports.  Returns the variant and sets *staging.
+int auto_choice(const ConvProblem &p, int *staging) {
+  *staging = 1;
+  if (p.gen) return FC_VARIANT_FFMA;  // only the general kernel computes it
+  const int entry = p.pool ? 2 : p.entry;  // 0 conv2d, 1 conv3d, 2 pooled
+  const int stride = p.pool ? p.tstride : p.stride;
+  const int pgen = p.pool && (p.pk != 2 || p.ps != 2);
+  const double lm = log2(problem_macs(p) + 1.0), lc = log2((double)p.C), lco = log2((double)p.CO);
+  int best = -1;
+  double bd = 0.0;
+  const int nrows = (int)(sizeof(kVariantTable) / sizeof(kVariantTable[0]));
+  for (int i = 0; i < nrows; ++i) {
+    const VariantRow &r = kVariantTable[i];
+    if (r.entry != entry || r.stride != stride || r.dil != p.dil || r.cl != p.cl ||
+        r.pool_general != pgen || r.k != p.KH)
+      continue;
+    const double d = fabs(lm - log2(r.macs + 1.0)) + 0.5 * fabs(lc - log2((double)r.C)) +
+                     0.5 * fabs(lco - log2((double)r.CO));
+    if (best < 0 || d < bd) { best = i; bd = d; }
+  }
+  if (best < 0) return rule_variant(p);
+  const VariantRow &r = kVariantTable[best];
+  // candidates: (FFMA), (TF32, loads), (TF32, tensor copies), (F16, loads), (F16, copies)
+  const int cv[kTableCols] = {FC_VARIANT_FFMA, FC_VARIANT_TC_TF32X3, FC_VARIANT_TC_TF32X3,
+                              FC_VARIANT_TC_F16X3, FC_VARIANT_TC_F16X3};
+  const int cs[kTableCols] = {1, 0, 1, 0, 1};
+  int pick = -1;
+  for (int i = 0; i < kTableCols; ++i) {
+    if (r.ms[i] < 0.f) continue;  // refused when measured
+    ConvProblem q = p;
+    q.staging = cs[i];
+    if (!variant_supported(q, cv[i])) continue;
+    if (pick < 0 || r.ms[i] < r.ms[pick]) pick = i;
+  }
+  if (pick < 0) return rule_variant(p);
+  *staging = cs[pick];
+  return cv[pick];
 }
 
 fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
@@ -150,11 +214,12 @@ fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
   WsLayout L = ws_layout(p);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < L.total)
     return FC_ERR_WORKSPACE;
-  int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : auto_variant(p);
-  if ((v == FC_VARIANT_TC_TF32X3 && !tc_supported(p, 0)) ||
-      (v == FC_VARIANT_TC_F16X3 && !tc_supported(p, 1)) ||
-      (v == FC_VARIANT_FFMA && (p.subpix || p.cl)))  // no parity-class or channels-last form
-    return FC_ERR_UNSUPPORTED;
+  int staging = 1;
+  const int va = auto_choice(p, &staging);
+  const int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : va;
+  if (g_variant_override != FC_VARIANT_AUTO && v != va) staging = 1;  // the override's own default
+  p.staging = g_staging_override >= 0 ? g_staging_override : staging;
+  if (!variant_supported(p, v)) return FC_ERR_UNSUPPORTED;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int launches = 0;
   cudaError_t e;
@@ -166,6 +231,7 @@ fc_status run(ConvProblem &p, void *ws, size_t ws_bytes, void *stream) {
   }
   t_last_variant = v;
   t_last_launches = launches;
+  t_last_staging = (v != FC_VARIANT_FFMA && tc_uses_tma(p, v == FC_VARIANT_TC_F16X3 ? 1 : 0)) ? 1 : 0;
   return FC_OK;
 }
 
@@ -211,6 +277,9 @@ WsLayout ws_layout(const ConvProblem &p) {
     L.partial_bytes = sizeof(float) * (size_t)p.N * T * p.CO;
   }
   off = align256(off + L.partial_bytes);
+  L.wmax = off;
+  L.wmax_bytes = sizeof(float) * kMaxPackBlocks;
+  off = align256(off + L.wmax_bytes);
   L.total = off;
   return L;
 }
@@ -271,39 +340,72 @@ fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, int W,
                        scratch, kNoAllocScratchBytes, stream);
 }
 
+// Layer parameters the entry points accept (every variant that supports a
+// shape computes the same values; the fixed-size kernels take kernel size 3,
+// stride and dilation 1 or 2, the general CUDA-core kernel the rest).
+static constexpr int kMaxK = 7, kMaxStride = 4, kMaxDil = 4, kMaxPad = 64;
+
+// Elements per image must stay below 2^31 (per-image offsets are 32-bit in
+// places); whole tensors may be larger (64-bit offsets).
+static bool image_fits(long long v) { return v >= 0 && v < (1LL << 31); }
+
+// Validates a conv2d / conv3d call and fills the problem.  `check_ptrs`:
+// also the pointers (a real call, not a query).
+static fc_status conv_problem(const float *x, int N, int C_in, int D, int H, int W, const float *w,
+                       int C_out, int kD, int kH, int kW, int stride, int pad, int dilation,
+                       const fc_epilogue *epi, float *y, int cl, int d3, bool check_ptrs,
+                       ConvProblem *out) {
+  if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 || kH < 1 ||
+      kW < 1 || stride < 1 || pad < 0 || dilation < 1)
+    return FC_ERR_INVALID_ARG;
+  if (stride > kMaxStride || dilation > kMaxDil || kD > kMaxK || kH > kMaxK || kW > kMaxK ||
+      pad > kMaxPad)
+    return FC_ERR_UNSUPPORTED;
+  const int pd = d3 ? pad : 0;
+  const int spanD = dilation * (kD - 1) + 1, spanH = dilation * (kH - 1) + 1,
+            spanW = dilation * (kW - 1) + 1;
+  if (D + 2 * pd < spanD || H + 2 * pad < spanH || W + 2 * pad < spanW) return FC_ERR_INVALID_ARG;
+  const int Do = (D + 2 * pd - spanD) / stride + 1, Ho = (H + 2 * pad - spanH) / stride + 1,
+            Wo = (W + 2 * pad - spanW) / stride + 1;
+  if (Do < 1 || Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
+  if (!image_fits((long long)C_in * D * H * W) || !image_fits((long long)C_out * Do * Ho * Wo) ||
+      !image_fits((long long)C_out * C_in * kD * kH * kW))
+    return FC_ERR_UNSUPPORTED;
+  ConvProblem &p = *out;
+  p = ConvProblem{};
+  fc_status s = decode_eltwise(epi, &p.epi, &p.chain);
+  if (s != FC_OK) return s;
+  if (check_ptrs && N > 0) {
+    if (!x || !w || !y) return FC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
+  }
+  p.x = x; p.w = w; p.y = y;
+  p.N = N; p.C = C_in; p.D = D; p.H = H; p.W = W;
+  p.CO = C_out; p.KD = kD; p.KH = kH; p.KW = kW;
+  p.pad_d = pd; p.pad = pad;
+  p.stride = stride;
+  p.dil = dilation;
+  p.cl = cl;
+  p.Do = Do; p.Ho = Ho; p.Wo = Wo;
+  p.wlayout = 0;
+  p.entry = d3 ? 1 : 0;
+  p.tstride = 1;
+  // the tensor-core kernel takes square odd kernels up to 7 (3D: cubic up
+  // to 5) at stride / dilation <= 2; the rest only the general CUDA-core one
+  p.gen = !(kH == kW && (kH & 1) && (d3 ? (kD == kH && kD <= 5) : kD == 1) && stride <= 2 &&
+            dilation <= 2);
+  return FC_OK;
+}
+
 static fc_status conv2d_impl(const float *x, int N, int C_in, int H, int W, const float *w,
                              int C_out, int kH, int kW, int stride, int pad, int dilation,
                              const fc_epilogue *epi, float *y, void *ws, size_t ws_bytes,
                              void *stream, int cl) {
-  if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || kH < 1 || kW < 1 ||
-      stride < 1 || pad < 0 || dilation < 1)
-    return FC_ERR_INVALID_ARG;
-  if (stride > 2 || dilation > 2 || kH != 3 || kW != 3 || pad > 2 * dilation)
-    return FC_ERR_UNSUPPORTED;
-  const int spanH = dilation * (kH - 1) + 1, spanW = dilation * (kW - 1) + 1;
-  if (H + 2 * pad < spanH || W + 2 * pad < spanW) return FC_ERR_INVALID_ARG;
-  const int Ho = (H + 2 * pad - spanH) / stride + 1, Wo = (W + 2 * pad - spanW) / stride + 1;
-  if (Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
-  if (!fits_int32((long long)N * C_in * H * W) ||
-      !fits_int32((long long)N * C_out * Ho * Wo) ||
-      !fits_int32((long long)C_out * C_in * kH * kW))
-    return FC_ERR_UNSUPPORTED;
-  if (N == 0) return FC_OK;
-  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
-  ConvProblem p{};
-  fc_status s = decode_eltwise(epi, &p.epi, &p.chain);
+  ConvProblem p;
+  const fc_status s = conv_problem(x, N, C_in, 1, H, W, w, C_out, 1, kH, kW, stride, pad,
+                                   dilation, epi, y, cl, 0, true, &p);
   if (s != FC_OK) return s;
-  p.x = x; p.w = w; p.y = y;
-  p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
-  p.CO = C_out; p.KD = 1; p.KH = kH; p.KW = kW;
-  p.pad_d = 0; p.pad = pad;
-  p.stride = stride;
-  p.dil = dilation;
-  p.cl = cl;
-  p.Do = 1; p.Ho = Ho; p.Wo = Wo;
-  p.wlayout = 0;
-  p.entry = 0;
+  if (N == 0) return FC_OK;
   return run(p, ws, ws_bytes, stream);
 }
 
@@ -326,37 +428,11 @@ static fc_status conv3d_impl(const float *x, int N, int C_in, int D, int H, int 
                              const float *w, int C_out, int kD, int kH, int kW, int stride,
                              int pad, int dilation, const fc_epilogue *epi, float *y, void *ws,
                              size_t ws_bytes, void *stream, int cl) {
-  if (N < 0 || C_in < 1 || C_out < 1 || D < 1 || H < 1 || W < 1 || kD < 1 ||
-      kH < 1 || kW < 1 || stride < 1 || pad < 0 || dilation < 1)
-    return FC_ERR_INVALID_ARG;
-  if (stride > 2 || dilation > 2 || kD != 3 || kH != 3 || kW != 3 || pad > 2 * dilation)
-    return FC_ERR_UNSUPPORTED;
-  const int span = dilation * 2 + 1;  // kD = kH = kW = 3
-  if (D + 2 * pad < span || H + 2 * pad < span || W + 2 * pad < span)
-    return FC_ERR_INVALID_ARG;
-  const int Do = (D + 2 * pad - span) / stride + 1, Ho = (H + 2 * pad - span) / stride + 1,
-            Wo = (W + 2 * pad - span) / stride + 1;
-  if (Do < 1 || Ho < 1 || Wo < 1) return FC_ERR_INVALID_ARG;
-  if (!fits_int32((long long)N * C_in * D * H * W) ||
-      !fits_int32((long long)N * C_out * Do * Ho * Wo) ||
-      !fits_int32((long long)C_out * C_in * kD * kH * kW))
-    return FC_ERR_UNSUPPORTED;
-  if (N == 0) return FC_OK;
-  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
-  ConvProblem p{};
-  fc_status s = decode_eltwise(epi, &p.epi, &p.chain);
+  ConvProblem p;
+  const fc_status s = conv_problem(x, N, C_in, D, H, W, w, C_out, kD, kH, kW, stride, pad,
+                                   dilation, epi, y, cl, 1, true, &p);
   if (s != FC_OK) return s;
-  p.x = x; p.w = w; p.y = y;
-  p.N = N; p.C = C_in; p.D = D; p.H = H; p.W = W;
-  p.CO = C_out; p.KD = kD; p.KH = kH; p.KW = kW;
-  p.pad_d = pad; p.pad = pad;
-  p.stride = stride;
-  p.dil = dilation;
-  p.cl = cl;
-  p.Do = Do; p.Ho = Ho; p.Wo = Wo;
-  p.wlayout = 0;
-  p.entry = 1;
+  if (N == 0) return FC_OK;
   return run(p, ws, ws_bytes, stream);
 }
 
@@ -376,47 +452,42 @@ fc_status fc_conv3d_epi_ndhwc(const float *x, int N, int C_in, int D, int H, int
                      ws, ws_bytes, stream, 1);
 }
 
-fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
-                               const float *w, int C_out, int k, int stride,
-                               int pad, int out_pad, const fc_epilogue *epi,
-                               float *y, void *ws, size_t ws_bytes,
-                               void *stream) {
-  if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || k < 1 || stride < 1 ||
-      pad < 0 || out_pad < 0)
+static fc_status convT_problem(const float *x, int N, int C_in, int H, int W, const float *w,
+                        int C_out, int k, int stride, int pad, int out_pad, const fc_epilogue *epi,
+                        float *y, bool check_ptrs, ConvProblem *out) {
+  if (N < 0 || C_in < 1 || C_out < 1 || H < 1 || W < 1 || k < 1 || stride < 1 || pad < 0 ||
+      out_pad < 0)
     return FC_ERR_INVALID_ARG;
-  if (k != 3 || pad != 1 || !((stride == 1 && out_pad == 0) || (stride == 2 && out_pad <= 1)))
+  // output padding below the stride (it selects among the output sizes a
+  // stride > 1 allows)
+  if (out_pad >= stride) return FC_ERR_INVALID_ARG;
+  if (k > kMaxK || stride > kMaxStride || pad > kMaxPad) return FC_ERR_UNSUPPORTED;
+  // transposed-conv output extent (H-1)*s - 2p + k + op
+  const long long Hl = (long long)(H - 1) * stride - 2LL * pad + k + out_pad;
+  const long long Wl = (long long)(W - 1) * stride - 2LL * pad + k + out_pad;
+  if (Hl < 1 || Wl < 1) return FC_ERR_INVALID_ARG;
+  if (!image_fits((long long)C_in * H * W) || !image_fits(Hl * Wl) ||
+      !image_fits((long long)C_out * C_in * k * k))
     return FC_ERR_UNSUPPORTED;
-  // transposed-conv output extent (H-1)*s - 2p + k + op: H at stride 1,
-  // 2H - 1 + op at stride 2
-  const int Ho = (H - 1) * stride - 2 * pad + k + out_pad;
-  const int Wo = (W - 1) * stride - 2 * pad + k + out_pad;
-  if (Ho < 2 || Wo < 2) return FC_ERR_INVALID_ARG;
-  if (!fits_int32((long long)N * C_in * H * W) ||
-      !fits_int32((long long)C_out * C_in * k * k))
-    return FC_ERR_UNSUPPORTED;
-  ConvProblem p{};
+  const int Ho = (int)Hl, Wo = (int)Wl;
+  ConvProblem &p = *out;
+  p = ConvProblem{};
   float lo = 0.f, hi = 0.f;
   int pk = 2, ps = 2;
   fc_status s = decode_pool(epi, &p.epi, &lo, &hi, &pk, &ps);
   if (s != FC_OK) return s;
-  if ((pk != 2 || ps != 2) && stride != 1) return FC_ERR_UNSUPPORTED;
   if (Ho < pk || Wo < pk) return FC_ERR_INVALID_ARG;  // no full pooling window
+  if (check_ptrs && N > 0) {
+    if (!x || !w || !y) return FC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
+  }
   p.pk = pk;
   p.ps = ps;
-  if (N == 0) return FC_OK;
-  if (!x || !w || !y) return FC_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FC_ERR_ALIGNMENT;
   p.x = x; p.w = w; p.y = y;
   p.N = N; p.C = C_in; p.D = 1; p.H = H; p.W = W;
   p.CO = C_out; p.KD = 1; p.KH = k; p.KW = k;
-  if (stride == 1) {
-    // the equivalent conv: swapped + flipped weights, padding k - 1 - p
-    p.pad_d = 0; p.pad = k - 1 - pad;
-  } else {
-    // computed per output parity class on the input grid (tensor cores only)
-    p.pad_d = 0; p.pad = 0;
-    p.subpix = 1;
-  }
+  p.tstride = stride; p.tpad = pad; p.top = out_pad;
+  p.pad_d = 0;
   p.stride = 1;
   p.dil = 1;
   p.Do = 1; p.Ho = Ho; p.Wo = Wo;
@@ -425,6 +496,31 @@ fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
   p.ht_lo = lo; p.ht_hi = hi;
   p.chain = CHAIN_NONE;
   p.entry = 2;
+  if (stride == 1 && pad <= k - 1) {
+    // the equivalent conv: swapped + flipped weights, padding k - 1 - p
+    p.pad = k - 1 - pad;
+    p.gen = (k & 1) == 0;  // the tensor-core kernel takes odd kernel sizes
+  } else if (stride == 2 && k == 3 && pad == 1 && pk == 2 && ps == 2) {
+    // per output parity class on the input grid (tensor cores); the
+    // general CUDA-core kernel for the CUDA-core variant
+    p.pad = 0;
+    p.subpix = 1;
+  } else {
+    p.gen = 1;
+  }
+  return FC_OK;
+}
+
+fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
+                               const float *w, int C_out, int k, int stride,
+                               int pad, int out_pad, const fc_epilogue *epi,
+                               float *y, void *ws, size_t ws_bytes,
+                               void *stream) {
+  ConvProblem p;
+  const fc_status s = convT_problem(x, N, C_in, H, W, w, C_out, k, stride, pad, out_pad, epi, y,
+                                    true, &p);
+  if (s != FC_OK) return s;
+  if (N == 0) return FC_OK;
   return run(p, ws, ws_bytes, stream);
 }
 
@@ -450,55 +546,96 @@ fc_status fc_pool_mean_tail(const float *x, int N, int C, int H, int W, int k, i
   return FC_OK;
 }
 
+// An epilogue holding the pooled entry's chain for a window / stride.
+static fc_epilogue pool_chain(int pk, int ps) {
+  fc_epilogue e;
+  memset(&e, 0, sizeof(e));
+  e.n_ops = 4;
+  if (pk == 2 && ps == 2) {
+    e.ops[0].kind = FC_EPI_MAXPOOL2X2;
+  } else {
+    e.ops[0].kind = FC_EPI_MAXPOOL;
+    e.ops[0].a = (float)pk;
+    e.ops[0].b = (float)ps;
+  }
+  e.ops[1].kind = FC_EPI_HARDTANH;
+  e.ops[1].a = -1.0f;
+  e.ops[1].b = 1.0f;
+  e.ops[2].kind = FC_EPI_MEAN_HW;
+  e.ops[3].kind = FC_EPI_TANH;
+  return e;
+}
+
 size_t fc_workspace_bytes(int entry, const int *d) {
   if (!d) return 0;
-  ConvProblem p{};
-  p.stride = 1;  // the workspace depends on neither the stride nor the dilation
-  p.dil = 1;
+  ConvProblem p;
   switch (entry) {
-    case 0:
-      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
-      p.KD = 1; p.KH = p.KW = d[5]; p.pad = d[6];
-      p.Do = 1; p.Ho = p.H + 2 * p.pad - p.KH + 1; p.Wo = p.W + 2 * p.pad - p.KW + 1;
-      break;
-    case 1:
-      p.N = d[0]; p.C = d[1]; p.D = d[2]; p.H = d[3]; p.W = d[4]; p.CO = d[5];
-      p.KD = p.KH = p.KW = d[6]; p.pad = p.pad_d = d[7];
-      p.Do = p.D + 2 * p.pad - p.KD + 1; p.Ho = p.H + 2 * p.pad - p.KH + 1;
-      p.Wo = p.W + 2 * p.pad - p.KW + 1;
-      break;
-    case 2:
-      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
-      p.KD = 1; p.KH = p.KW = d[5]; p.pad = p.KH - 1 - d[6];
-      p.Do = 1; p.Ho = p.H - 1 - 2 * d[6] + p.KH; p.Wo = p.W - 1 - 2 * d[6] + p.KW;
-      p.pool = 1; p.wlayout = 1; p.pk = p.ps = 2;
-      break;
-    case 3:  // {N, C_in, H, W, C_out, k, pad, stride 1, out_pad 0, pool k, pool s}
-      if (d[7] != 1 || d[8] != 0 || d[9] < 1 || d[10] < 1) return 0;
-      p.N = d[0]; p.C = d[1]; p.D = 1; p.H = d[2]; p.W = d[3]; p.CO = d[4];
-      p.KD = 1; p.KH = p.KW = d[5]; p.pad = p.KH - 1 - d[6];
-      p.Do = 1; p.Ho = p.H - 1 - 2 * d[6] + p.KH; p.Wo = p.W - 1 - 2 * d[6] + p.KW;
-      p.pool = 1; p.wlayout = 1; p.pk = d[9]; p.ps = d[10];
-      if (p.Ho < p.pk || p.Wo < p.pk) return 0;
-      break;
+    case 0:  // {N, C_in, H, W, C_out, k, pad}: independent of stride and dilation
+      if (conv_problem(nullptr, d[0], d[1], 1, d[2], d[3], nullptr, d[4], 1, d[5], d[5], 1, d[6],
+                       1, nullptr, nullptr, 0, 0, false, &p) != FC_OK)
+        return 0;
+      return ws_layout(p).total;
+    case 1:  // {N, C_in, D, H, W, C_out, k, pad}
+      if (conv_problem(nullptr, d[0], d[1], d[2], d[3], d[4], nullptr, d[5], d[6], d[6], d[6], 1,
+                       d[7], 1, nullptr, nullptr, 0, 1, false, &p) != FC_OK)
+        return 0;
+      return ws_layout(p).total;
+    case 2: {  // {N, C_in, H, W, C_out, k, pad}, 2x2 pool: covers every stride / output padding
+      const fc_epilogue e = pool_chain(2, 2);
+      size_t total = 0;
+      for (int st = 1; st <= kMaxStride; ++st)
+        for (int op = 0; op < st; ++op)
+          if (convT_problem(nullptr, d[0], d[1], d[2], d[3], nullptr, d[4], d[5], st, d[6], op,
+                            &e, nullptr, false, &p) == FC_OK) {
+            const size_t t = ws_layout(p).total;
+            if (t > total) total = t;
+          }
+      return total;
+    }
+    case 3: {  // {N, C_in, H, W, C_out, k, pad, stride, out_pad, pool k, pool s}
+      if (d[9] < 1 || d[10] < 1 || d[9] > 4 || d[10] > 4) return 0;
+      const fc_epilogue e = pool_chain(d[9], d[10]);
+      if (convT_problem(nullptr, d[0], d[1], d[2], d[3], nullptr, d[4], d[5], d[7], d[6], d[8], &e,
+                        nullptr, false, &p) != FC_OK)
+        return 0;
+      return ws_layout(p).total;
+    }
     default:
       return 0;
   }
-  if (p.N < 0 || p.C < 1 || p.CO < 1 || p.KH < 1 || p.Ho < 1 || p.Wo < 1 || p.Do < 1)
-    return 0;
-  size_t total = ws_layout(p).total;
-  if (entry == 2) {
-    // the size covers every supported stride: stride 2 (output padding 0
-    // or 1) has its own per-tile partials
-    for (int op = 0; op <= 1; ++op) {
-      ConvProblem q = p;
-      q.subpix = 1; q.pad = 0;
-      q.Ho = 2 * p.H - 1 + op; q.Wo = 2 * p.W - 1 + op;
-      const size_t t = ws_layout(q).total;
-      if (t > total) total = t;
+}
+
+int fc_select_variant(int entry, const int *d) {
+  if (!d) return -1;
+  ConvProblem p;
+  fc_status s;
+  switch (entry) {
+    case 0:
+    case 4:  // {N, C_in, H, W, C_out, k, stride, pad, dilation}
+      s = conv_problem(nullptr, d[0], d[1], 1, d[2], d[3], nullptr, d[4], 1, d[5], d[5], d[6],
+                       d[7], d[8], nullptr, nullptr, entry == 4, 0, false, &p);
+      break;
+    case 1:
+    case 5:  // {N, C_in, D, H, W, C_out, k, stride, pad, dilation}
+      s = conv_problem(nullptr, d[0], d[1], d[2], d[3], d[4], nullptr, d[5], d[6], d[6], d[6],
+                       d[7], d[8], d[9], nullptr, nullptr, entry == 5, 1, false, &p);
+      break;
+    case 2: {  // {N, C_in, H, W, C_out, k, stride, pad, out_pad, pool k, pool s}
+      if (d[9] < 1 || d[10] < 1 || d[9] > 4 || d[10] > 4) return -1;
+      const fc_epilogue e = pool_chain(d[9], d[10]);
+      s = convT_problem(nullptr, d[0], d[1], d[2], d[3], nullptr, d[4], d[5], d[6], d[7], d[8], &e,
+                        nullptr, false, &p);
+      break;
     }
+    default:
+      return -1;
   }
-  return total;
+  if (s != FC_OK) return -1;
+  int staging = 1;
+  const int va = auto_choice(p, &staging);
+  const int v = g_variant_override != FC_VARIANT_AUTO ? g_variant_override : va;
+  p.staging = g_staging_override >= 0 ? g_staging_override : staging;
+  return variant_supported(p, v) ? v : -1;
 }
 
 fc_status fc_set_variant(int v) {
@@ -506,6 +643,14 @@ fc_status fc_set_variant(int v) {
   g_variant_override = v;
   return FC_OK;
 }
+
+fc_status fc_set_staging(int mode) {
+  if (mode < -1 || mode > 1) return FC_ERR_INVALID_ARG;
+  g_staging_override = mode;
+  return FC_OK;
+}
+
+int fc_last_staging(void) { return t_last_staging; }
 
 int fc_last_variant(void) { return t_last_variant; }
 
@@ -539,6 +684,7 @@ fc_status fc_get_last_device_error(void *stream) {
     if (cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return FC_ERR_CUDA;
   }
+  if (word & ST_PLAN) return FC_ERR_CUDA;
   if (word & ST_TIMEOUT) return FC_ERR_TIMEOUT;
   if (word & ST_RANGE) return FC_ERR_RANGE;
   return FC_OK;

@@ -147,14 +147,15 @@ __device__ __forceinline__ void apply_chain_generic_n(const EpiDev &e, int co0, 
 }
 
 // Two adjacent channels of one pixel through the fused chains on the paired
-// fp32 pipe: y = chain(hi + scale * lo + bias).  Bit-identical to
-// apply_chain on each lane.  Only the two fixed chains.
+// fp32 pipe, from conv sums already combined (hi + scale lo) in registers:
+// y = chain(x + bias).  Bit-identical to apply_chain on each lane (the
+// paired ops round per lane like the scalar ones).  Only the two fixed
+// chains.
 template <int CHAIN>
-__device__ __forceinline__ void apply_chain2(const EpiDev &e, float scale, float h0, float h1,
-                                             float l0, float l1, float b0, float b1, float a0,
-                                             float a1, float &o0, float &o1) {
-  uint64_t x = ptx::fma2(ptx::pk2(scale, scale), ptx::pk2(l0, l1), ptx::pk2(h0, h1));
-  x = ptx::add2(x, ptx::pk2(b0, b1));
+__device__ __forceinline__ void apply_chain2x(const EpiDev &e, float v0, float v1, float b0,
+                                              float b1, float a0, float a1, float &o0,
+                                              float &o1) {
+  uint64_t x = ptx::add2(ptx::pk2(v0, v1), ptx::pk2(b0, b1));
   float x0, x1;
   if constexpr (CHAIN == CHAIN_RELU_HARDSWISH) {
     ptx::upk2(x, x0, x1);

@@ -450,7 +450,15 @@ static int pooled_h(const ConvProblem &p) { return (p.Ho - p.pk) / p.ps + 1; }
 static int pooled_w(const ConvProblem &p) { return (p.Wo - p.pk) / p.ps + 1; }
 static bool pool_general(const ConvProblem &p) { return p.pk != 2 || p.ps != 2; }
 
+bool ffma_fixed_supported(const ConvProblem &p) {
+  if (p.gen || p.cl || p.subpix) return false;
+  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return false;
+  if (p.pool) return p.KD == 1 && p.stride == 1 && p.dil == 1;
+  return p.stride <= 2 && p.dil <= 2;
+}
+
 int ffma_pool_tiles_per_image(const ConvProblem &p) {
+  if (!ffma_fixed_supported(p)) return ffma_gen_tiles_per_image(p);
   if (pool_general(p)) return ceil_div(pooled_h(p), kPoolTH) * ceil_div(pooled_w(p), kPoolTW);
   return ceil_div(p.Ho, 8) * ceil_div(p.Wo, 16);
 }
@@ -477,6 +485,10 @@ cudaError_t ffma_launch(const ConvProblem &p, void *ws, const WsLayout &L,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *launches = 1;
+  if (!ffma_fixed_supported(p)) {
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
+    return ffma_gen_launch(p, wp, Cp, COp, p.pool ? partial : nullptr, s, launches);
+  }
   if (p.pool && pool_general(p)) {
     float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
     const int Hp = pooled_h(p), Wp = pooled_w(p);

@@ -35,10 +35,13 @@
 // copies).  All waits are
 // bounded (4 s on %globaltimer) and warp-uniform; a timeout sets a status
 // bit, every role drains, and the CTA frees its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "fc_epi.cuh"
 #include "fc_internal.h"
@@ -58,7 +61,11 @@ constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr uint32_t kSleepHintNs = 20000;  // hardware sleep per poll while waiting
+constexpr float kF16SplitMin = 1.0f / 4096.0f;  // 2^-12: smallest data maximum of the fp16 split
 constexpr unsigned int kWaitRecords = 32;  // diagnostic records kept after the status word
+// Kernel sizes the tensor-core plans take: odd, up to 7 x 7 in 2-D and
+// 5 x 5 x 5 in 3-D (125 taps); K-step tables hold kMaxTaps + 2 entries.
+constexpr int kMaxTaps = 126;
 
 // Division of 0 <= n < 2^31 by a divisor fixed at plan time, as a
 // multiply-high, add and shift (the round-up method of Granlund and
@@ -96,6 +103,7 @@ struct TcPlan {
   int NCH;        // stages per unit (chunks of C_in)
   int KS;         // K steps per chunk
   int TAPS;
+  int KH, KW;     // kernel rows / columns (odd; 3-D kernels are KH x KH x KH)
   int pairtaps;   // f16 with one plane per chunk: a K step spans two taps
   int U, R, RS, WT, RIN;
   // Staging geometry.  RS is the pitch (pixels) between the M tile's output
@@ -107,7 +115,7 @@ struct TcPlan {
   // reads sub-plane (a & 1, b & 1) at a shift of (a >> 1, b >> 1) -- again
   // one shifted descriptor start per tap.  DIL is the dilation.
   int S2, DIL, LW, SR, SUB, DSL;
-  uint8_t perm[28];  // K order of the taps (paired taps: increasing shifts)
+  uint8_t perm[kMaxTaps + 2];  // K order of the taps (paired taps: increasing shifts)
   // Stride-2 transposed conv by output parity class (SP): K step ks feeds
   // class kcls[ks] & 3 (accumulator (kcls & 3) x 128 columns); bit 7 marks
   // the class's first K step of a chunk.  skd[ks] is the step's A start |
@@ -136,6 +144,23 @@ struct TcPlan {
   FastDiv fd_ct, fd_rt, fd_do, fd_n, fd_cb;  // unit index -> position
   int smem_bytes;
   int off_b, off_bar, off_misc;
+  // Tensor-copy staging (TMA, stride 1): one producer warp loads the raw
+  // fp32 input of each (chunk, depth slice) -- RIN rows of LW pixels, all
+  // chunk channels, zeros outside the tensor -- with one tiled tensor copy
+  // into a ring of TR slots (raw_bytes each, raw_tx bytes per copy); the
+  // other producer warps split it into the stage's hi / lo slices.
+  // Channels-first slots are [chunk_ci][RIN][BW] (BW = LW + coff rounded up
+  // to 4: the copy starts coff columns early so that its first column is
+  // 16-byte aligned); channels-last slots [RIN][LW][chunk_ci].
+  int TMA, TR, raw_bytes, raw_tx, off_raw, BW, coff;
+  FastDiv fd_lw;
+  // Unit origin: input rows / columns advance by ROWSTEP / COLSTEP conv
+  // outputs per unit row / column index (U R and WT, except for the general
+  // max pool).  General max pool (GP, window pk, stride ps other than 2 / 2):
+  // a unit is one pooled row -- U = pk conv rows, one tile each -- of PJ
+  // pooled columns; the epilogue writes each lane's row maximum to XB bytes
+  // of shared memory at off_xb and takes the windows there.
+  int ROWSTEP, COLSTEP, GP, PJ, off_xb, XB;
 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -145,7 +170,8 @@ constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in
 struct SmemCtl {
   uint32_t tmem_base;
   int abort;
-  uint32_t kdelta[28];  // per K step: A start (16-byte units) | slice distance << 16
+  uint32_t amax_bits;  // largest |x| the producers staged (fp32 bits)
+  uint32_t kdelta[kMaxTaps + 2];  // per K step: A start (16-byte units) | slice distance << 16
   uint32_t kcls[28];    // per K step (stride-2 transposed conv): class | first << 7
   alignas(16) float red[4][64];          // pool: per-warp partial sums
   alignas(16) float bias[kMaxCoTc];      // bias per output channel (0 without bias)
@@ -162,10 +188,11 @@ static_assert(sizeof(SmemCtl) % 16 == 0, "SmemCtl size");
 // then (a >> 1) rows and (b >> 1) columns.  (Depth slice kd is staged input
 // depth od*stride + kd*DIL - pad.)
 __host__ __device__ __forceinline__ int tap_shift(int t, const TcPlan &q) {
-  const int kd = t / 9, a = ((t / 3) % 3) * q.DIL, b = (t % 3) * q.DIL;
+  const int kd = t / (q.KH * q.KW), a = ((t / q.KW) % q.KH) * q.DIL, b = (t % q.KW) * q.DIL;
   if (!q.S2) return kd * q.DSL + a * q.RS + b;
   return kd * q.DSL + (2 * (a & 1) + (b & 1)) * q.SUB + (a >> 1) * q.RS + (b >> 1);
 }
+
 
 // Channel chunks and K steps of a plan.  They do not depend on the
 // geometry, so neither does the weight image (nor the workspace): stride,
@@ -178,7 +205,9 @@ void plan_chunks(const ConvProblem &p, int prec, TcPlan &q) {
   const int Cp = cdiv(p.C, q.chunk_ci) * q.chunk_ci;
   q.P = q.chunk_ci / q.E;
   q.NCH = Cp / q.chunk_ci;
-  q.TAPS = p.KD * 9;
+  q.KH = p.KH;
+  q.KW = p.KW;
+  q.TAPS = p.KD * p.KH * p.KW;
   q.pairtaps = (q.P == 1);
   q.KS = q.pairtaps ? cdiv(q.TAPS, 2) : q.TAPS;
   q.COB = cdiv(p.CO, 64);
@@ -186,20 +215,31 @@ void plan_chunks(const ConvProblem &p, int prec, TcPlan &q) {
 }
 
 // Plan with `U` M tiles per unit (pooling needs 2).
+// Kernel shapes the tensor-core plans take: square, odd, 1..7 in 2-D and
+// cubic, odd, 1..5 in 3-D.
+bool tc_kernel_ok(const ConvProblem &p) {
+  if (p.KH != p.KW || (p.KH & 1) == 0 || p.KH > 7) return false;
+  if (p.KD > 1) return p.KD == p.KH && p.KD <= 5;
+  return p.entry != 1 || p.KH == 1;
+}
+
 TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   TcPlan q{};
-  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return q;
+  if (!tc_kernel_ok(p)) return q;
   if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
   if (p.cl && (p.pool || p.stride != 1)) return q;  // channels-last: stride 1, no pool
-  if (p.pool && U != 2) return q;
+  const bool gp = p.pool && (p.pk != 2 || p.ps != 2);
+  if (p.pool && U != (gp ? p.pk : 2)) return q;  // general pool: one tile per window row
   if (p.pool && p.KD != 1) return q;
-  if (p.pool && (p.pk != 2 || p.ps != 2)) return q;  // 2x2 / 2 pool only
+  if (gp && (p.pk < 1 || p.pk > 4 || p.ps < 1 || p.ps > 4)) return q;
   plan_chunks(p, prec, q);
+  q.GP = gp;
   q.S2 = p.stride == 2;
   q.DIL = p.dil;
   // staged columns past the tile's outputs: the last tap's column offset
-  // 2 DIL (stride 2: DIL in the half-width sub-planes)
-  const int halo = q.S2 ? q.DIL : 2 * q.DIL;
+  // (KW - 1) DIL (stride 2: half of it, in the half-width sub-planes)
+  const int span = (p.KW - 1) * q.DIL, spanh = (p.KH - 1) * q.DIL;
+  const int halo = q.S2 ? span / 2 : span;
   const bool rowpack = (p.Wo + halo <= 128);
   if (rowpack) {
     q.RS = p.Wo + halo;
@@ -213,20 +253,37 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
     q.R = 1;
   }
   q.U = U;
-  if (!q.S2) {  // output rows u read input rows u + kh DIL: UR + 2 DIL rows
-    q.RIN = q.U * q.R + 2 * q.DIL;
+  q.ROWSTEP = q.U * q.R;
+  q.COLSTEP = q.WT;
+  if (gp) {
+    // pooled columns per tile: the windows wholly inside its WT columns
+    const int Wp = (p.Wo - p.pk) / p.ps + 1;
+    q.PJ = (q.WT - p.pk) / p.ps + 1;
+    if (q.PJ > Wp) q.PJ = Wp;
+    // strips advance by PJ ps columns: keep that a multiple of 4 so every
+    // strip's first staged column stays 16-byte aligned for tensor copies
+    if (q.PJ < Wp)
+      while (q.PJ > 1 && (q.PJ * p.ps) % 4 != 0) --q.PJ;
+    if (q.PJ < 1) return q;
+    q.COLSTEP = q.PJ * p.ps;
+    q.n_ct = cdiv(Wp, q.PJ);
+    q.ROWSTEP = p.ps;
+    q.XB = 64 * 128 * 4;  // row maxima of 64 channels x 128 columns
+  }
+  if (!q.S2) {  // output rows u read input rows u + kh DIL: UR + (KH - 1) DIL rows
+    q.RIN = q.U * q.R + spanh;
     q.LW = q.RS;
     q.DSL = q.RIN * q.RS;
-  } else {  // output rows u read input rows 2u + kh DIL: 2UR - 1 + 2 DIL rows
-    q.RIN = 2 * q.U * q.R - 1 + 2 * q.DIL;
+  } else {  // output rows u read input rows 2u + kh DIL: 2UR - 1 + (KH - 1) DIL rows
+    q.RIN = 2 * q.U * q.R - 1 + spanh;
     q.LW = 2 * q.RS;  // of 2 RS columns
-    q.SR = q.U * q.R + q.DIL;  // even input rows (odd rows: one fewer)
+    q.SR = q.U * q.R + spanh / 2;  // even input rows (odd rows: one fewer)
     q.SUB = q.SR * q.RS;
     q.DSL = 4 * q.SUB;
   }
   // K order of the taps: by increasing shift, so a K step's two paired taps
   // are one positive LBO apart (stride 1: the natural order)
-  int shift[27];
+  int shift[kMaxTaps];
   for (int t = 0; t < q.TAPS; ++t) {
     shift[t] = tap_shift(t, q);
     q.perm[t] = (uint8_t)t;
@@ -237,7 +294,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
       q.perm[j] = q.perm[j - 1];
       q.perm[j - 1] = tmp;
     }
-  for (int t = q.TAPS; t < 28; ++t) q.perm[t] = 255;  // zero-weight padding slot
+  for (int t = q.TAPS; t < kMaxTaps + 2; ++t) q.perm[t] = 255;  // zero-weight padding slot
   // last staged pixel any MMA can touch: the largest tap shift (+1 for the
   // paired zero-weight slice), the last tile, 128 rows
   int maxshift = 0;
@@ -249,7 +306,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.plane_bytes = q.NPIX * 16;
   q.a_stage_bytes = 2 * q.P * q.plane_bytes;
   if (q.COB * 64 > kMaxCoTc) return q;
-  q.n_rt = p.pool ? p.Ho / 2 : cdiv(p.Ho, q.U * q.R);
+  q.n_rt = gp ? (p.Ho - p.pk) / p.ps + 1 : p.pool ? p.Ho / 2 : cdiv(p.Ho, q.U * q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
   if (q.units >= (1L << 31)) return q;  // unit indices are 32-bit
   q.fd_ct = make_fastdiv((uint32_t)q.n_ct);
@@ -257,13 +314,34 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.fd_do = make_fastdiv((uint32_t)p.Do);
   q.fd_n = make_fastdiv((uint32_t)p.N);
   q.fd_cb = make_fastdiv((uint32_t)((long)p.N * p.Do * q.n_rt * q.n_ct));
-  q.NACC = q.U == 2 ? 2 : 4;
-  q.tmem_cols = q.NACC * q.U * 128;
+  q.NACC = q.U == 1 ? 4 : q.U == 2 ? 2 : 1;
+  q.tmem_cols = q.U == 3 ? 512 : q.NACC * q.U * 128;  // allocations are powers of two
   if (q.tmem_cols > 512) return q;
-  // shared memory: A stages + B (resident or a ring) + barriers/misc
-  const int misc = 512 + (int)sizeof(SmemCtl) + 256;
+  // shared memory: A stages + raw slots (tensor-copy staging) + B (resident
+  // or a ring) + barriers/misc (+ the general pool's row maxima)
+  const int misc = 512 + (int)sizeof(SmemCtl) + 256 + q.XB;
   const long b_all = (long)q.COB * q.NCH * q.b_chunk_bytes;
-  int S = 0, resident = 0, SB = 0;
+  // Tensor-copy staging needs 16-byte multiples for the tensor's strides
+  // (channels-first: W % 4 == 0; channels-last: C_in % 4 == 0) and box
+  // extents of at most 256.
+  q.coff = p.cl ? 0 : (((-p.pad) % 4) + 4) % 4;
+  q.BW = p.cl ? q.LW : (q.LW + q.coff + 3) / 4 * 4;
+  // (channels-first: every unit's first column iw0 - coff a multiple of 4,
+  // so the strips must advance by a multiple of 4 columns)
+  const bool tma_ok = p.staging && !q.S2 && (p.cl ? (p.C % 4 == 0) : (p.W % 4 == 0)) &&
+                      (p.cl || q.n_ct == 1 || q.COLSTEP % 4 == 0) && q.BW <= 256 &&
+                      q.RIN <= 256;
+  q.raw_tx = q.chunk_ci * q.RIN * q.BW * 4;
+  q.raw_bytes = (q.raw_tx + 127) / 128 * 128;
+  int S = 0, resident = 0, SB = 0, TR = 0;
+  if (tma_ok) {  // at least two stages and two slots (a stage's depth slices + 1 in 3D)
+    const int tr_min = p.KD > 1 ? p.KD + 1 : 2;
+    for (int s = 4; s >= 2 && !S; --s)
+      for (int tr = 4; tr >= tr_min && !S; --tr)
+        if ((long)s * q.a_stage_bytes + (long)tr * q.raw_bytes + b_all + misc <= kMaxSmem) {
+          S = s; TR = tr; resident = 1;
+        }
+  }
   for (int s = 4; s >= 2 && !S; --s)
     if ((long)s * q.a_stage_bytes + b_all + misc <= kMaxSmem) { S = s; resident = 1; }
   if (!S)
@@ -274,11 +352,16 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
       if ((long)s * q.a_stage_bytes + 1L * q.b_chunk_bytes + misc <= kMaxSmem) { S = s; SB = 1; }
   if (!S) return q;
   q.S = S;
+  q.TMA = TR > 0;
+  q.TR = TR;
+  q.fd_lw = make_fastdiv((uint32_t)q.LW);
   q.b_resident = resident;
   q.SB = resident ? 1 : SB;
-  q.off_b = S * q.a_stage_bytes;
+  q.off_raw = S * q.a_stage_bytes;  // 128-byte aligned (NPIX is a multiple of 8)
+  q.off_b = q.off_raw + TR * q.raw_bytes;
   q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
   q.off_misc = q.off_bar + 512;  // 16-byte aligned: off_b and the B region are
+  q.off_xb = q.off_misc + (int)sizeof(SmemCtl);
   q.smem_bytes = q.off_bar + misc;
   if (q.smem_bytes < 120 * 1024) q.smem_bytes = 120 * 1024;  // one CTA per SM
   q.ok = 1;
@@ -316,6 +399,8 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
     q.R = 1;
   }
   q.U = 1;
+  q.ROWSTEP = q.R;
+  q.COLSTEP = q.WT;
   q.RIN = q.R + 1;
   q.LW = q.RS;
   q.DSL = q.RIN * q.RS;
@@ -342,7 +427,7 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
   }
   const int nslots = slot;
   if (q.KS != (q.pairtaps ? nslots / 2 : nslots)) return q;
-  for (int t = nslots; t < 28; ++t) q.perm[t] = 255;
+  for (int t = nslots; t < kMaxTaps + 2; ++t) q.perm[t] = 255;
   int prev = -1;
   for (int ks = 0; ks < q.KS; ++ks) {
     const int s0 = q.pairtaps ? 2 * ks : ks;
@@ -392,6 +477,7 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
   q.S = S;
   q.b_resident = resident;
   q.SB = resident ? 1 : SB;
+  q.off_raw = S * q.a_stage_bytes;
   q.off_b = S * q.a_stage_bytes;
   q.off_bar = q.off_b + (int)(resident ? b_all : (long)q.SB * q.b_chunk_bytes);
   q.off_misc = q.off_bar + 512;
@@ -409,7 +495,7 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
 // at least three stages; otherwise one.
 TcPlan make_plan(const ConvProblem &p, int prec) {
   if (p.subpix) return make_plan_subpix(p, prec);
-  if (p.pool) return make_plan_u(p, prec, 2);
+  if (p.pool) return make_plan_u(p, prec, (p.pk == 2 && p.ps == 2) ? 2 : p.pk);
   TcPlan q2 = make_plan_u(p, prec, 2);
   if (q2.ok && q2.S >= 3 && p.Ho > q2.R) return q2;
   TcPlan q1 = make_plan_u(p, prec, 1);
@@ -478,6 +564,9 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Weight-ring slot of chunk g.
+__device__ __forceinline__ int psb_tma_slot(uint32_t g, int SB) { return (int)(g % (uint32_t)SB); }
+
 // AND of a predicate over the 256 epilogue threads (named barrier 1).
 __device__ __forceinline__ bool epi_all(bool v) {
   uint32_t r;
@@ -523,6 +612,7 @@ __device__ __forceinline__ bool f16_out_of_range(float v) {
 // output channels, rows 64-127 W_lo (zero rows past C_out).
 __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ out) {
   const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
+  float wmx = 0.0f;  // largest |w| this thread packs (fp16 split: range check)
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nelem;
        i += (long)gridDim.x * blockDim.x) {
     const int e = (int)(i % q.E);
@@ -548,8 +638,8 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
       } else if (q.SP) {  // transposed conv by parity class: W[ci][co][kh][kw] as is
         w = p.w[((long)ci * p.CO + co) * 9 + tap];
       } else {  // transposed conv as a conv: swap channel axes, flip both taps
-        const int kh = tap / 3, kw = tap % 3;
-        w = p.w[(((long)ci * p.CO + co) * 3 + (2 - kh)) * 3 + (2 - kw)];
+        const int kh = tap / q.KW, kw = tap % q.KW;
+        w = p.w[(((long)ci * p.CO + co) * q.KH + (q.KH - 1 - kh)) * q.KW + (q.KW - 1 - kw)];
       }
     }
     const bool lo = row >= 64;
@@ -560,9 +650,22 @@ __global__ void tc_pack_weights(ConvProblem p, TcPlan q, uint8_t *__restrict__ o
       reinterpret_cast<uint32_t *>(out + base)[e] = v;
     } else {
       if (f16_out_of_range(w)) atomicOr(p.status, ST_RANGE);
+      wmx = fmaxf(wmx, fabsf(w));
       const __half hi = __float2half_rn(w);
       const __half v = lo ? __float2half_rn((w - __half2float(hi)) * 2048.0f) : hi;
       reinterpret_cast<__half *>(out + base)[e] = v;
+    }
+  }
+  if (q.prec == 1 && p.wmax) {  // the block's maximum, for the main kernel's check
+    __shared__ float red[8];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wmx = fmaxf(wmx, __shfl_xor_sync(0xffffffffu, wmx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wmx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.0f;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+      p.wmax[blockIdx.x] = m;
     }
   }
 }
@@ -621,10 +724,10 @@ __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, 
                                                    const ConvProblem &p, int nrows, int E, bool s2,
                                                    bool cl = false) {
   RowJob jb;
-  // a stage holds at most 2 slice planes of at most 3 depth slices
+  // a stage holds at most 2 slice planes of KD depth slices
   const int plane = job >= nrows ? 1 : 0;
   const int sr = job - plane * nrows;
-  const int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
+  const int kdp = sr / q.RIN;
   const int r = sr - kdp * q.RIN;
   const int id = ss.id0 + kdp * q.DIL, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
@@ -833,13 +936,14 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP, bool CL>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP, bool CL, bool GP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
-               float *__restrict__ partial) {
+               float *__restrict__ partial, const __grid_constant__ CUtensorMap tmx) {
   constexpr int E = PREC ? 8 : 4;
-  static_assert(U == 1 || U == 2, "one or two M tiles per unit");
-  static_assert(!POOL || U == 2 || SP, "pooling takes two output rows per unit");
+  static_assert(U >= 1 && U <= 4, "one to four M tiles per unit");
+  static_assert(!POOL || U == 2 || SP || GP, "the 2x2 pool takes two output rows per unit");
+  static_assert(!GP || (POOL && !SP && !S2 && !CL), "general pool: stride-1 pooled entry");
   static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
   static_assert(!CL || (!POOL && !S2), "channels-last: stride-1 elementwise entries");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -847,7 +951,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + q.off_bar);
   constexpr int A_FULL = 0, A_EMPTY = 4, B_FULL = 8, B_EMPTY = 10, ACC_FULL = 12,
-                ACC_EMPTY = 16, DRAIN = 20;
+                ACC_EMPTY = 16, DRAIN = 20, RAW_FULL = 21, RAW_EMPTY = 25;
   uint64_t *a_full = bars + A_FULL;
   uint64_t *a_empty = bars + A_EMPTY;
   uint64_t *b_full = bars + B_FULL;
@@ -862,9 +966,13 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   const int warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < q.S; ++s) {
-      ptx::mbar_init(&a_full[s], (uint32_t)kProdWarps);
+    for (int s = 0; s < q.S; ++s) {  // tensor-copy staging: one warp loads, the rest convert
+      ptx::mbar_init(&a_full[s], (uint32_t)(q.TMA ? kProdWarps - 1 : kProdWarps));
       ptx::mbar_init(&a_empty[s], 1);
+    }
+    for (int r = 0; r < q.TR; ++r) {
+      ptx::mbar_init(&bars[RAW_FULL + r], 1);
+      ptx::mbar_init(&bars[RAW_EMPTY + r], (uint32_t)(kProdWarps - 1));
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&b_full[s], 1);
@@ -876,6 +984,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     }
     ptx::mbar_init(drain, 1);
     ctl->abort = 0;
+    ctl->amax_bits = 0;
     ptx::fence_mbar_init();
   }
   if (SP && tid < q.KS) {  // per-class K steps, laid out on the host
@@ -893,7 +1002,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       lbo16 = (uint32_t)(q.plane_bytes >> 4);
     }
     ctl->kdelta[tid] = (off16 & 0x3FFFu) | ((lbo16 & 0x3FFFu) << 16);
-  } else if (tid < 28) {
+  } else if (tid < kMaxTaps + 2) {
     ctl->kdelta[tid] = 0;  // read (unused) by the last step's prefetch
   }
   for (int c = tid; c < q.COB * 64; c += kThreads) {
@@ -954,6 +1063,162 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             *reinterpret_cast<uint4 *>(smem + (long)st * q.a_stage_bytes + pl * q.plane_bytes +
                                        px * 16) = make_uint4(0, 0, 0, 0);
     }
+    bool tma_done = false;
+    if constexpr (!S2 && !SP) {
+      if (q.TMA) {
+        // ---- tensor-copy staging.  Warp kProdWarp0 (its first lane) issues
+        // one tiled tensor copy per (chunk, depth slice) into the raw ring and
+        // streams the weights; warps kProdWarp0+1.. split each raw slice into
+        // the stage's hi / lo slices (zeros outside the image come from the
+        // copy itself).
+        uint8_t *raw0 = smem + q.off_raw;
+        int rs = 0;
+        uint32_t rph = 0;
+        const int iw_adj = CL ? 0 : q.coff;
+        if (pw == 0) {
+          ptx::tma_prefetch_desc(&tmx);
+          int last_rs = -1;
+          uint32_t last_par = 0;  // bit r: phase parity of the last copy into slot r
+          for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const UnitPos up = decode_unit(u, q);
+            const int id0 = up.od - p.pad_d;
+            const int ih0 = up.rt * q.ROWSTEP - p.pad;
+            const int iw0 = up.ct * q.COLSTEP - p.pad - iw_adj;
+            for (int c = 0; ok && c < q.NCH; ++c, ++g) {
+              if (!q.b_resident) {
+                const int sb = psb_tma_slot(g, q.SB);
+                if (!wait_bar_warp(bars, B_EMPTY + sb, ((g / q.SB) & 1) ^ 1, abort_flag, p.status,
+                                   0x11000000u | g)) {
+                  ok = false;
+                  break;
+                }
+                if (lane == 0) {
+                  ptx::mbar_arrive_expect_tx(&b_full[sb], (uint32_t)q.b_chunk_bytes);
+                  const uint8_t *src = bimg + ((long)up.cb * q.NCH + c) * q.b_chunk_bytes;
+                  uint8_t *dst = smem + q.off_b + (long)sb * q.b_chunk_bytes;
+                  for (int off = 0; off < q.b_chunk_bytes; off += 16384) {
+                    const int nb = (q.b_chunk_bytes - off) < 16384 ? (q.b_chunk_bytes - off) : 16384;
+                    ptx::bulk_g2s(dst + off, src + off, (uint32_t)nb, &b_full[sb]);
+                  }
+                }
+                __syncwarp();
+              }
+              const int ci0 = c * q.chunk_ci;
+              for (int kd = 0; kd < p.KD; ++kd) {
+                if (!wait_bar_warp(bars, RAW_EMPTY + rs, rph ^ 1, abort_flag, p.status,
+                                   0x14000000u | g)) {
+                  ok = false;
+                  break;
+                }
+                if (!CL && (iw0 & 3)) {
+                  // a plan error (the copy's first column must be 16-byte
+                  // aligned): report it and stop instead of issuing the copy
+                  if (lane == 0) {
+                    record_timeout(p.status, &bars[RAW_FULL + rs], RAW_FULL + rs, rph, 0x17000000u | g);
+                    atomicOr(p.status, ST_PLAN);
+                    *abort_flag = 1;
+                  }
+                  ok = false;
+                  break;
+                }
+                if (lane == 0) {
+                  uint64_t *bar = &bars[RAW_FULL + rs];
+                  uint8_t *dst = raw0 + (long)rs * q.raw_bytes;
+                  ptx::mbar_arrive_expect_tx(bar, (uint32_t)q.raw_tx);
+                  const int id = id0 + kd * q.DIL;
+                  // 3-D entry (any kernel depth): a rank-5 map with a depth axis
+                  if constexpr (CL) {
+                    if (p.entry != 1) ptx::tma_load_4d(dst, &tmx, ci0, iw0, ih0, up.n, bar);
+                    else ptx::tma_load_5d(dst, &tmx, ci0, iw0, ih0, id, up.n, bar);
+                  } else {
+                    if (p.entry != 1) ptx::tma_load_4d(dst, &tmx, iw0, ih0, ci0, up.n, bar);
+                    else ptx::tma_load_5d(dst, &tmx, iw0, ih0, id, ci0, up.n, bar);
+                  }
+                }
+                __syncwarp();
+                last_rs = rs > last_rs ? rs : last_rs;
+                last_par = (last_par & ~(1u << rs)) | (rph << rs);
+                if (++rs == q.TR) { rs = 0; rph ^= 1; }
+              }
+            }
+          }
+          // every issued copy has landed before the CTA can exit (waits bounded
+          // by time only: they run even after an abort)
+          if (lane == 0) {
+            volatile int no_abort = 0;
+            for (int r = 0; r <= last_rs; ++r)
+              wait_bar(bars, RAW_FULL + r, (last_par >> r) & 1u, &no_abort, p.status,
+                       0x15000000u | r);
+          }
+          if (pt == 0 && q.b_resident)
+            wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
+          if (lane == 0 && !q.b_resident && g > 0) {
+            const uint32_t lb = g - 1;
+            wait_bar(bars, B_FULL + (int)(lb % q.SB), (lb / q.SB) & 1, abort_flag, p.status,
+                     0x13000000u | lb);
+          }
+        } else {
+          const int ct = pt - 32;  // converter thread, 0 .. 32 (kProdWarps - 1) - 1
+          constexpr int kConv = 32 * (kProdWarps - 1);
+          const int lo_off = q.P * q.plane_bytes;
+          const int items = q.P * q.RIN * q.LW;  // (plane, row, column) per depth slice
+          const int chs = q.RIN * q.BW;          // channels-first: floats between channels
+          int ps = 0;
+          uint32_t pph = 0;
+          for (long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            for (int c = 0; ok && c < q.NCH; ++c, ++g) {
+              const int s = ps;
+              uint8_t *stage = smem + (long)s * q.a_stage_bytes;
+              if (!wait_bar_warp(bars, A_EMPTY + s, pph ^ 1, abort_flag, p.status, 0x10000000u | g)) {
+                ok = false;
+                break;
+              }
+              for (int kd = 0; kd < p.KD; ++kd) {
+                if (!wait_bar_warp(bars, RAW_FULL + rs, rph, abort_flag, p.status, 0x16000000u | g)) {
+                  ok = false;
+                  break;
+                }
+                const float *raw = reinterpret_cast<const float *>(raw0 + (long)rs * q.raw_bytes);
+                for (int it = ct; it < items; it += kConv) {
+                  const int row = (int)fdiv((uint32_t)it, q.fd_lw);
+                  const int cc = it - row * q.LW;
+                  const int pl = row >= q.RIN ? 1 : 0;
+                  const int r = row - pl * q.RIN;
+                  float v[E];
+                  if constexpr (CL) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        raw + ((long)r * q.LW + cc) * q.chunk_ci + pl * E);
+#pragma unroll
+                    for (int e = 0; e < E; e += 4) {
+                      const float4 f = src[e / 4];
+                      v[e] = f.x; v[e + 1] = f.y; v[e + 2] = f.z; v[e + 3] = f.w;
+                    }
+                  } else {
+                    const float *src = raw + ((long)pl * E * q.RIN + r) * q.BW + cc + q.coff;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) v[e] = src[e * chs];
+                  }
+                  const uint32_t o = (uint32_t)(pl * q.plane_bytes + (kd * q.DSL + r * q.RS + cc) * 16);
+                  store_slice<PREC, E>(stage + o, stage + lo_off + o, v, amax);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&bars[RAW_EMPTY + rs]);
+                if (++rs == q.TR) { rs = 0; rph ^= 1; }
+              }
+              if (!ok) break;
+              if (++ps == q.S) { ps = 0; pph ^= 1; }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&a_full[s]);
+            }
+          }
+        }
+        if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
+        atomicMax(&ctl->amax_bits, __float_as_uint(amax));    // |x| >= 0: bits order as values
+        tma_done = true;
+      }
+    }
+    if (!tma_done) {
     // Job J of a stage goes to producer warp (rot + J) % kProdWarps, where
     // rot counts the jobs of all earlier stages: the remainder of
     // njobs / kProdWarps moves round the warps instead of always landing on
@@ -969,8 +1234,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       StageSrc ss;
       const int st = p.stride;
       ss.id0 = up.od * st - p.pad_d;
-      ss.ih0 = up.rt * U * q.R * st - p.pad;  // input row of the unit's first output row
-      ss.iw0 = up.ct * q.WT * st - p.pad;
+      ss.ih0 = up.rt * q.ROWSTEP * st - p.pad;  // input row of the unit's first output row
+      ss.iw0 = up.ct * q.COLSTEP * st - p.pad;
       ss.xn = (long)up.n * p.C * p.D * HW;
       for (int c = 0; c < q.NCH; ++c, ++g) {
         const int s = ps;
@@ -1048,11 +1313,13 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
+    atomicMax(&ctl->amax_bits, __float_as_uint(amax));    // |x| >= 0: bits order as values
     // drain outstanding weight copies before the CTA can exit
     if (pt == 0 && q.b_resident) wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
     if (lane == 0 && last_b != 0xffffffffu)
       wait_bar(bars, B_FULL + (int)(last_b % q.SB), (last_b / q.SB) & 1, abort_flag, p.status,
                0x13000000u | last_b);
+    }  // register-load producers
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
     // The warp stays converged; every MMA burst and every commit is issued
@@ -1185,11 +1452,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           for (int t = 0; t < U; ++t) {
             const int ab = acc * U + t;
             const uint32_t at = a_lo + (uint32_t)t * tile_delta, dt = dacc + (uint32_t)(t * 128);
-            switch (q.KS) {  // 2D: 5 or 9 K steps, 3D: 14 or 27
+            switch (q.KS) {  // 3 x 3 kernels: 2D 5 or 9 K steps, 3D 14 or 27
               case 5: issue_chunk<PREC, 1, 5>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
               case 9: issue_chunk<PREC, 1, 9>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
               case 14: issue_chunk<PREC, 1, 14>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
-              default: issue_chunk<PREC, 1, 27>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+              case 27: issue_chunk<PREC, 1, 27>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
+              default:  // other kernel sizes: K-step table in shared memory
+                issue_chunk_loop<PREC, 1>(ctl->kdelta, q.KS, at, b_lo, dt, lo_delta, tile_delta, first);
+                break;
             }
             if (c == q.NCH - 1) {
               if (ptx::elect_one()) ptx::tc_commit(&acc_full[ab]);
@@ -1264,15 +1534,55 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ptx::tc_fence_after();
           const int oh = (up.rt * U + t) * q.R + r;
           const bool valid = r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo;
+          const uint32_t col0 = (uint32_t)((acc * U + t) * 128 + ch0);
+          // Heavy chains (GELU, the general chain): the warp's 32 channels of
+          // this tile leave tensor memory at once, are combined (hi + scale lo)
+          // in registers and the accumulator is released before the chain and
+          // the stores, so a later unit's MMAs overlap them (measured: conv3d
+          // + GELU chain 0.653 -> 0.639 ms).  Light chains keep two loads of 16
+          // channels and release after the stores (conv2d + ReLU + HardSwish
+          // 0.122 ms, 0.133 ms with the early release).
+          constexpr bool kEarly = CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU ||
+                                  CHAIN == CHAIN_LEAKY_ADD_CLAMP_GELU || CHAIN == CHAIN_GENERIC;
+          float acc32[32];
+          auto load_sums = [&](int c0, int n16) {
+            uint32_t h0[16], l0[16], h1[16], l1[16];
+            ptx::tmem_ld16(tl + col0 + c0, h0);
+            ptx::tmem_ld16(tl + col0 + 64 + c0, l0);
+            if (n16 == 2) {
+              ptx::tmem_ld16(tl + col0 + c0 + 16, h1);
+              ptx::tmem_ld16(tl + col0 + 80 + c0, l1);
+            }
+            ptx::tmem_wait_ld();
+            const uint64_t sc2 = ptx::pk2(scale, scale);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2)
+              ptx::upk2(ptx::fma2(sc2, ptx::pk2(__uint_as_float(l0[j]), __uint_as_float(l0[j + 1])),
+                                  ptx::pk2(__uint_as_float(h0[j]), __uint_as_float(h0[j + 1]))),
+                        acc32[c0 + j], acc32[c0 + j + 1]);
+            if (n16 == 2) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                ptx::upk2(ptx::fma2(sc2, ptx::pk2(__uint_as_float(l1[j]), __uint_as_float(l1[j + 1])),
+                                    ptx::pk2(__uint_as_float(h1[j]), __uint_as_float(h1[j + 1]))),
+                          acc32[c0 + 16 + j], acc32[c0 + 16 + j + 1]);
+            }
+          };
+          auto release = [&]() {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[acc * U + t]);
+          };
+          if constexpr (kEarly) {
+            load_sums(0, 2);
+            release();
+          }
           float *yp = p.y + (((long)up.n * p.CO + co_base + ch0) * p.Do + up.od) * plane +
                       (long)oh * p.Wo + ow;
-          const uint32_t col0 = (uint32_t)((acc * U + t) * 128 + ch0);
-  #pragma unroll 1
+#pragma unroll
           for (int cc = 0; cc < 32; cc += 16) {
-            uint32_t hi[16], lo[16];
-            ptx::tmem_ld16(tl + col0 + cc, hi);
-            ptx::tmem_ld16(tl + col0 + 64 + cc, lo);
-            ptx::tmem_wait_ld();
+            if constexpr (!kEarly) load_sums(cc, 1);
+            float *v = acc32 + cc;  // conv sums of channels cc .. cc + 15 (no bias yet)
             float bv[16], av[16];
             const float *sb = &ctl->bias[co_base + ch0 + cc];
             const float *sa = &ctl->addend[co_base + ch0 + cc];
@@ -1284,29 +1594,25 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               else
                 av[j] = av[j + 1] = av[j + 2] = av[j + 3] = 0.0f;
             }
+            float o[16];
+            if constexpr (CHAIN == CHAIN_GENERIC) {
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = v[j] + bv[j];
+              apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, o);
+            } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
+                                 CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
+  #pragma unroll
+              for (int j = 0; j < 16; j += 2)  // channel pairs on the paired fp32 pipe
+                apply_chain2x<CHAIN>(p.epi, v[j], v[j + 1], bv[j], bv[j + 1], av[j], av[j + 1],
+                                     o[j], o[j + 1]);
+            } else {
+  #pragma unroll
+              for (int j = 0; j < 16; ++j)
+                o[j] = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v[j] + bv[j], av[j]);
+            }
             if constexpr (CL) {
               // channels-last output: this pixel's 16 channels are adjacent
               if (valid) {
-                float o[16];
-                if constexpr (CHAIN == CHAIN_GENERIC) {
-  #pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    o[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, o);
-                } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
-                                     CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
-  #pragma unroll
-                  for (int j = 0; j < 16; j += 2)
-                    apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
-                                        __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
-                                        bv[j + 1], av[j], av[j + 1], o[j], o[j + 1]);
-                } else {
-  #pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    const float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                    o[j] = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-                  }
-                }
                 float *yc = p.y + ((((long)up.n * p.Do + up.od) * p.Ho + oh) * p.Wo + ow) * p.CO +
                             co_base + ch0 + cc;
                 if (cc + 16 <= nco && (p.CO & 3) == 0) {  // 16-byte aligned vectors
@@ -1322,67 +1628,78 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             } else {
               float *yc = yp + (long)cc * cstride;
               if (valid && cc + 16 <= nco) {  // all 16 channels exist: no per-channel test
-                if constexpr (CHAIN == CHAIN_GENERIC) {  // op loop outside, 16 values inside
-                  float v[16];
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, 16, v);
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    *yc = v[j];
-                    yc += cstride;
-                  }
-                } else if constexpr (CHAIN == CHAIN_RELU_HARDSWISH ||
-                                     CHAIN == CHAIN_LEAKY_ADD_CLAMP1_GELU) {
-    #pragma unroll
-                  for (int j = 0; j < 16; j += 2) {  // channel pairs on the paired fp32 pipe
-                    float o0, o1;
-                    apply_chain2<CHAIN>(p.epi, scale, __uint_as_float(hi[j]), __uint_as_float(hi[j + 1]),
-                                        __uint_as_float(lo[j]), __uint_as_float(lo[j + 1]), bv[j],
-                                        bv[j + 1], av[j], av[j + 1], o0, o1);
-                    yc[0] = o0;
-                    yc[cstride] = o1;
-                    yc += 2 * cstride;
-                  }
-                } else {
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                    *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-                    yc += cstride;
-                  }
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  *yc = o[j];
+                  yc += cstride;
                 }
               } else if (valid) {
-                if constexpr (CHAIN == CHAIN_GENERIC) {
-                  float v[16];
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    v[j] = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                  apply_chain_generic_n<16>(p.epi, co_base + ch0 + cc, nco - cc, v);
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    if (cc + j < nco) *yc = v[j];
-                    yc += cstride;
-                  }
-                } else {
-    #pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    if (cc + j < nco) {
-                      float v = fmaf(scale, __uint_as_float(lo[j]), __uint_as_float(hi[j])) + bv[j];
-                      *yc = apply_chain<CHAIN>(p.epi, co_base + ch0 + cc + j, v, av[j]);
-                    }
-                    yc += cstride;
-                  }
+  #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (cc + j < nco) *yc = o[j];
+                  yc += cstride;
                 }
               }
             }
           }
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&acc_empty[acc * U + t]);
+          if constexpr (!kEarly) release();
         }
         if (!okt) break;
+      } else if constexpr (GP) {
+        // General max pool: lane m is conv column m of the tile; the row
+        // maximum over the unit's U conv rows (the pooled row's window rows)
+        // goes to shared memory, the accumulator is released, and the 256
+        // epilogue threads take the windows across columns there.
+        float *xb = reinterpret_cast<float *>(smem + q.off_xb);  // [64 channels][128 columns]
+#pragma unroll 1
+        for (int cc = 0; cc < 32; cc += 16) {
+          float mx[16];
+#pragma unroll 1
+          for (int t = 0; t < U; ++t) {
+            uint32_t h0[16], l0[16];
+            const uint32_t col = (uint32_t)((acc * U + t) * 128 + ch0 + cc);
+            ptx::tmem_ld16(tl + col, h0);
+            ptx::tmem_ld16(tl + col + 64, l0);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float v = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j]));
+              mx[j] = t ? fmaxf(mx[j], v) : v;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xb[(ch0 + cc + j) * 128 + m] = mx[j];
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+        epi_sync();
+        // windows: thread (jq, ch) takes pooled columns jq, jq + 4, ... of
+        // channel ch in increasing order; the bias is common to a window, so
+        // it is added after the max (x -> x + b is monotone in fp32)
+        const int et = warp * 32 + lane;  // 0 .. 255
+        const int ch = et & 63, jq = et >> 6;
+        const int Wp = (p.Wo - p.pk) / p.ps + 1;
+        const float bias = ctl->bias[co_base + ch];
+        float sum = 0.0f;
+        for (int j = jq; j < q.PJ; j += 4) {
+          if (up.ct * q.PJ + j >= Wp) break;
+          const float *w = xb + ch * 128 + j * p.ps;
+          float mxw = w[0];
+          for (int a = 1; a < p.pk; ++a) mxw = fmaxf(mxw, w[a]);
+          sum += fminf(fmaxf(mxw + bias, p.ht_lo), p.ht_hi);
+        }
+        ctl->red[jq][ch] = sum;
+        epi_sync();
+        if (et < 64) {
+          const int T = q.n_rt * q.n_ct;
+          const int t = up.rt * q.n_ct + up.ct;
+          const int co = co_base + et;
+          if (co < p.CO)
+            partial[((long)up.n * T + t) * p.CO + co] =
+                ((ctl->red[0][et] + ctl->red[1][et]) + ctl->red[2][et]) + ctl->red[3][et];
+        }
+        epi_sync();
       } else if constexpr (SP) {
         // lane m = pooled pixel (rt R + m_row, ct WT + m_col); the 2x2 window
         // is the four class accumulators of that lane
@@ -1554,6 +1871,23 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
+  if constexpr (PREC == 1) {
+    // Bottom of the fp16 split's range: below 2^-14 the hi part of a value is
+    // subnormal and below 2^-24 it vanishes, so inputs whose largest
+    // magnitude is under 2^-12 would lose relative accuracy.  Flag it when
+    // this CTA's staged x, or the weights (checked by CTA 0), are that small
+    // everywhere (all-zero data is exact and not flagged).
+    if (warp == kProdWarp0) {
+      const float xm = __uint_as_float(ctl->amax_bits);
+      float wm = 0.0f;
+      if (blockIdx.x == 0 && p.wmax)
+        for (int i = lane; i < p.wmax_n; i += 32) wm = fmaxf(wm, p.wmax[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+      if (lane == 0 && ((xm > 0.0f && xm < kF16SplitMin) || (wm > 0.0f && wm < kF16SplitMin)))
+        atomicOr(p.status, ST_RANGE);
+    }
+  }
 }
 
 // Failure-detection self-test: warp 0 waits, with a limit of `limit_ns`, on
@@ -1580,12 +1914,96 @@ __global__ void selftest_wait_kernel(unsigned int *status, uint64_t limit_ns) {
   __syncthreads();
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+cudaError_t encode_fn() {
+  if (g_encode_tiled) return cudaSuccess;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult qr;
+  const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &qr);
+  if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+  g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// Geometry of the tensor map of x for the tensor-copy staging (fp32):
+// channels-first dims W, H, [D,] C, N with box BW x RIN x [1 x] chunk_ci;
+// channels-last dims C, W, H, [D,] N with box chunk_ci x LW x RIN [x 1].
+// The 3-D entry points always use the rank-5 form (a depth axis), whatever
+// the kernel depth.  Strides in bytes for dims 1.. (dim 0 is contiguous).
+struct XMapGeom {
+  int rank;
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
+};
+
+XMapGeom x_map_geometry(const ConvProblem &p, const TcPlan &q) {
+  XMapGeom g{};
+  const bool d3 = p.entry == 1;
+  const uint64_t C = p.C, D = p.D, H = p.H, W = p.W, N = p.N;
+  if (!p.cl) {
+    g.dims[0] = W; g.dims[1] = H;
+    g.box[0] = q.BW; g.box[1] = q.RIN;
+    if (d3) {
+      g.dims[2] = D; g.dims[3] = C; g.dims[4] = N;
+      g.box[2] = 1; g.box[3] = q.chunk_ci; g.box[4] = 1;
+      g.rank = 5;
+    } else {
+      g.dims[2] = C; g.dims[3] = N;
+      g.box[2] = q.chunk_ci; g.box[3] = 1;
+      g.rank = 4;
+    }
+  } else {
+    g.dims[0] = C; g.dims[1] = W; g.dims[2] = H;
+    g.box[0] = q.chunk_ci; g.box[1] = q.LW; g.box[2] = q.RIN;
+    if (d3) {
+      g.dims[3] = D; g.dims[4] = N;
+      g.box[3] = 1; g.box[4] = 1;
+      g.rank = 5;
+    } else {
+      g.dims[3] = N;
+      g.box[3] = 1;
+      g.rank = 4;
+    }
+  }
+  uint64_t st = 4;
+  for (int i = 0; i < g.rank - 1; ++i) {
+    st *= g.dims[i];
+    g.strides[i] = st;
+  }
+  return g;
+}
+
+// The tensor map itself: zeros outside the tensor, no swizzle.
+cudaError_t make_x_map(const ConvProblem &p, const TcPlan &q, CUtensorMap *m) {
+  cudaError_t e = encode_fn();
+  if (e != cudaSuccess) return e;
+  const XMapGeom g = x_map_geometry(p, q);
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5], es[5] = {1, 1, 1, 1, 1};
+  for (int i = 0; i < g.rank; ++i) {
+    dims[i] = g.dims[i];
+    box[i] = g.box[i];
+    if (i < g.rank - 1) strides[i] = g.strides[i];
+  }
+  const CUresult r = g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)g.rank,
+                                    const_cast<float *>(p.x), dims, strides, box, es,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int g_num_sms = 0;
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false, bool CL = false>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false, bool CL = false,
+          bool GP = false>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
-                          float *partial, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP, CL>;
+                          float *partial, const CUtensorMap &tm, cudaStream_t s) {
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP, CL, GP>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1597,46 +2015,59 @@ cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *
   }
   const long grid = q.units < g_num_sms ? q.units : g_num_sms;
   prof_begin(s);
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(p, q, bimg, partial);
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(p, q, bimg, partial, tm);
   prof_end(s, p.entry);
   return cudaGetLastError();
 }
 
 template <int PREC, int U, bool S2, bool CL = false>
 cudaError_t launch_chain(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
-                         float *partial, cudaStream_t s) {
+                         float *partial, const CUtensorMap &tm, cudaStream_t s) {
   switch (p.chain) {
-    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U, S2, false, CL>(p, q, bimg, partial, s);
+    case CHAIN_NONE: return launch_kernel<PREC, CHAIN_NONE, false, U, S2, false, CL>(p, q, bimg, partial, tm, s);
     case CHAIN_RELU_HARDSWISH:
-      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U, S2, false, CL>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_RELU_HARDSWISH, false, U, S2, false, CL>(p, q, bimg, partial, tm, s);
     case CHAIN_LEAKY_ADD_CLAMP_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U, S2, false, CL>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP_GELU, false, U, S2, false, CL>(p, q, bimg, partial, tm, s);
     case CHAIN_LEAKY_ADD_CLAMP1_GELU:
-      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U, S2, false, CL>(p, q, bimg, partial, s);
-    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U, S2, false, CL>(p, q, bimg, partial, s);
+      return launch_kernel<PREC, CHAIN_LEAKY_ADD_CLAMP1_GELU, false, U, S2, false, CL>(p, q, bimg, partial, tm, s);
+    default: return launch_kernel<PREC, CHAIN_GENERIC, false, U, S2, false, CL>(p, q, bimg, partial, tm, s);
   }
 }
 
 template <int PREC>
 cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
-                        float *partial, cudaStream_t s) {
-  if (p.subpix) return launch_kernel<PREC, CHAIN_NONE, true, 1, false, true>(p, q, bimg, partial, s);
-  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, s);
+                        float *partial, const CUtensorMap &tm, cudaStream_t s) {
+  if (p.subpix) return launch_kernel<PREC, CHAIN_NONE, true, 1, false, true>(p, q, bimg, partial, tm, s);
+  if (p.pool && q.GP) {  // general max pool: one tile per window row
+    switch (q.U) {
+      case 1: return launch_kernel<PREC, CHAIN_NONE, true, 1, false, false, false, true>(p, q, bimg, partial, tm, s);
+      case 2: return launch_kernel<PREC, CHAIN_NONE, true, 2, false, false, false, true>(p, q, bimg, partial, tm, s);
+      case 3: return launch_kernel<PREC, CHAIN_NONE, true, 3, false, false, false, true>(p, q, bimg, partial, tm, s);
+      default: return launch_kernel<PREC, CHAIN_NONE, true, 4, false, false, false, true>(p, q, bimg, partial, tm, s);
+    }
+  }
+  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, tm, s);
   // stride 2 (even / odd sub-plane staging) is its own instance, so the
   // stride-1 producer carries none of its index arithmetic
   if (q.S2)
-    return q.U == 2 ? launch_chain<PREC, 2, true>(p, q, bimg, partial, s)
-                    : launch_chain<PREC, 1, true>(p, q, bimg, partial, s);
+    return q.U == 2 ? launch_chain<PREC, 2, true>(p, q, bimg, partial, tm, s)
+                    : launch_chain<PREC, 1, true>(p, q, bimg, partial, tm, s);
   if (p.cl)  // channels-last input and output: its own instances
-    return q.U == 2 ? launch_chain<PREC, 2, false, true>(p, q, bimg, partial, s)
-                    : launch_chain<PREC, 1, false, true>(p, q, bimg, partial, s);
-  return q.U == 2 ? launch_chain<PREC, 2, false>(p, q, bimg, partial, s)
-                  : launch_chain<PREC, 1, false>(p, q, bimg, partial, s);
+    return q.U == 2 ? launch_chain<PREC, 2, false, true>(p, q, bimg, partial, tm, s)
+                    : launch_chain<PREC, 1, false, true>(p, q, bimg, partial, tm, s);
+  return q.U == 2 ? launch_chain<PREC, 2, false>(p, q, bimg, partial, tm, s)
+                  : launch_chain<PREC, 1, false>(p, q, bimg, partial, tm, s);
 }
 
 }  // namespace
 
 bool tc_supported(const ConvProblem &p, int prec) { return make_plan(p, prec).ok != 0; }
+
+int tc_uses_tma(const ConvProblem &p, int prec) {
+  const TcPlan q = make_plan(p, prec);
+  return q.ok && q.TMA;
+}
 
 cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaStream_t s) {
   selftest_wait_kernel<<<1, 64, 0, s>>>(status, limit_ns);
@@ -1644,7 +2075,7 @@ cudaError_t selftest_wait_launch(unsigned int *status, uint64_t limit_ns, cudaSt
 }
 
 size_t tc_weight_bytes(const ConvProblem &p) {
-  if (p.KH != 3 || p.KW != 3 || !(p.KD == 1 || p.KD == 3)) return 0;
+  if (!tc_kernel_ok(p)) return 0;
   size_t m = 0;
   for (int prec = 0; prec < 2; ++prec) {
     TcPlan q{};
@@ -1674,12 +2105,21 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
   float *partial = reinterpret_cast<float *>(static_cast<char *>(ws) + L.partial);
   const long nelem = (long)q.COB * q.NCH * q.KS * 2 * 128 * q.E;
   int blocks = (int)((nelem + 255) / 256);
-  if (blocks > 2048) blocks = 2048;
-  tc_pack_weights<<<blocks, 256, 0, s>>>(p, q, bimg);
+  if (blocks > kMaxPackBlocks) blocks = kMaxPackBlocks;
+  ConvProblem pp = p;
+  pp.wmax = reinterpret_cast<float *>(static_cast<char *>(ws) + L.wmax);
+  pp.wmax_n = blocks;
+  tc_pack_weights<<<blocks, 256, 0, s>>>(pp, q, bimg);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *launches = 1;
-  e = prec ? launch_prec<1>(p, q, bimg, partial, s) : launch_prec<0>(p, q, bimg, partial, s);
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof(tm));
+  if (q.TMA) {
+    e = make_x_map(p, q, &tm);
+    if (e != cudaSuccess) return e;
+  }
+  e = prec ? launch_prec<1>(pp, q, bimg, partial, tm, s) : launch_prec<0>(pp, q, bimg, partial, tm, s);
   if (e != cudaSuccess) return e;
   *launches += 1;
   if (p.pool) {

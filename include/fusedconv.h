@@ -1,8 +1,9 @@
 /*
  * fusedconv.h -- C ABI of libfusedconv: dense 2-D / 3-D convolutions
- * (stride 1 or 2, dilation 1 or 2) and a transposed convolution (stride 1
- * or 2) with their elementwise and reduction epilogues fused into the same
- * kernel, for one NVIDIA GB300 (sm_103a).
+ * (kernel sizes 1-7, strides and dilations 1-4, any padding up to 64) and a
+ * transposed convolution (kernel sizes 1-7, strides 1-4) with their
+ * elementwise and reduction epilogues fused into the same kernel, for one
+ * NVIDIA GB300 (sm_103a).
  *
  * Sources of the operations (three POPCORNBENCH reasoning traces):
  *  - fc_conv2d_epi: trace "Kimi-K2.6__l2_p57", problem statement and
@@ -68,7 +69,7 @@ typedef enum {
   FC_ERR_WORKSPACE = 4,   /* ws is NULL/misaligned or ws_bytes too small */
   FC_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
   FC_ERR_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device) */
-  FC_ERR_RANGE = 7        /* |x| or |w| beyond the fp16-split range (device) */
+  FC_ERR_RANGE = 7        /* x or w outside the fp16-split range (device) */
 } fc_status;
 
 /* Epilogue ops, applied in order to the conv output (bias already added). */
@@ -102,14 +103,20 @@ typedef struct {
 } fc_epilogue;
 
 /* How the contraction is computed.  AUTO picks per shape from a table of
- * measured times.  FFMA: fp32 CUDA-core register-blocked direct conv.
+ * measured times (fc_select_variant).  FFMA: fp32 CUDA-core
+ * register-blocked direct conv (fixed-size kernels for 3 x 3 (x 3) at
+ * stride / dilation 1-2, a general kernel for every other parameter).
  * TC_TF32X3: tcgen05 tensor cores, each fp32 operand split into a tf32
  * high part and a tf32 remainder, three products (hi*hi + hi*lo + lo*hi)
  * accumulated in fp32 in tensor memory.  TC_F16X3: the same split with fp16
  * parts (the remainder scaled by 2^11): same accuracy as TC_TF32X3 for
- * |x| < 65520 and |w| <= 65504 (fp16's largest finite value), twice the
- * tensor rate; values outside that range set FC_ERR_RANGE in the device
- * status word. */
+ * |x| < 65520 and |w| <= 65504 (fp16's largest finite value) as long as the
+ * data is not tiny throughout -- the largest |w|, and the largest |x| that a
+ * CTA stages, at least 2^-12 (below 2^-14 fp16 parts turn subnormal) --
+ * twice the tensor rate; data outside that range sets FC_ERR_RANGE in the
+ * device status word (run TC_TF32X3 or FFMA for it).  The tensor-core
+ * variants take square odd kernels up to 7 x 7 (cubic up to 5 x 5 x 5) at
+ * stride / dilation 1-2 where the plan fits shared memory. */
 typedef enum {
   FC_VARIANT_AUTO = 0,
   FC_VARIANT_FFMA = 1,
@@ -125,12 +132,15 @@ typedef enum {
  * and column ow*stride + kw*dilation - pad (the dilated extent is the one
  * trace "Kimi-K2.6__l2_p10" states for pooling windows; its l2_p57 trace
  * names the layer's stride / padding / dilation defaults 1 / 0 / 1).
- * Supported: stride 1 or 2, dilation 1 or 2, kH = kW = 3,
- * 0 <= pad <= 2 dilation, 1 <= C_in, 1 <= C_out, H + 2 pad and W + 2 pad
- * at least the dilated window 2 dilation + 1, and every tensor below 2^31
- * elements; every variant takes every stride / dilation pair (the
- * tensor-core variants stage stride 2 as even/odd row x column
- * sub-planes).  N = 0 is a valid empty call (nothing is launched). */
+ * Supported: kH, kW 1..7, stride 1..4, dilation 1..4, 0 <= pad <= 64,
+ * 1 <= C_in, 1 <= C_out, H + 2 pad and W + 2 pad at least the dilated
+ * window, fewer than 2^31 elements per image of x, of y and in w (whole
+ * tensors may be larger: offsets are 64-bit).  FFMA takes all of it;
+ * the tensor-core variants the square odd kernels at stride / dilation
+ * 1-2 whose plan fits (they stage stride 2 as even/odd row x column
+ * sub-planes).  N = 0 is a valid empty call (nothing is launched).
+ * Argument order: the survey's boundary lists (..., stride, pad, epi, ...);
+ * `dilation` is inserted after `pad` (every variant takes it). */
 FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,
                         int pad, int dilation, const fc_epilogue *epi, float *y,
@@ -162,8 +172,11 @@ FC_API fc_status fc_conv2d_epi_noalloc(const float *x, int N, int C_in, int H, i
  * y [N][C_out][Do][Ho][Wo], each extent
  * (in + 2 pad - dilation (k - 1) - 1) / stride + 1, output (od, oh, ow)
  * reading input od*stride + kd*dilation - pad on each axis.
- * Supported: stride 1 or 2, dilation 1 or 2 (on every variant, as for
- * fc_conv2d_epi), kD = kH = kW = 3, 0 <= pad <= 2 dilation. */
+ * Supported: kD, kH, kW 1..7, stride 1..4, dilation 1..4, pad 0..64 (the
+ * same padding on every axis), as for fc_conv2d_epi; the general
+ * CUDA-core kernel refuses (FC_ERR_UNSUPPORTED) a layer whose staged window
+ * for one input channel exceeds its shared memory (large kernels at large
+ * strides and dilations). */
 FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, int W,
                         const float *w, int C_out, int kD, int kH, int kW,
                         int stride, int pad, int dilation, const fc_epilogue *epi,
@@ -173,12 +186,15 @@ FC_API fc_status fc_conv3d_epi(const float *x, int N, int C_in, int D, int H, in
  * arguments (sizes as N, C_in, [D,] H, W; weights [C_out][C_in][k...] as
  * there), but x is [N][H][W][C_in] ([N][D][H][W][C_in]) and y is
  * [N][Ho][Wo][C_out] ([N][Do][Ho][Wo][C_out]).  A pixel's channels are then
- * adjacent, so the kernel reads them (and writes its outputs) as 16-byte
- * vectors when C_in (C_out) is a multiple of 4.  Tensor-core variants only
- * (FC_VARIANT_FFMA returns FC_ERR_UNSUPPORTED; AUTO picks the tensor
- * cores); stride 1 (dilation 1 or 2, pads as above); stride 2 returns
- * FC_ERR_UNSUPPORTED.  Workspace: fc_workspace_bytes(0 or 1, ...) as for
- * the channels-first calls. */
+ * adjacent: with C_in a multiple of 4 a tiled tensor copy (TMA) brings each
+ * channel chunk's input halo -- rows of pixels of chunk_ci channels -- into
+ * shared memory in one operation (fc_set_staging), else the producers read
+ * pixels as 16-byte vectors; outputs are written as 16-byte vectors when
+ * C_out is a multiple of 4.  Tensor-core variants only (FC_VARIANT_FFMA
+ * returns FC_ERR_UNSUPPORTED; AUTO picks the tensor cores): stride 1, the
+ * kernels and dilations the tensor-core variants take; other parameters
+ * return FC_ERR_UNSUPPORTED.  Workspace: fc_workspace_bytes(0 or 1, ...) as
+ * for the channels-first calls. */
 FC_API fc_status fc_conv2d_epi_nhwc(const float *x, int N, int C_in, int H, int W,
                                     const float *w, int C_out, int kH, int kW, int stride,
                                     int pad, int dilation, const fc_epilogue *epi, float *y,
@@ -191,43 +207,81 @@ FC_API fc_status fc_conv3d_epi_ndhwc(const float *x, int N, int C_in, int D, int
 /* ConvTranspose2d + bias -> MaxPool2d -> Hardtanh[a,b] -> mean(H,W)
  * -> tanh.  x [N][C_in][H][W]; w [C_in][C_out][k][k];
  * y [N][C_out][1][1].  The epilogue chain must be exactly
- * MAXPOOL2X2 (or MAXPOOL(k_p, s_p)), HARDTANH(a, b), MEAN_HW, TANH.  A
- * general window (k_p, s_p) other than 2 / 2 -- overlapping or not, floor
- * extent, the general max-pool of trace "Kimi-K2.6__l2_p10" -- runs at
- * stride 1 on the CUDA-core variant only (the tensor-core variants return
- * FC_ERR_UNSUPPORTED; AUTO picks FFMA), the conv output never leaving the
- * kernel.  Supported: k = 3, pad 1 and
- *   stride 1, out_pad 0: conv output extent Ho = H, Wo = W (H, W >= 2);
- *   stride 2, out_pad 0 or 1: Ho = 2H - 1 + out_pad (likewise Wo; the
- *   output-size formula (H-1)s - 2p + k + op of trace "Kimi-K2.6__l2_p10"),
- *   computed per output parity class on the tensor-core variants only
- *   (FC_VARIANT_FFMA returns FC_ERR_UNSUPPORTED; AUTO picks tensor cores).
- * The 2x2 pool takes the floor extent (Ho / 2, Wo / 2).  The mean is
- * reduced in a fixed order (per-tile partials, then a second kernel sums
- * them in index order), so results are bitwise reproducible. */
+ * MAXPOOL2X2 (or MAXPOOL(k_p, s_p), window and stride 1..4), HARDTANH(a, b),
+ * MEAN_HW, TANH.  Transposed-conv output extent Ho = (H - 1) stride -
+ * 2 pad + k + out_pad (likewise Wo; the output-size formula of trace
+ * "Kimi-K2.6__l2_p10"), pooled with the floor extent (Ho - k_p) / s_p + 1.
+ * Supported: k 1..7, stride 1..4, 0 <= pad <= 64, 0 <= out_pad < stride,
+ * Ho, Wo >= k_p.  How each form runs:
+ *   stride 1, pad <= k - 1: the equivalent conv (swapped channel axes,
+ *     flipped taps, padding k - 1 - pad) -- tensor cores for odd k (2x2/2
+ *     pool: two conv rows per unit; other windows: one tile per window row,
+ *     windows taken in shared memory), CUDA cores for every k;
+ *   stride 2, k 3, pad 1, 2x2/2 pool: per output parity class on the input
+ *     grid (tensor cores); the general CUDA-core kernel for FFMA;
+ *   anything else: the general CUDA-core kernel (the zero-inserted input
+ *     staged in shared memory), FFMA only.
+ * The conv output never leaves the kernel.  The mean is reduced in a fixed
+ * order (per-tile partials, then a second kernel sums them in index order),
+ * so results are bitwise reproducible. */
 FC_API fc_status fc_convT2d_pool_mean(const float *x, int N, int C_in, int H, int W,
                                const float *w, int C_out, int k, int stride,
                                int pad, int out_pad, const fc_epilogue *epi,
                                float *y, void *ws, size_t ws_bytes,
                                void *stream);
 
-/* Workspace bytes needed by one call.  entry: 0 = fc_conv2d_epi,
- * 1 = fc_conv3d_epi, 2 = fc_convT2d_pool_mean (any supported stride and
- * out_pad, 2x2 pool), 3 = fc_convT2d_pool_mean with a general pool window.
+/* Workspace bytes needed by one call.  entry: 0 = fc_conv2d_epi (and the
+ * _nhwc / _noalloc forms), 1 = fc_conv3d_epi (and _ndhwc),
+ * 2 = fc_convT2d_pool_mean with the 2x2 pool (any supported stride and
+ * out_pad), 3 = fc_convT2d_pool_mean with a general pool window.
  * dims:
  *   entry 0: {N, C_in, H, W, C_out, k, pad}
  *   entry 1: {N, C_in, D, H, W, C_out, k, pad}
  *   entry 2: {N, C_in, H, W, C_out, k, pad}
- *   entry 3: {N, C_in, H, W, C_out, k, pad, stride (1), out_pad (0),
+ *   entry 3: {N, C_in, H, W, C_out, k, pad, stride, out_pad,
  *             pool window, pool stride}
  * The size covers every variant, so it does not depend on the selection.
  * Returns 0 for an invalid entry or NULL dims. */
 FC_API size_t fc_workspace_bytes(int entry, const int *dims);
 
+/* The variant a call would run (FC_VARIANT_AUTO's choice, or the override
+ * set by fc_set_variant), without a device and without running anything:
+ * the automatic choice takes, among the shapes of a table of kernel times
+ * measured per variant on a GB300 (same entry point, kernel size, stride,
+ * dilation, layout and pool window), the one nearest in log2 of the MAC
+ * count and of the channel counts, and its fastest variant this problem
+ * supports.  entry / dims:
+ *   0 fc_conv2d_epi, 4 fc_conv2d_epi_nhwc:
+ *     {N, C_in, H, W, C_out, k, stride, pad, dilation}
+ *   1 fc_conv3d_epi, 5 fc_conv3d_epi_ndhwc:
+ *     {N, C_in, D, H, W, C_out, k, stride, pad, dilation}
+ *   2 fc_convT2d_pool_mean:
+ *     {N, C_in, H, W, C_out, k, stride, pad, out_pad, pool window, pool stride}
+ * Returns an fc_variant (1 .. 3), or -1 for an invalid or unsupported
+ * problem (or an override the problem does not support).  The pages have
+ * no counterpart: it exposes the library's own selection. */
+FC_API int fc_select_variant(int entry, const int *dims);
+
 /* Process-wide variant override (FC_VARIANT_AUTO restores the automatic
  * choice).  Returns FC_ERR_INVALID_ARG for an unknown value.  Not
  * synchronised with calls running on other host threads. */
 FC_API fc_status fc_set_variant(int variant);
+
+/* How the tensor-core variants bring x into shared memory (process-wide,
+ * like fc_set_variant).  1: tiled tensor copies (TMA) of the input halo --
+ * one copy per channel chunk and depth slice into a ring of raw fp32 slots,
+ * zeros outside the tensor supplied by the copy -- which producer warps then
+ * split into the hi / lo operand slices; used where the plan allows it
+ * (stride 1, channels-first W or channels-last C_in a multiple of 4, room
+ * in shared memory), register loads elsewhere.  0: register loads by the
+ * producer warps everywhere.  -1 (the default): chosen per shape together
+ * with the variant, from the measured table (see fc_select_variant).  All
+ * give the same results.  FC_ERR_INVALID_ARG for another value. */
+FC_API fc_status fc_set_staging(int mode);
+
+/* The input staging the calling thread's last successful entry-point call
+ * used: 1 tensor copies, 0 register loads (and the CUDA-core variant). */
+FC_API int fc_last_staging(void);
 
 /* The variant the calling thread's last successful entry-point call used. */
 FC_API int fc_last_variant(void);

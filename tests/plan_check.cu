@@ -31,11 +31,86 @@ void check_stage(const char *name, const ConvProblem &p, const TcPlan &q, int n,
   StageSrc ss{};
   ss.xn = (long)n * p.C * p.D * p.H * p.W;
   ss.id0 = od * p.stride - p.pad_d;
-  ss.ih0 = rt * q.U * q.R * p.stride - p.pad;
-  ss.iw0 = ct * q.WT * p.stride - p.pad;
+  ss.ih0 = rt * q.ROWSTEP * p.stride - p.pad;
+  ss.iw0 = ct * q.COLSTEP * p.stride - p.pad;
   ss.ci0 = 0;
   const int nrows = p.KD * q.RIN, jobs = q.P * nrows;
   const int s2sub = q.S2 ? q.SUB : 0;
+  if (q.TMA) {
+    // tensor-copy staging: replay the converters' items against the copy's
+    // box layout (which x element each raw slot float holds)
+    REQ(!q.S2 && !q.SP && q.LW == q.RS, "%s TMA plan geometry", name);
+    const int iwt = ss.iw0 - (p.cl ? 0 : q.coff);
+    REQ(p.cl || (iwt % 4 + 4) % 4 == 0, "%s tensor copy starts at column %d (not 16-byte aligned)",
+        name, iwt);
+    const int items = q.P * q.RIN * q.LW;
+    // the tensor map: the box coordinates the loader passes (innermost
+    // first, as in the kernel) and the map's strides must address the x
+    // element the converter expects at every raw float
+    const XMapGeom mg = x_map_geometry(p, q);
+    REQ(mg.rank == (p.entry == 1 ? 5 : 4), "%s map rank", name);
+    long boxn = 1;
+    for (int i = 0; i < mg.rank; ++i) boxn *= mg.box[i];
+    REQ(boxn * 4 == q.raw_tx, "%s box bytes %ld vs %d", name, boxn * 4, q.raw_tx);
+    for (int kd = 0; kd < p.KD; ++kd) {
+      const int id = ss.id0 + kd * p.dil;
+      long c0[5];
+      if (p.cl) { c0[0] = 0; c0[1] = iwt; c0[2] = ss.ih0; c0[3] = p.entry == 1 ? id : n; c0[4] = n; }
+      else { c0[0] = iwt; c0[1] = ss.ih0; c0[2] = p.entry == 1 ? id : 0; c0[3] = p.entry == 1 ? 0 : n; c0[4] = n; }
+      for (long f = 0; f < boxn; f += 7) {  // every 7th float of the box
+        long rem = f, off = 0;
+        bool inside = true;
+        long co[5];
+        for (int i = 0; i < mg.rank; ++i) {
+          co[i] = c0[i] + rem % mg.box[i];
+          rem /= mg.box[i];
+          if (co[i] < 0 || co[i] >= (long)mg.dims[i]) inside = false;
+          off += co[i] * (i ? (long)mg.strides[i - 1] / 4 : 1);
+        }
+        if (!inside) continue;
+        // expected element offset of the same coordinates in x's own layout
+        long want;
+        if (p.cl) {
+          const long c = co[0], w = co[1], h = co[2], d = p.entry == 1 ? co[3] : 0,
+                     nn = p.entry == 1 ? co[4] : co[3];
+          want = (((nn * p.D + d) * p.H + h) * p.W + w) * p.C + c;
+        } else {
+          const long w = co[0], h = co[1], d = p.entry == 1 ? co[2] : 0,
+                     c = p.entry == 1 ? co[3] : co[2], nn = p.entry == 1 ? co[4] : co[3];
+          want = (((nn * p.C + c) * p.D + d) * p.H + h) * p.W + w;
+        }
+        REQ(off == want, "%s map offset %ld, x offset %ld", name, off, want);
+      }
+    }
+    for (int kd = 0; kd < p.KD; ++kd)
+      for (int it = 0; it < items; ++it) {
+        const int row = (int)fdiv((uint32_t)it, q.fd_lw), cc = it - row * q.LW;
+        REQ(row == it / q.LW, "%s fast division by LW", name);
+        const int pl = row >= q.RIN ? 1 : 0, r = row - pl * q.RIN;
+        for (int e = 0; e < q.E; ++e) {
+          long f;  // raw float read by the converter (as in the kernel)
+          if (p.cl) f = ((long)r * q.LW + cc) * q.chunk_ci + pl * q.E + e;
+          else f = ((long)pl * q.E * q.RIN + r) * q.BW + cc + q.coff + (long)e * q.RIN * q.BW;
+          REQ(f >= 0 && f < q.raw_tx / 4, "%s raw read %ld outside the slot", name, f);
+          int xc, xr, xw;  // x coordinates the copy put there
+          if (p.cl) { xc = (int)(f % q.chunk_ci); xw = iwt + (int)((f / q.chunk_ci) % q.LW); xr = ss.ih0 + (int)(f / ((long)q.chunk_ci * q.LW)); }
+          else { xw = iwt + (int)(f % q.BW); xr = ss.ih0 + (int)((f / q.BW) % q.RIN); xc = (int)(f / ((long)q.BW * q.RIN)); }
+          REQ(xc == pl * q.E + e && xr == ss.ih0 + r && xw == ss.iw0 + cc,
+              "%s converter item (%d,%d,%d,e%d) reads x (%d,%d,%d)", name, pl, r, cc, e, xc, xr, xw);
+        }
+        const long a = (long)pl * plane_px + kd * q.DSL + (long)r * q.RS + cc;
+        REQ(a >= 0 && a < plane_px * q.P, "%s converter store outside hi planes", name);
+        if (a < 0 || a >= plane_px * q.P) continue;
+        const int id = ss.id0 + kd * p.dil, ih = ss.ih0 + r, iw = ss.iw0 + cc;
+        const bool in = id >= 0 && id < p.D && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W;
+        for (int hl = 0; hl < 2; ++hl) {
+          const long aa = a + hl * q.P * plane_px;
+          cnt[aa]++;
+          REQ(cnt[aa] == 1, "%s pixel %ld written twice (TMA)", name, aa);
+          who[aa] = Px{id, ih, iw, pl, !in};
+        }
+      }
+  } else {
   const int G = q.LW >> 5, parts = q.S2 ? (G + 3) >> 2 : (G ? 1 : 0), tail = q.LW - 32 * G, mjobs = jobs * parts;
   const int njobs = mjobs + (jobs * tail + 31) / 32;
   std::vector<std::pair<int, int>> stores;  // (row job, column)
@@ -69,6 +144,7 @@ void check_stage(const char *name, const ConvProblem &p, const TcPlan &q, int n,
       }
     }
   }
+  }
   // MMA operand reads for valid outputs
   for (int ks = 0; ks < q.KS; ++ks)
     for (int half = 0; half < 2; ++half) {
@@ -99,7 +175,7 @@ void check_stage(const char *name, const ConvProblem &p, const TcPlan &q, int n,
       }
       REQ(off >= 0 && off < (1 << 14), "%s K offset %ld", name, off);
       if (tap >= q.TAPS) continue;  // zero-weight slot: any finite data
-      const int kd = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+      const int kd = tap / (q.KH * q.KW), kh = (tap / q.KW) % q.KH, kw = tap % q.KW;
       for (int t = 0; t < q.U; ++t)
         for (int m = 0; m < 128; ++m)
           for (int hl = 0; hl < 2; ++hl) {
@@ -107,7 +183,10 @@ void check_stage(const char *name, const ConvProblem &p, const TcPlan &q, int n,
             REQ(a >= 0 && a < tot_px, "%s MMA read outside the stage (ks %d m %d)", name, ks, m);
             if (a < 0 || a >= tot_px) continue;
             const int r = m / q.RS, c = m % q.RS;
-            const int oh = (rt * q.U + t) * q.R + r, ow = ct * q.WT + c;
+            // the output pixel the epilogue assigns to this M row (its own
+            // formulas, independent of the plan's unit steps)
+            const int oh = q.GP ? rt * p.ps + t : (rt * q.U + t) * q.R + r;
+            const int ow = q.GP ? ct * q.PJ * p.ps + c : ct * q.WT + c;
             const bool valid = q.SP ? (r < q.R && c < q.WT && oh < p.Ho / 2 && ow < p.Wo / 2)
                                     : (r < q.R && c < q.WT && oh < p.Ho && ow < p.Wo);
             if (!valid) continue;
@@ -136,23 +215,31 @@ void check_stage(const char *name, const ConvProblem &p, const TcPlan &q, int n,
 }
 
 void check(const char *name, ConvProblem p) {
-  for (int prec = 0; prec < 2; ++prec) {
+  for (int pv = 0; pv < 4; ++pv) {  // both precisions, both input stagings
+    const int prec = pv & 1;
+    p.staging = pv >> 1;
     TcPlan q = make_plan(p, prec);
+    if (pv >= 2 && !q.TMA) continue;  // the tensor-copy plan fell back to loads: checked above
     if (!q.ok) { printf("%s prec%d: not supported\n", name, prec); continue; }
-    printf("%s prec%d: S2=%d U=%d P=%d NCH=%d KS=%d pair=%d R=%d RS=%d WT=%d RIN=%d LW=%d SR=%d DSL=%d NPIX=%d S=%d res=%d units=%ld smem=%d\n",
-           name, prec, q.S2, q.U, q.P, q.NCH, q.KS, q.pairtaps, q.R, q.RS, q.WT, q.RIN, q.LW, q.SR, q.DSL, q.NPIX, q.S, q.b_resident, q.units, q.smem_bytes);
+    printf("%s prec%d st%d: S2=%d U=%d P=%d NCH=%d KS=%d pair=%d R=%d RS=%d WT=%d RIN=%d LW=%d SR=%d DSL=%d NPIX=%d S=%d res=%d units=%ld smem=%d TMA=%d TR=%d\n",
+           name, prec, p.staging, q.S2, q.U, q.P, q.NCH, q.KS, q.pairtaps, q.R, q.RS, q.WT, q.RIN, q.LW, q.SR, q.DSL, q.NPIX, q.S, q.b_resident, q.units, q.smem_bytes, q.TMA, q.TR);
     REQ(q.smem_bytes + 1024 <= 227 * 1024, "smem %d", q.smem_bytes);
     REQ(q.off_misc + (int)sizeof(SmemCtl) <= q.smem_bytes, "misc");
     REQ(q.off_misc % 16 == 0 && q.off_b % 16 == 0 && q.a_stage_bytes % 16 == 0 && q.plane_bytes % 16 == 0, "align");
     REQ(q.R * q.RS <= 128 || (q.R == 1 && q.WT == 128), "tile");
-    REQ(((long)q.S * q.a_stage_bytes) == q.off_b, "stages end at B");
+    REQ(((long)q.S * q.a_stage_bytes) == q.off_raw, "stages end at the raw slots");
+    REQ((long)q.off_raw + (long)q.TR * q.raw_bytes == q.off_b, "raw slots end at B");
+    REQ(q.off_raw % 128 == 0 && q.raw_bytes % 128 == 0, "raw slots 128-byte aligned");
+    REQ(!q.TMA || (q.TR >= 2 && q.TR <= 4 && q.BW <= 256 && q.RIN <= 256 && q.chunk_ci <= 256),
+        "TMA ring / box");
+    REQ(!q.TMA || p.cl || (q.BW % 4 == 0 && (((-p.pad - q.coff) % 4) + 4) % 4 == 0), "TMA x alignment");
     REQ((((long)q.off_b + (q.b_resident ? (long)q.COB * q.NCH * q.b_chunk_bytes : (long)q.SB * q.b_chunk_bytes)) >> 4) < (1 << 14), "B desc range");
-    std::vector<int> seen(28, 0);
-    for (int k = 0; k < 28; ++k) if (q.perm[k] < q.TAPS) seen[q.perm[k]]++;
+    std::vector<int> seen(kMaxTaps + 2, 0);
+    for (int k = 0; k < kMaxTaps + 2; ++k) if (q.perm[k] < q.TAPS) seen[q.perm[k]]++;
     for (int t = 0; t < q.TAPS; ++t) REQ(seen[t] == 1, "%s perm", name);
     const int n = p.N - 1;
-    const int ods[2] = {0, p.Do - 1}, rts[3] = {0, q.n_rt / 2, q.n_rt - 1}, cts[2] = {0, q.n_ct - 1};
-    for (int a : ods) for (int b : rts) for (int c : cts) check_stage(name, p, q, n, a, b, c);
+    const int ods[2] = {0, p.Do - 1}, rts[3] = {0, q.n_rt / 2, q.n_rt - 1};
+    for (int a : ods) for (int b : rts) for (int c = 0; c < q.n_ct; ++c) check_stage(name, p, q, n, a, b, c);
   }
 }
 
@@ -163,14 +250,27 @@ ConvProblem conv2d(int N, int C, int H, int W, int CO, int pad, int stride = 1, 
 }
 ConvProblem conv3d(int N, int C, int D, int H, int W, int CO, int pad, int stride = 1, int dil = 1) {
   ConvProblem p = conv2d(N, C, H, W, CO, pad, stride, dil); p.D = D; p.KD = 3; p.pad_d = pad;
+  p.entry = 1;
   p.Do = (D + 2 * pad - 2 * dil - 1) / stride + 1; return p;
+}
+// kernel size k (square / cubic)
+ConvProblem convk(int N, int C, int D, int H, int W, int CO, int k, int pad, int stride = 1,
+                  int dil = 1, bool d3 = false) {
+  ConvProblem p{}; p.N = N; p.C = C; p.D = D; p.H = H; p.W = W; p.CO = CO;
+  p.KD = d3 ? k : 1; p.KH = p.KW = k; p.pad = pad; p.pad_d = d3 ? pad : 0;
+  p.stride = stride; p.dil = dil; p.entry = d3 ? 1 : 0;
+  const int span = (k - 1) * dil + 1;
+  p.Do = d3 ? (D + 2 * pad - span) / stride + 1 : 1;
+  p.Ho = (H + 2 * pad - span) / stride + 1; p.Wo = (W + 2 * pad - span) / stride + 1; return p;
 }
 ConvProblem convT2(int N, int C, int H, int W, int CO, int op) {
   ConvProblem p = conv2d(N, C, H, W, CO, 0); p.pool = 1; p.wlayout = 1; p.subpix = 1;
+  p.pk = p.ps = 2; p.tstride = 2; p.tpad = 1; p.entry = 2;
   p.Ho = 2 * H - 1 + op; p.Wo = 2 * W - 1 + op; return p;
 }
-ConvProblem convT(int N, int C, int H, int W, int CO) {
-  ConvProblem p = conv2d(N, C, H, W, CO, 1); p.pool = 1; p.wlayout = 1; return p;
+ConvProblem convT(int N, int C, int H, int W, int CO, int pk = 2, int ps = 2) {
+  ConvProblem p = conv2d(N, C, H, W, CO, 1); p.pool = 1; p.wlayout = 1; p.pk = pk; p.ps = ps;
+  p.tstride = 1; p.tpad = 1; p.entry = 2; return p;
 }
 int main() {
   check("cfg1", conv2d(4, 8, 32, 32, 64, 0));
@@ -214,6 +314,40 @@ int main() {
   check("d2s2-3d-c", conv3d(2, 8, 11, 12, 20, 64, 2, 2, 2));
   check("d2s2-3d-d", conv3d(2, 8, 11, 10, 12, 64, 1, 2, 2));
   check("d2-3d-c", conv3d(1, 16, 8, 20, 70, 64, 0, 1, 2));
+  {  // channels-last (tensor-copy staging reads pixel-major slots)
+    ConvProblem a = conv2d(2, 8, 33, 36, 64, 0); a.cl = 1; check("cl-a", a);
+    ConvProblem b = conv2d(1, 12, 17, 20, 70, 1); b.cl = 1; check("cl-b", b);
+    ConvProblem c = conv2d(1, 16, 9, 150, 64, 2, 1, 2); c.cl = 1; check("cl-c", c);
+    ConvProblem d = conv3d(2, 8, 6, 10, 30, 64, 1); d.cl = 1; check("cl-3d", d);
+    ConvProblem e = conv2d(2, 64, 10, 30, 64, 1); e.cl = 1; check("cl-c64", e);
+  }
+  // general max pool on the tensor cores: one tile per window row
+  check("gp-3s2", convT(2, 16, 17, 21, 64, 3, 2));
+  check("gp-4s4", convT(1, 8, 20, 40, 70, 4, 4));
+  check("gp-2s1", convT(1, 8, 12, 40, 64, 2, 1));
+  check("gp-1s1", convT(1, 8, 6, 7, 64, 1, 1));
+  check("gp-3s3-wide", convT(1, 64, 9, 300, 64, 3, 3));
+  check("gp-3s2-big", convT(16, 64, 256, 256, 64, 3, 2));
+  check("gp-3s2-strips", convT(2, 8, 9, 260, 64, 3, 2));
+  check("gp-3s3-strips", convT(1, 8, 9, 300, 64, 3, 3));
+  check("gp-4s2-strips", convT(1, 8, 9, 520, 64, 4, 2));
+  // kernel sizes 1, 5, 7 (2-D) and 1, 5 (3-D), strides / dilations 1-2
+  check("k1", convk(2, 8, 1, 20, 36, 64, 1, 0));
+  check("k1-c64", convk(1, 64, 1, 9, 40, 70, 1, 0));
+  check("k5", convk(2, 8, 1, 21, 37, 64, 5, 2));
+  check("k5-s2", convk(1, 16, 1, 19, 140, 64, 5, 1, 2));
+  check("k5-d2", convk(1, 8, 1, 25, 60, 64, 5, 4, 1, 2));
+  check("k7", convk(1, 8, 1, 23, 44, 64, 7, 3));
+  check("k7-wide", convk(1, 12, 1, 12, 300, 70, 7, 0));
+  check("k7-s2-d2", convk(1, 8, 1, 30, 70, 64, 7, 6, 2, 2));
+  check("k1-3d", convk(1, 8, 6, 9, 20, 64, 1, 0, 1, 1, true));
+  check("k5-3d", convk(1, 8, 9, 12, 20, 64, 5, 2, 1, 1, true));
+  check("k5-3d-s2", convk(1, 8, 11, 13, 30, 64, 5, 1, 2, 1, true));
+  // channels-first shapes that take the tensor copies (W a multiple of 4)
+  check("tma-pad1-strips", conv2d(1, 8, 9, 260, 64, 1));
+  check("tma-pad3-d2", conv2d(1, 8, 11, 132, 64, 3, 1, 2));
+  check("tma-c12", conv2d(2, 12, 17, 20, 70, 1));
+  check("tma-3d-d2", conv3d(1, 8, 8, 12, 36, 64, 2, 1, 2));
   printf(fails ? "CHECK FAILED (%d)\n" : "CHECK OK\n", fails);
   return fails != 0;
 }

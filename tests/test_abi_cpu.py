@@ -72,12 +72,13 @@ def test_host_validation_rejects_before_launch(L):
     assert _conv2d(L, N=-1) == INVALID
     assert _conv2d(L, C=0) == INVALID
     assert _conv2d(L, stride=0) == INVALID
-    assert _conv2d(L, stride=3) == UNSUP  # stride 1 and 2 are supported
-    assert _conv2d(L, k=5) == UNSUP
-    assert _conv2d(L, pad=3) == UNSUP
+    assert _conv2d(L, stride=5) == UNSUP  # strides 1 .. 4 are supported
+    assert _conv2d(L, k=8) == UNSUP      # kernel sizes 1 .. 7
+    assert _conv2d(L, k=9, H=20, W=20) == UNSUP
+    assert _conv2d(L, pad=65) == UNSUP   # padding up to 64
     assert _conv2d(L, dilation=0) == INVALID
-    assert _conv2d(L, dilation=3) == UNSUP  # dilation 1 and 2 are supported
-    assert _conv2d(L, dilation=2, pad=5) == UNSUP  # pad at most 2 x dilation
+    assert _conv2d(L, dilation=5) == UNSUP  # dilations 1 .. 4
+    assert _conv2d(L, stride=4, k=7, dilation=4, pad=3, H=30, W=30, N=0) == 0  # valid
     assert _conv2d(L, H=2) == INVALID  # Ho = 0
     assert _conv2d(L, H=4, dilation=2) == INVALID  # window of 5 rows over 4
     assert _conv2d(L, H=4, W=4, dilation=2, pad=1, N=0) == 0  # 6 padded rows: valid
@@ -96,13 +97,17 @@ def test_pool_entry_requires_exact_chain(L):
     assert st == 2
     e, _ = _epi(fc.pool_mean_ops())
     st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
-                                4, 3, 3, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
+                                4, 3, 5, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
                                 ctypes.c_void_p(256), 1 << 20, None)
-    assert st == 2  # stride 3 is not supported (1 and 2 are)
+    assert st == 2  # stride 5 is not supported (1 .. 4 are)
     st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
                                 4, 3, 1, 1, 1, ctypes.byref(e), ctypes.c_void_p(16),
                                 ctypes.c_void_p(256), 1 << 20, None)
-    assert st == 2  # output padding 1 only with stride 2
+    assert st == 1  # output padding must be below the stride
+    st = L.fc_convT2d_pool_mean(ctypes.c_void_p(16), 1, 4, 8, 8, ctypes.c_void_p(16),
+                                4, 8, 1, 1, 0, ctypes.byref(e), ctypes.c_void_p(16),
+                                ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 2  # kernel sizes 1 .. 7
 
 
 def test_no_cpu_fallback_without_gpu(L):
@@ -159,10 +164,11 @@ def test_general_pool_chain_validation(L):
     assert pool_call((5, 2)) == UNSUP      # window above 4
     assert pool_call((3, 0)) == UNSUP      # stride below 1
     assert pool_call((2.5, 2)) == UNSUP    # not an integer
-    assert pool_call((3, 2), stride=2, out_pad=1) == UNSUP  # general pool at stride 2
-    # workspace entry 3 (general pool) covers its per-tile partials
+    # workspace entry 3 (general pool) covers its per-tile partials, at any
+    # supported stride / output padding
     assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 1, 0, 3, 2)) > 0
-    assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 2, 1, 3, 2)) == 0  # stride 2: no
+    assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 2, 1, 3, 2)) > 0
+    assert fc.workspace_bytes(3, (2, 8, 20, 20, 64, 3, 1, 2, 2, 3, 2)) == 0  # out_pad >= stride
 
 
 def test_binding_refuses_wrong_output_shapes_before_any_launch():

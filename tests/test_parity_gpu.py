@@ -378,6 +378,38 @@ def test_f16_split_range_boundary():
         m.set_variant("auto")
 
 
+@pytest.mark.parametrize("scale_exp", [8, 16, 24])
+def test_small_magnitudes_relative_accuracy(scale_exp):
+    """x and w scaled by 2^-e, compared with rtol = 1e-4 and atol = 0 on the
+    outputs that are not near zero (so the relative error decides, which
+    the suite's atol hides at the workloads' scales).  tf32x3 keeps fp32's
+    exponent range: it passes at every scale.  f16x3's parts are fp16: it
+    passes while the data's largest magnitude is at least 2^-12 (x ~ N(0,1)
+    2^-8 has max ~2^-6, w ~ 2^-11) and reports FC_ERR_RANGE below that
+    (2^-16, 2^-24) instead of a less accurate result."""
+    st = synth.seeded(3000 + scale_exp)
+    x = (st.normal((2, 8, 20, 36)) * np.float32(2.0 ** -scale_exp)).astype(np.float32)
+    w = (st.uniform((64, 8, 3, 3), 1.0 / np.sqrt(72.0)) * np.float32(2.0 ** -scale_exp)).astype(
+        np.float32)
+    ref = oracle.conv_epi(x, w, None, (), pad=1)
+    sel = np.abs(ref) >= 0.05 * np.abs(ref).max()
+    m = fc()
+    for variant in ("tc_tf32x3", "tc_f16x3"):
+        m.set_variant(variant)
+        try:
+            y = m.fc_conv2d_epi(_dev(x), _dev(w), None, (), pad=1).cpu().numpy()
+            assert m.last_variant() == variant
+            status = m.get_last_device_error()
+        finally:
+            m.set_variant("auto")
+        if variant == "tc_f16x3" and scale_exp >= 16:
+            assert status == 7, f"f16x3 at 2^-{scale_exp}: status {status}, FC_ERR_RANGE expected"
+            continue
+        assert status == 0
+        rel = np.abs(y[sel] - ref[sel]) / np.abs(ref[sel])
+        assert rel.max() <= 1e-4, f"{variant} at 2^-{scale_exp}: max relative error {rel.max():.3g}"
+
+
 @pytest.mark.parametrize("k,s,shape,ht", [
     (2, 2, (2, 5, 36, 40), (-1.0, 1.0)),    # the configs' pooling, even extents
     (2, 2, (1, 3, 37, 41), (-1.0, 1.0)),    # odd extents: last row / column dropped
@@ -584,16 +616,229 @@ def test_convT_stride2_pool_mean(variant, shape, op):
     _check(got, ref, f"{variant} convT stride 2 {shape} op {op}")
 
 
-def test_convT_stride2_refused_by_cuda_core_variant():
+@pytest.mark.parametrize("shape,op", [((2, 16, 12, 20, 64), 1), ((1, 8, 9, 33, 70), 0)])
+def test_convT_stride2_pool_mean_cuda_cores(shape, op):
+    """The CUDA-core variant computes the stride-2 transposed conv with the
+    general kernel (zero-inserted input staged in shared memory)."""
+    N, C, H, W, CO = shape
+    st = synth.seeded(765 + C + op)
+    x = st.normal((N, C, H, W))
+    w = st.uniform((C, CO, 3, 3), 1.0 / np.sqrt(9.0 * C))
+    b = st.uniform((CO,), 0.1)
+    got = _run_pool_s2("ffma", x, w, b, op, (-0.5, 0.7))
+    ref = oracle.convT_pool_mean(x, w, b, stride=2, pad=1, out_pad=op, hardtanh=(-0.5, 0.7))
+    _check(got, ref, f"ffma convT stride 2 {shape} op {op}")
+
+
+# ------------------------------------------------------ the general layer
+GENERAL_2D = [
+    # (shape N C H W, C_out, k, stride, pad, dilation, chain)
+    ((2, 5, 17, 23), 70, 1, 1, 0, 1, "rh"),
+    ((1, 8, 20, 37), 64, 5, 1, 2, 1, "gelu"),
+    ((2, 3, 19, 31), 10, 7, 2, 3, 1, "generic"),
+    ((1, 16, 23, 29), 64, 5, 3, 4, 2, "rh"),
+    ((1, 4, 30, 35), 64, 3, 4, 1, 3, "none"),
+    ((2, 6, 14, 18), 33, 4, 2, 1, 1, "rh"),      # even kernel size
+    ((1, 8, 9, 130), 64, 3, 3, 2, 4, "gelu"),    # stride 3, dilation 4, wide rows
+    ((1, 64, 12, 16), 64, 7, 1, 3, 1, "none"),  # 7x7 over 64 channels (smaller chunks)
+]
+
+
+@pytest.mark.parametrize("variant", ["auto", "ffma"])
+@pytest.mark.parametrize("case", GENERAL_2D)
+def test_conv2d_general_layer(variant, case):
+    """Kernel sizes 1-7, strides 3-4, dilations 3-4 and other paddings: the
+    general CUDA-core kernel, against the oracle."""
+    shape, CO, k, stride, pad, dil, chain = case
+    st = synth.seeded(850 + k + 7 * stride + 31 * dil)
+    N, C, H, W = shape
+    x = st.normal(shape)
+    w = st.uniform((CO, C, k, k), 1.0 / np.sqrt(k * k * C))
+    b = st.uniform((CO,), 0.1)
+    ops = _chain(chain, CO, st)
     m = fc()
-    x = _dev(np.zeros((1, 8, 8, 8), np.float32))
-    w = _dev(np.zeros((8, 64, 3, 3), np.float32))
-    m.set_variant("ffma")
+    m.set_variant(variant)
     try:
-        with pytest.raises(m.FcError):
-            m.fc_convT2d_pool_mean(x, w, None, stride=2, out_pad=1)
+        y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=stride,
+                            dilation=dil)
+        assert m.last_variant() == "ffma"
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy()
     finally:
         m.set_variant("auto")
+    _check(got, oracle.conv_epi(x, w, b, ops, stride=stride, pad=pad, dilation=dil),
+           f"{variant} general conv2d {case}")
+
+
+@pytest.mark.parametrize("case", [
+    ((1, 5, 6, 9, 11), 64, 1, 1, 0, 1),
+    ((1, 8, 9, 12, 14), 70, 5, 1, 2, 1),
+    ((2, 4, 11, 13, 12), 16, 3, 3, 1, 2),
+    ((1, 3, 8, 9, 10), 20, 5, 2, 3, 1),
+])
+def test_conv3d_general_layer(case):
+    shape, CO, k, stride, pad, dil = case
+    st = synth.seeded(870 + k + stride)
+    C = shape[1]
+    x = st.normal(shape)
+    w = st.uniform((CO, C, k, k, k), 1.0 / np.sqrt(k ** 3 * C))
+    b = st.uniform((CO,), 0.1)
+    ops = chain_gelu(st.normal((CO,)))
+    got = _run_conv_strided("ffma", x, w, b, ops, pad, stride, dilation=dil)
+    _check(got, oracle.conv_epi(x, w, b, ops, stride=stride, pad=pad, dilation=dil),
+           f"general conv3d {case}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "ffma"])
+@pytest.mark.parametrize("case", [
+    # (N C H W, C_out, k, stride, pad, out_pad, pool)
+    ((2, 8, 9, 11), 64, 3, 3, 1, 2, (2, 2)),
+    ((1, 16, 7, 8), 70, 3, 4, 0, 3, (3, 2)),
+    ((2, 5, 10, 9), 64, 3, 2, 0, 1, (2, 2)),
+    ((1, 8, 12, 13), 64, 3, 2, 2, 0, (3, 3)),
+    ((2, 4, 8, 10), 33, 5, 2, 2, 1, (2, 2)),
+    ((1, 12, 11, 9), 64, 7, 1, 3, 0, (4, 2)),
+    ((1, 8, 6, 7), 64, 1, 3, 0, 2, (2, 1)),
+    ((2, 64, 9, 10), 64, 3, 1, 0, 0, (2, 2)),  # stride 1, pad 0: equivalent conv with pad 2
+    ((1, 8, 10, 12), 64, 4, 2, 1, 0, (2, 2)),  # even kernel size
+])
+def test_convT_general_layer_pool_mean(variant, case):
+    """Transposed conv at kernel sizes 1-7, strides 1-4, paddings and output
+    paddings, with 2x2 and general pools, against the oracle's scatter form."""
+    shape, CO, k, stride, pad, op, pool = case
+    st = synth.seeded(890 + k + 5 * stride + 13 * pad + 29 * op)
+    N, C, H, W = shape
+    x = st.normal(shape)
+    w = st.uniform((C, CO, k, k), 1.0 / np.sqrt(k * k * C))
+    b = st.uniform((CO,), 0.1)
+    ht = (-0.6, 0.8)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), hardtanh=ht, pad=pad,
+                                   stride=stride, out_pad=op, pool=pool)
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    ref = oracle.convT_pool_mean(x, w, b, stride=stride, pad=pad, out_pad=op, pool=pool,
+                                 hardtanh=ht)
+    _check(got, ref, f"{variant} general convT pool mean {case}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
+@pytest.mark.parametrize("case", [
+    # (N C H W, C_out, k, stride, pad, dilation, chain, tf32 plan fits)
+    ((2, 8, 20, 36), 64, 1, 1, 0, 1, "rh", True),
+    ((1, 64, 9, 40), 70, 1, 1, 0, 1, "none", True),
+    ((2, 8, 21, 37), 64, 5, 1, 2, 1, "gelu", True),
+    ((1, 16, 19, 140), 64, 5, 2, 1, 1, "rh", True),
+    ((1, 8, 25, 60), 64, 5, 1, 4, 2, "generic", True),
+    ((1, 8, 23, 44), 64, 7, 1, 3, 1, "rh", False),
+    ((1, 8, 30, 70), 64, 7, 2, 6, 2, "none", False),
+])
+def test_conv2d_kernel_sizes_tensor_cores(variant, case):
+    """Square odd kernels 1, 5, 7 on the tensor-core kernel (a longer tap
+    table of shifted descriptor starts), strides / dilations 1-2."""
+    shape, CO, k, stride, pad, dil, chain, tf32_fits = case
+    if variant == "tc_tf32x3" and not tf32_fits:
+        pytest.skip("the tf32 split's K steps do not fit shared memory at this size")
+    st = synth.seeded(900 + k + 7 * stride + 31 * dil)
+    N, C, H, W = shape
+    x = st.normal(shape)
+    w = st.uniform((CO, C, k, k), 1.0 / np.sqrt(k * k * C))
+    b = st.uniform((CO,), 0.1)
+    ops = _chain(chain, CO, st)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_conv2d_epi(_dev(x), _dev(w), _dev(b), _ops_torch(ops), pad=pad, stride=stride,
+                            dilation=dil)
+        if variant != "auto":
+            assert m.last_variant() == variant
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    _check(got, oracle.conv_epi(x, w, b, ops, stride=stride, pad=pad, dilation=dil),
+           f"{variant} kernel {k} conv2d {case}")
+
+
+@pytest.mark.parametrize("variant", ["tc_tf32x3", "tc_f16x3"])
+def test_conv3d_pointwise_tensor_cores(variant):
+    st = synth.seeded(905)
+    x = st.normal((1, 8, 6, 9, 20))
+    w = st.uniform((64, 8, 1, 1, 1), 0.3)
+    b = st.uniform((64,), 0.1)
+    ops = chain_gelu(st.normal((64,)))
+    got = _run_conv_strided(variant, x, w, b, ops, 0, 1)
+    _check(got, oracle.conv_epi(x, w, b, ops), f"{variant} conv3d 1x1x1")
+
+
+@pytest.mark.parametrize("variant", ["auto", "tc_f16x3", "ffma"])
+def test_convT_kernel5_stride1_pool_mean(variant):
+    """A 5 x 5 transposed conv (stride 1, pad 2) as the equivalent conv with
+    flipped weights on the tensor cores, or the general CUDA-core kernel."""
+    st = synth.seeded(906)
+    x = st.normal((2, 16, 18, 20))
+    w = st.uniform((16, 64, 5, 5), 1.0 / np.sqrt(400.0))
+    b = st.uniform((64,), 0.1)
+    m = fc()
+    m.set_variant(variant)
+    try:
+        y = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), pad=2)
+        if variant != "auto":
+            assert m.last_variant() == variant
+        assert m.get_last_device_error() == 0
+        got = y.cpu().numpy()
+    finally:
+        m.set_variant("auto")
+    _check(got, oracle.convT_pool_mean(x, w, b, pad=2), f"{variant} convT k5")
+
+
+def test_general_layer_refused_by_tensor_cores():
+    """Parameters outside the fixed-size kernels run on the general CUDA-core
+    kernel only: the tensor-core variants refuse them, AUTO takes FFMA."""
+    m = fc()
+    x = _dev(np.zeros((1, 8, 12, 12), np.float32))
+    w4 = _dev(np.zeros((64, 8, 4, 4), np.float32))  # even kernel size
+    for v in ("tc_tf32x3", "tc_f16x3"):
+        m.set_variant(v)
+        try:
+            with pytest.raises(m.FcError):
+                m.fc_conv2d_epi(x, w4, None, (), pad=2)
+            with pytest.raises(m.FcError):
+                m.fc_conv2d_epi(x, _dev(np.zeros((64, 8, 3, 3), np.float32)), None, (),
+                                stride=3)
+            with pytest.raises(m.FcError):
+                m.fc_convT2d_pool_mean(x, _dev(np.zeros((8, 64, 3, 3), np.float32)), None,
+                                       stride=3, out_pad=0)
+        finally:
+            m.set_variant("auto")
+    m.fc_conv2d_epi(x, w4, None, (), pad=2)
+    assert m.last_variant() == "ffma"
+
+
+def test_pooled_batch_1024_beyond_2_31_elements():
+    """x [1024,64,256,256] has 2^32 elements (16 GiB): the pooled workload's
+    128 images eight times over.  Offsets are 64-bit, so the call is
+    accepted and every block of 128 images gives bitwise the batch-128
+    result, which the whole-output test checks against the oracle."""
+    inp = _full_inputs(5)
+    m = fc()
+    x1 = _dev(inp["x"])
+    w, b = _dev(inp["w"]), _dev(inp["b"])
+    y1 = m.fc_convT2d_pool_mean(x1, w, b).cpu().numpy()
+    x8 = x1.repeat(8, 1, 1, 1)
+    del x1
+    assert x8.numel() == 1 << 32
+    y8 = m.fc_convT2d_pool_mean(x8, w, b).cpu().numpy()
+    assert m.get_last_device_error() == 0
+    del x8
+    torch.cuda.empty_cache()
+    for r in range(8):
+        np.testing.assert_array_equal(y8[128 * r:128 * (r + 1)], y1)
+    _check(y8[:128], _full_ref(5), "batch 1024 vs the oracle")
 
 
 @pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
@@ -619,17 +864,22 @@ def test_convT_stride2_full_size_sampled(variant):
 
 
 # ------------------------------------------- general max-pool windows (fused)
-@pytest.mark.parametrize("variant", ["auto", "ffma"])
+@pytest.mark.parametrize("variant", ["auto", "ffma", "tc_tf32x3", "tc_f16x3"])
 @pytest.mark.parametrize("shape,pool", [
     ((2, 16, 17, 21, 64), (3, 2)),   # overlapping windows, odd extents
     ((1, 8, 12, 40, 70), (2, 1)),    # stride 1: every conv output in 4 windows
     ((2, 64, 13, 14, 64), (3, 3)),   # non-overlapping 3x3
     ((1, 5, 9, 35, 64), (4, 2)),     # 4x4 windows, C_in not a multiple of 8
     ((1, 8, 6, 7, 64), (1, 1)),      # window 1: plain mean of the clamped conv
+    ((1, 8, 20, 40, 70), (4, 4)),    # non-overlapping 4x4, TMA-eligible width
+    ((1, 64, 9, 300, 64), (3, 3)),   # 128-column strips of 42 windows
+    ((2, 8, 9, 260, 64), (3, 2)),    # strips of 63 overlapping windows
 ])
 def test_convT_general_pool_mean(variant, shape, pool):
     """Transposed conv (stride 1, pad 1) + max pool of any window / stride
-    (floor extent) + hardtanh + mean + tanh in one pass, against the oracle."""
+    (floor extent) + hardtanh + mean + tanh in one pass, against the oracle:
+    the CUDA-core kernel (each thread its window) and the tensor-core kernel
+    (one tile per window row, the windows taken in shared memory)."""
     N, C, H, W, CO = shape
     st = synth.seeded(780 + pool[0] * 4 + pool[1])
     x = st.normal((N, C, H, W))
@@ -640,7 +890,8 @@ def test_convT_general_pool_mean(variant, shape, pool):
     m.set_variant(variant)
     try:
         y = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), hardtanh=ht, pool=pool)
-        assert m.last_variant() == "ffma"
+        if variant != "auto":
+            assert m.last_variant() == variant
         assert m.get_last_device_error() == 0
         got = y.cpu().numpy()
     finally:
@@ -649,17 +900,21 @@ def test_convT_general_pool_mean(variant, shape, pool):
     _check(got, ref, f"{variant} general pool {pool} {shape}")
 
 
-def test_general_pool_refused_by_tensor_core_variants():
+@pytest.mark.parametrize("variant", ["tc_tf32x3", "tc_f16x3"])
+def test_general_pool_deterministic_tensor_cores(variant):
+    st = synth.seeded(788)
+    x = st.normal((2, 16, 17, 21))
+    w = st.uniform((16, 64, 3, 3), 0.08)
+    b = st.uniform((64,), 0.1)
     m = fc()
-    x = _dev(np.zeros((1, 8, 8, 8), np.float32))
-    w = _dev(np.zeros((8, 64, 3, 3), np.float32))
-    for v in ("tc_tf32x3", "tc_f16x3"):
-        m.set_variant(v)
-        try:
-            with pytest.raises(m.FcError):
-                m.fc_convT2d_pool_mean(x, w, None, pool=(3, 2))
-        finally:
-            m.set_variant("auto")
+    m.set_variant(variant)
+    try:
+        a = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), pool=(3, 2)).cpu().numpy()
+        for _ in range(3):
+            np.testing.assert_array_equal(
+                m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b), pool=(3, 2)).cpu().numpy(), a)
+    finally:
+        m.set_variant("auto")
 
 
 # ------------------------------------------------ channels-last (N(D)HWC)
