@@ -328,7 +328,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.BW = p.cl ? q.LW : (q.LW + q.coff + 3) / 4 * 4;
   // (channels-first: every unit's first column iw0 - coff a multiple of 4,
   // so the strips must advance by a multiple of 4 columns)
-  const bool tma_ok = p.staging && !q.S2 && (p.cl ? (p.C % 4 == 0) : (p.W % 4 == 0)) &&
+  const bool tma_ok = p.staging && !q.S2 && !p.pool && (p.cl ? (p.C % 4 == 0) : (p.W % 4 == 0)) &&
                       (p.cl || q.n_ct == 1 || q.COLSTEP % 4 == 0) && q.BW <= 256 &&
                       q.RIN <= 256;
   q.raw_tx = q.chunk_ci * q.RIN * q.BW * 4;
@@ -727,7 +727,8 @@ __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, 
   // a stage holds at most 2 slice planes of KD depth slices
   const int plane = job >= nrows ? 1 : 0;
   const int sr = job - plane * nrows;
-  const int kdp = sr / q.RIN;
+  int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
+  if (p.KD > 3) kdp = sr / q.RIN;  // 5 x 5 x 5 kernels
   const int r = sr - kdp * q.RIN;
   const int id = ss.id0 + kdp * q.DIL, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
@@ -1064,7 +1065,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                                        px * 16) = make_uint4(0, 0, 0, 0);
     }
     bool tma_done = false;
-    if constexpr (!S2 && !SP) {
+    if constexpr (!S2 && !SP && !POOL) {  // the pooled instances keep the smaller code
       if (q.TMA) {
         // ---- tensor-copy staging.  Warp kProdWarp0 (its first lane) issues
         // one tiled tensor copy per (chunk, depth slice) into the raw ring and
