@@ -229,8 +229,8 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
   if (p.cl && (p.pool || p.stride != 1)) return q;  // channels-last: stride 1, no pool
   const bool gp = p.pool && (p.pk != 2 || p.ps != 2);
-  // 2x2 pool: row pairs per unit; general pool: one tile per window row
-  if (p.pool && (gp ? U != p.pk : (U != 2 && U != 4))) return q;
+  // 2x2 pool: one row pair per unit; general pool: one tile per window row
+  if (p.pool && U != (gp ? p.pk : 2)) return q;
   if (p.pool && p.KD != 1) return q;
   if (gp && (p.pk < 1 || p.pk > 4 || p.ps < 1 || p.ps > 4)) return q;
   plan_chunks(p, prec, q);
@@ -307,7 +307,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.plane_bytes = q.NPIX * 16;
   q.a_stage_bytes = 2 * q.P * q.plane_bytes;
   if (q.COB * 64 > kMaxCoTc) return q;
-  q.n_rt = gp ? (p.Ho - p.pk) / p.ps + 1 : p.pool ? cdiv(p.Ho / 2, q.U / 2) : cdiv(p.Ho, q.U * q.R);
+  q.n_rt = gp ? (p.Ho - p.pk) / p.ps + 1 : p.pool ? p.Ho / 2 : cdiv(p.Ho, q.U * q.R);
   q.units = (long)q.COB * p.N * p.Do * q.n_rt * q.n_ct;
   if (q.units >= (1L << 31)) return q;  // unit indices are 32-bit
   q.fd_ct = make_fastdiv((uint32_t)q.n_ct);
@@ -947,7 +947,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial, const __grid_constant__ CUtensorMap tmx) {
   constexpr int E = PREC ? 8 : 4;
   static_assert(U >= 1 && U <= 4, "one to four M tiles per unit");
-  static_assert(!POOL || U == 2 || U == 4 || SP || GP, "the 2x2 pool takes row pairs per unit");
+  static_assert(!POOL || U == 2 || SP || GP, "the 2x2 pool takes two output rows per unit");
   static_assert(!GP || (POOL && !SP && !S2 && !CL), "general pool: stride-1 pooled entry");
   static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
   static_assert(!CL || (!POOL && !S2), "channels-last: stride-1 elementwise entries");
@@ -1444,22 +1444,20 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
         const uint32_t first = c != 0;
         if constexpr (POOL) {
-          // every tile per K step (measured faster for the pooled chunks; with
-          // the K loop unrolled for 3 x 3 kernels: pooled transposed conv
-          // 1.495 -> 1.450 ms)
+          // every tile per K step, K-step deltas from the shared-memory table
+          // (measured faster for the pooled chunks than tile by tile, and than
+          // the K loop unrolled: 1.49 against 1.53 ms on the pooled workload)
           if constexpr (SP) {
             if (q.KS == 5) issue_subpix<PREC, 0, 5>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
             else issue_subpix<PREC, 0, 9>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
-          } else if (q.KS == 9) {  // every tile of a K step, the K loop unrolled
-            issue_chunk<PREC, U, 9>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
-          } else if (q.KS == 5) {
-            issue_chunk<PREC, U, 5>(kdr, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
           } else {
             issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
           }
         } else {
           // Tile by tile, each committed to its own accumulator-full barrier:
           // the epilogue starts on a tile once its last chunk's MMAs are done.
+          // (Both tiles per K step, committed together, measured slower:
+          // conv3d 0.565 -> 0.676 ms, conv2d 0.116 -> 0.127 ms.)
 #pragma unroll 1
           for (int t = 0; t < U; ++t) {
             const int ab = acc * U + t;
@@ -1829,38 +1827,30 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       } else {
         const int c = m;  // one output row per M tile
         const int ow = up.ct * q.WT + c;
-        const bool colok = ((c & 1) == 0) && (c + 1 < q.WT) && (ow + 1 < p.Wo);
-        const uint32_t col0 = (uint32_t)(acc * U * 128 + ch0);
+        const bool valid = ((c & 1) == 0) && (c + 1 < q.WT) && (ow + 1 < p.Wo);
+        const uint32_t col0 = (uint32_t)(acc * 256 + ch0);
 #pragma unroll 1
         for (int cc = 0; cc < 32; cc += 16) {
+          uint32_t h0[16], l0[16], h1[16], l1[16];
+          ptx::tmem_ld16(tl + col0 + cc, h0);
+          ptx::tmem_ld16(tl + col0 + 64 + cc, l0);
+          ptx::tmem_ld16(tl + col0 + 128 + cc, h1);
+          ptx::tmem_ld16(tl + col0 + 192 + cc, l1);
+          ptx::tmem_wait_ld();
           float part[16], bv[16];
 #pragma unroll
           for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<float4 *>(&bv[j]) =
                 *reinterpret_cast<const float4 *>(&ctl->bias[co_base + ch0 + cc + j]);
-          // pooled row r2 of the unit = conv rows (tiles) 2 r2, 2 r2 + 1; the
-          // unit's pooled rows are summed into one partial
-#pragma unroll 1
-          for (int r2 = 0; r2 < U / 2; ++r2) {
-            uint32_t h0[16], l0[16], h1[16], l1[16];
-            const uint32_t cr = col0 + (uint32_t)(r2 * 256 + cc);
-            ptx::tmem_ld16(tl + cr, h0);
-            ptx::tmem_ld16(tl + cr + 64, l0);
-            ptx::tmem_ld16(tl + cr + 128, h1);
-            ptx::tmem_ld16(tl + cr + 192, l1);
-            ptx::tmem_wait_ld();
-            const bool valid = colok && (up.rt * (U / 2) + r2 < p.Ho / 2);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float bias = bv[j];
-              const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
-              const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
-              float mx = fmaxf(v0, v1);
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-              mx = fminf(fmaxf(mx, p.ht_lo), p.ht_hi);
-              const float v = valid ? mx : 0.0f;
-              part[j] = r2 ? part[j] + v : v;
-            }
+          for (int j = 0; j < 16; ++j) {
+            const float bias = bv[j];
+            const float v0 = fmaf(scale, __uint_as_float(l0[j]), __uint_as_float(h0[j])) + bias;
+            const float v1 = fmaf(scale, __uint_as_float(l1[j]), __uint_as_float(h1[j])) + bias;
+            float mx = fmaxf(v0, v1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fminf(fmaxf(mx, p.ht_lo), p.ht_hi);
+            part[j] = valid ? mx : 0.0f;
           }
           // Sum over the warp's 32 pixels by halving exchanges: at each step a
           // lane keeps half of its channels and adds its partner's sums of
