@@ -154,6 +154,7 @@ struct TcPlan {
   // 16-byte aligned); channels-last slots [RIN][LW][chunk_ci].
   int TMA, TR, raw_bytes, raw_tx, off_raw, BW, coff;
   FastDiv fd_lw;
+  FastDiv fd_rin;  // division by RIN (depth slice of a staged row)
   // Unit origin: input rows / columns advance by ROWSTEP / COLSTEP conv
   // outputs per unit row / column index (U R and WT, except for the general
   // max pool).  General max pool (GP, window pk, stride ps other than 2 / 2):
@@ -356,6 +357,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   q.TMA = TR > 0;
   q.TR = TR;
   q.fd_lw = make_fastdiv((uint32_t)q.LW);
+  q.fd_rin = make_fastdiv((uint32_t)q.RIN);
   q.b_resident = resident;
   q.SB = resident ? 1 : SB;
   q.off_raw = S * q.a_stage_bytes;  // 128-byte aligned (NPIX is a multiple of 8)
@@ -403,6 +405,7 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
   q.ROWSTEP = q.R;
   q.COLSTEP = q.WT;
   q.RIN = q.R + 1;
+  q.fd_rin = make_fastdiv((uint32_t)q.RIN);
   q.LW = q.RS;
   q.DSL = q.RIN * q.RS;
   // K slots class by class, each class's taps by increasing shift; with
@@ -731,8 +734,7 @@ __host__ __device__ __forceinline__ RowJob row_job(int job, const StageSrc &ss, 
   // a stage holds at most 2 slice planes of KD depth slices
   const int plane = job >= nrows ? 1 : 0;
   const int sr = job - plane * nrows;
-  int kdp = (sr >= q.RIN ? 1 : 0) + (sr >= 2 * q.RIN ? 1 : 0);
-  if (p.KD > 3) kdp = sr / q.RIN;  // 5 x 5 x 5 kernels
+  const int kdp = (int)fdiv((uint32_t)sr, q.fd_rin);  // no division routine in the loop
   const int r = sr - kdp * q.RIN;
   const int id = ss.id0 + kdp * q.DIL, ih = ss.ih0 + r;
   jb.ok = id >= 0 && id < p.D && ih >= 0 && ih < p.H;
@@ -1504,6 +1506,22 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u);
   } else {
     // ------------------------------------------------------------ epilogue
+    if constexpr (PREC == 1) {
+      // Bottom of the fp16 split's range: below 2^-14 the hi part of a value
+      // is subnormal and below 2^-24 it vanishes, so data whose largest
+      // magnitude is under 2^-12 would lose relative accuracy.  The largest
+      // |w| (per-block maxima from the weight pack) is checked here, by one
+      // warp of CTA 0 while it waits for its first accumulator; each CTA's
+      // staged x at the end.  All-zero data is exact and not flagged.
+      if (blockIdx.x == 0 && warp == kEpiWarps - 1 && p.wmax) {
+        float wm = 0.0f;
+#pragma unroll 8
+        for (int i = lane; i < p.wmax_n; i += 32) wm = fmaxf(wm, __ldg(p.wmax + i));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        if (lane == 0 && wm > 0.0f && wm < kF16SplitMin) atomicOr(p.status, ST_RANGE);
+      }
+    }
     // Warp w reads TMEM lane quadrant w % 4 (one output pixel per lane) and
     // channel half w / 4 (32 of the 64 channels).
     const int quad = warp & 3, half = warp >> 2;
@@ -1882,20 +1900,11 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   ptx::tc_fence_after();
   if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
   if constexpr (PREC == 1) {
-    // Bottom of the fp16 split's range: below 2^-14 the hi part of a value is
-    // subnormal and below 2^-24 it vanishes, so inputs whose largest
-    // magnitude is under 2^-12 would lose relative accuracy.  Flag it when
-    // this CTA's staged x, or the weights (checked by CTA 0), are that small
-    // everywhere (all-zero data is exact and not flagged).
-    if (warp == kProdWarp0) {
+    // Bottom of the fp16 split's range (see the weights' check above): this
+    // CTA's staged x
+    if (tid == kProdWarp0 * 32) {
       const float xm = __uint_as_float(ctl->amax_bits);
-      float wm = 0.0f;
-      if (blockIdx.x == 0 && p.wmax)
-        for (int i = lane; i < p.wmax_n; i += 32) wm = fmaxf(wm, p.wmax[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-      if (lane == 0 && ((xm > 0.0f && xm < kF16SplitMin) || (wm > 0.0f && wm < kF16SplitMin)))
-        atomicOr(p.status, ST_RANGE);
+      if (xm > 0.0f && xm < kF16SplitMin) atomicOr(p.status, ST_RANGE);
     }
   }
 }
