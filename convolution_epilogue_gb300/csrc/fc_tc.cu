@@ -894,6 +894,83 @@ __device__ __forceinline__ void issue_chunk_loop(const uint32_t *kd_smem, int KS
   }
 }
 
+// Every MMA of a CTA's pooled units (2x2 or general window), weights
+// resident, issued by one thread.  The tensor pipe runs at most about one
+// MMA ahead of the issuing thread (measured: a pause of n clocks between
+// two chunks lengthens the chunk by about n), so the work between two
+// chunks is kept to a commit and a fence: the next chunk's stage (and, in a
+// unit's last chunk, the next accumulator) is tested before the chunk's last
+// K step, while its MMAs run; no warp vote, no per-step elect; addresses
+// from counters.  Barrier arrays are indexed by stage / accumulator.
+// Returns false when a wait gave up (the abort flag is then set).
+template <int PREC, int U>
+__device__ __forceinline__ bool issue_pool_units(const TcPlan &q, long units, uint32_t sbase,
+                                              uint32_t tmem, uint64_t *bars,
+                                              const uint32_t *kd_smem, uint32_t lo_delta,
+                                              uint32_t tile_delta, volatile int *abort,
+                                              unsigned int *status) {
+  constexpr int A_FULL = 0, A_EMPTY = 4, ACC_FULL = 12, ACC_EMPTY = 16;
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;  // SBO 128 B, version 1
+  const volatile uint32_t *kt = kd_smem;
+  const uint32_t a_base = (sbase >> 4) & 0x3FFFu, a_step = (uint32_t)(q.a_stage_bytes >> 4);
+  const uint32_t b_base = ((sbase + (uint32_t)q.off_b) >> 4) & 0x3FFFu;
+  const uint32_t b_step = (uint32_t)(q.b_chunk_bytes >> 4);
+  int ms = 0, macc = 0;
+  uint32_t mph = 0, mpar = 0, g = 0, it = 0;
+  bool full_ok = false, acc_ok = false;  // seen complete by the look-ahead tests
+  for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+    const uint32_t cb = fdiv((uint32_t)u, q.fd_cb);
+    const int acc = macc;
+    const uint32_t acc_par = mpar ^ 1;
+    if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
+    if (!acc_ok && !wait_bar(bars, ACC_EMPTY + acc, acc_par, abort, status, 0x21000000u | it))
+      return false;
+    ptx::tc_fence_after();
+    const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
+    uint32_t b_lo = (b_base + cb * (uint32_t)q.NCH * b_step) | ((2048u >> 4) << 16);
+    for (int c = 0; c < q.NCH; ++c, ++g, b_lo += b_step) {
+      const int s = ms;
+      const uint32_t sph = mph;
+      if (++ms == q.S) { ms = 0; mph ^= 1; }
+      if (!full_ok && !wait_bar(bars, A_FULL + s, sph, abort, status, 0x22000000u | g))
+        return false;
+      ptx::tc_fence_after();
+      const uint32_t a_lo = a_base + (uint32_t)s * a_step;
+      const bool last = c == q.NCH - 1;
+      uint32_t kd_next = kt[0];
+      for (int ks = 0; ks < q.KS; ++ks) {
+        const uint32_t kd_cur = kd_next;
+        kd_next = kt[ks + 1];
+        if (ks == q.KS - 1) {  // look ahead while this chunk's MMAs run
+          full_ok = ptx::mbar_test_wait(bars + A_FULL + ms, mph);
+          if (last) acc_ok = ptx::mbar_test_wait(bars + ACC_EMPTY + macc, mpar ^ 1);
+        }
+        const uint32_t ah = a_lo + kd_cur;
+        const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+        const uint32_t accum = (ks | c) ? 1u : 0u;
+#pragma unroll
+        for (int t = 0; t < U; ++t) {
+          const uint32_t aht = ah + (uint32_t)t * tile_delta;
+          const uint32_t d = dacc + (uint32_t)(t * 128);
+          if constexpr (PREC == 0) {
+            ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
+            ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+          } else {
+            ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
+            ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+          }
+        }
+      }
+      ptx::tc_commit(bars + A_EMPTY + s);
+    }
+    ptx::tc_commit(bars + ACC_FULL + acc);
+  }
+  return true;
+}
+
 // Issues one chunk of the stride-2 transposed conv by parity class: K step
 // ks adds into accumulator (kcls[ks] & 3) x 128 columns; the class's first
 // K step of the unit's first chunk starts the accumulator (accumulate 0).
@@ -1356,7 +1433,19 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     bool pre_full = false, pre_acc = false;
     bool ok = true;
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
-    for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
+    bool issued = false;  // the pooled units went through the single-thread loop
+    if constexpr (POOL && !SP) {
+      if (ok && q.b_resident) {
+        int r = 1;
+        if (ptx::elect_one()) r = issue_pool_units<PREC, U>(q, units, sbase, tmem, bars, ctl->kdelta,
+                                                            lo_delta, tile_delta, abort_flag, p.status)
+                                      ? 1 : 0;
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+        issued = true;
+      }
+    }
+    for (long u = blockIdx.x; ok && !issued && u < units; u += gridDim.x, ++it) {
       const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
       const int acc = macc;
       const uint32_t acc_par = mpar ^ 1;
