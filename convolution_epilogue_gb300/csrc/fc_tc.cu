@@ -817,99 +817,58 @@ __device__ __forceinline__ bool fill_row(const float *__restrict__ x, const RowJ
   return true;
 }
 
-// Issues the MMAs of one chunk: KS K steps x U M tiles, each an N=128
-// product (A_hi against [W_hi | W_lo]) and an N=64 product (A_lo against
-// W_hi).  Fully unrolled: per K step only the A and B start addresses move
-// (kd[ks] and ks x 4 KB), so the issuing warp spends few instructions per
-// MMA pair.  Every MMA pair is issued under elect.sync by the converged
-// warp.  `first_accum` is 0 for the first chunk of an accumulator.
-template <int PREC, int U, int KS>
-__device__ __forceinline__ void issue_chunk(const uint32_t (&kd)[28], uint32_t a_lo, uint32_t b_lo,
-                                            uint32_t dacc, uint32_t lo_delta, uint32_t tile_delta,
-                                            uint32_t first_accum) {
-  constexpr uint32_t fmt = PREC ? 0u : 2u;
-  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
-  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
-  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;  // SBO 128 B, version 1
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const uint32_t ah = a_lo + kd[ks];
-    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
-    const uint32_t accum = ks ? 1u : first_accum;
-    if (ptx::elect_one()) {
-#pragma unroll
-      for (int t = 0; t < U; ++t) {
-        const uint32_t aht = ah + (uint32_t)t * tile_delta;
-        const uint64_t dh = desc_hi | aht;
-        const uint64_t dl = desc_hi | (aht + lo_delta);
-        const uint32_t d = dacc + (uint32_t)(t * 128);
-        if constexpr (PREC == 0) {
-          ptx::mma_tf32(d, dh, bd, idesc1, accum);
-          ptx::mma_tf32(d + 64, dl, bd, idesc2, 1u);
-        } else {
-          ptx::mma_f16(d, dh, bd, idesc1, accum);
-          ptx::mma_f16(d + 64, dl, bd, idesc2, 1u);
-        }
-      }
-    }
-    __syncwarp();
-  }
-}
-
-// The same MMAs as issue_chunk with a run-time K-step count: each step's
-// delta is read from the table in shared memory one step ahead.
-template <int PREC, int U>
-__device__ __forceinline__ void issue_chunk_loop(const uint32_t *kd_smem, int KS, uint32_t a_lo,
-                                                 uint32_t b_lo, uint32_t dacc, uint32_t lo_delta,
-                                                 uint32_t tile_delta, uint32_t first_accum) {
+// One M tile's KS K steps (elementwise units), unrolled: every step's
+// shared-memory delta and weight offset at a constant address, the next
+// step's delta read while this step's MMAs issue (few registers, no loop
+// control between two MMA pairs); `look` runs before the last step when
+// `lk`.
+template <int PREC, int KS, class F>
+__device__ __forceinline__ void issue_tile_fixed(const volatile uint32_t *kt, uint32_t at,
+                                                 uint32_t b_lo, uint32_t d, uint32_t lo_delta,
+                                                 int c, bool lk, F &&look) {
   constexpr uint32_t fmt = PREC ? 0u : 2u;
   constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
   constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
   constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
-  const volatile uint32_t *kt = kd_smem;
   uint32_t kd_next = kt[0];
+#pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     const uint32_t kd_cur = kd_next;
-    kd_next = kt[ks + 1];
-    const uint32_t ah = a_lo + kd_cur;
+    if (ks + 1 < KS) kd_next = kt[ks + 1];
+    if (ks == KS - 1 && lk) look();
+    const uint32_t ah = at + kd_cur;
     const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
-    const uint32_t accum = ks ? 1u : first_accum;
-    if (ptx::elect_one()) {
-#pragma unroll
-      for (int t = 0; t < U; ++t) {
-        const uint32_t aht = ah + (uint32_t)t * tile_delta;
-        const uint64_t dh = desc_hi | aht;
-        const uint64_t dl = desc_hi | (aht + lo_delta);
-        const uint32_t d = dacc + (uint32_t)(t * 128);
-        if constexpr (PREC == 0) {
-          ptx::mma_tf32(d, dh, bd, idesc1, accum);
-          ptx::mma_tf32(d + 64, dl, bd, idesc2, 1u);
-        } else {
-          ptx::mma_f16(d, dh, bd, idesc1, accum);
-          ptx::mma_f16(d + 64, dl, bd, idesc2, 1u);
-        }
-      }
+    const uint32_t accum = (ks | c) ? 1u : 0u;
+    if constexpr (PREC == 0) {
+      ptx::mma_tf32(d, desc_hi | ah, bd, idesc1, accum);
+      ptx::mma_tf32(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
+    } else {
+      ptx::mma_f16(d, desc_hi | ah, bd, idesc1, accum);
+      ptx::mma_f16(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
     }
-    __syncwarp();
   }
 }
 
-// Every MMA of a CTA's pooled units (2x2 or general window), weights
-// resident, issued by one thread.  The tensor pipe runs at most about one
-// MMA ahead of the issuing thread (measured: a pause of n clocks between
-// two chunks lengthens the chunk by about n), so the work between two
-// chunks is kept to a commit and a fence: the next chunk's stage (and, in a
-// unit's last chunk, the next accumulator) is tested before the chunk's last
-// K step, while its MMAs run; no warp vote, no per-step elect; addresses
-// from counters.  Barrier arrays are indexed by stage / accumulator.
-// Returns false when a wait gave up (the abort flag is then set).
-template <int PREC, int U>
-__device__ __forceinline__ bool issue_pool_units(const TcPlan &q, long units, uint32_t sbase,
-                                              uint32_t tmem, uint64_t *bars,
-                                              const uint32_t *kd_smem, uint32_t lo_delta,
-                                              uint32_t tile_delta, volatile int *abort,
-                                              unsigned int *status) {
-  constexpr int A_FULL = 0, A_EMPTY = 4, ACC_FULL = 12, ACC_EMPTY = 16;
+// Every MMA of a CTA's units issued by one thread (all entries but the
+// parity-class pooled one).  The tensor pipe runs at most about one MMA
+// ahead of the issuing thread (measured: a pause of n clocks between two
+// chunks lengthens the chunk by about n), so the work between two chunks is
+// kept to commits and a fence: the next chunk's stage (with streamed
+// weights also the next weight slot, and in a unit's last chunk the next
+// accumulator) is tested before the chunk's last K step, while its MMAs
+// run; no warp vote, no per-step elect; addresses from counters.
+// Pooled units (POOL) issue every tile per K step and complete the unit's
+// accumulator at once; elementwise units go tile by tile, each tile's
+// accumulator completed by its own commit in the unit's last chunk, so the
+// epilogue can start on it.  UNROLL: 14-step tiles unrolled (off for the
+// channels-last instances, where it spilled registers).  Returns false
+// when a wait gave up (the abort flag is then set).
+template <int PREC, int U, bool POOL, bool UNROLL>
+__device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_t sbase,
+                                            uint32_t tmem, uint64_t *bars, const uint32_t *kd_smem,
+                                            uint32_t lo_delta, uint32_t tile_delta,
+                                            volatile int *abort, unsigned int *status) {
+  constexpr int A_FULL = 0, A_EMPTY = 4, B_FULL = 8, B_EMPTY = 10, ACC_FULL = 12, ACC_EMPTY = 16;
   constexpr uint32_t fmt = PREC ? 0u : 2u;
   constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
   constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
@@ -918,55 +877,113 @@ __device__ __forceinline__ bool issue_pool_units(const TcPlan &q, long units, ui
   const uint32_t a_base = (sbase >> 4) & 0x3FFFu, a_step = (uint32_t)(q.a_stage_bytes >> 4);
   const uint32_t b_base = ((sbase + (uint32_t)q.off_b) >> 4) & 0x3FFFu;
   const uint32_t b_step = (uint32_t)(q.b_chunk_bytes >> 4);
-  int ms = 0, macc = 0;
-  uint32_t mph = 0, mpar = 0, g = 0, it = 0;
-  bool full_ok = false, acc_ok = false;  // seen complete by the look-ahead tests
+  const bool resident = q.b_resident != 0;
+  int ms = 0, macc = 0, msb = 0;
+  uint32_t mph = 0, mpar = 0, msbph = 0, g = 0, it = 0;
+  // seen complete by the look-ahead tests
+  bool full_ok = false, acc_ok = false, wfull_ok = false;
   for (long u = blockIdx.x; u < units; u += gridDim.x, ++it) {
     const uint32_t cb = fdiv((uint32_t)u, q.fd_cb);
     const int acc = macc;
     const uint32_t acc_par = mpar ^ 1;
     if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
-    if (!acc_ok && !wait_bar(bars, ACC_EMPTY + acc, acc_par, abort, status, 0x21000000u | it))
+    // one wait for the whole accumulator: the epilogue frees a unit's tiles
+    // in order, so the last tile's barrier implies the others
+    if (!acc_ok && !wait_bar(bars, ACC_EMPTY + (POOL ? acc : acc * U + U - 1), acc_par, abort,
+                             status, 0x21000000u | it))
       return false;
     ptx::tc_fence_after();
     const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
-    uint32_t b_lo = (b_base + cb * (uint32_t)q.NCH * b_step) | ((2048u >> 4) << 16);
-    for (int c = 0; c < q.NCH; ++c, ++g, b_lo += b_step) {
-      const int s = ms;
-      const uint32_t sph = mph;
+    uint32_t b_res = (b_base + cb * (uint32_t)q.NCH * b_step) | ((2048u >> 4) << 16);
+    for (int c = 0; c < q.NCH; ++c, ++g, b_res += b_step) {
+      const int s = ms, sb = msb;
+      const uint32_t sph = mph, sbph = msbph;
       if (++ms == q.S) { ms = 0; mph ^= 1; }
       if (!full_ok && !wait_bar(bars, A_FULL + s, sph, abort, status, 0x22000000u | g))
         return false;
+      uint32_t b_lo = b_res;
+      if (!resident) {  // weight ring slot sb
+        if (++msb == q.SB) { msb = 0; msbph ^= 1; }
+        if (!wfull_ok && !wait_bar(bars, B_FULL + sb, sbph, abort, status, 0x23000000u | g))
+          return false;
+        b_lo = (b_base + (uint32_t)sb * b_step) | ((2048u >> 4) << 16);
+      }
       ptx::tc_fence_after();
       const uint32_t a_lo = a_base + (uint32_t)s * a_step;
       const bool last = c == q.NCH - 1;
-      uint32_t kd_next = kt[0];
-      for (int ks = 0; ks < q.KS; ++ks) {
-        const uint32_t kd_cur = kd_next;
-        kd_next = kt[ks + 1];
-        if (ks == q.KS - 1) {  // look ahead while this chunk's MMAs run
-          full_ok = ptx::mbar_test_wait(bars + A_FULL + ms, mph);
-          if (last) acc_ok = ptx::mbar_test_wait(bars + ACC_EMPTY + macc, mpar ^ 1);
-        }
-        const uint32_t ah = a_lo + kd_cur;
-        const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
-        const uint32_t accum = (ks | c) ? 1u : 0u;
+      auto look_ahead = [&]() {  // while this chunk's last MMAs run
+        full_ok = ptx::mbar_test_wait(bars + A_FULL + ms, mph);
+        if (!resident) wfull_ok = ptx::mbar_test_wait(bars + B_FULL + msb, msbph);
+        if (last)
+          acc_ok = ptx::mbar_test_wait(bars + ACC_EMPTY + (POOL ? macc : macc * U + U - 1),
+                                       mpar ^ 1);
+      };
+      if constexpr (POOL) {
+        uint32_t kd_next = kt[0];
+        for (int ks = 0; ks < q.KS; ++ks) {
+          const uint32_t kd_cur = kd_next;
+          kd_next = kt[ks + 1];
+          if (ks == q.KS - 1) look_ahead();
+          const uint32_t ah = a_lo + kd_cur;
+          const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+          const uint32_t accum = (ks | c) ? 1u : 0u;
 #pragma unroll
-        for (int t = 0; t < U; ++t) {
-          const uint32_t aht = ah + (uint32_t)t * tile_delta;
-          const uint32_t d = dacc + (uint32_t)(t * 128);
-          if constexpr (PREC == 0) {
-            ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
-            ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
-          } else {
-            ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
-            ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+          for (int t = 0; t < U; ++t) {
+            const uint32_t aht = ah + (uint32_t)t * tile_delta;
+            const uint32_t d = dacc + (uint32_t)(t * 128);
+            if constexpr (PREC == 0) {
+              ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
+              ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+            } else {
+              ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
+              ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+            }
           }
+        }
+      } else {
+#pragma unroll 1
+        for (int t = 0; t < U; ++t) {
+          const uint32_t at = a_lo + (uint32_t)t * tile_delta;
+          const uint32_t d = dacc + (uint32_t)(t * 128);
+          const bool lk = t == U - 1;
+          // 3x3x3 with 8-channel chunks (14 paired K steps): unrolled
+          // (0.653 -> 0.563 ms on the conv3d workload); the loop measured
+          // faster for 5 steps (conv2d 0.135 unrolled against 0.114 ms)
+          switch (UNROLL ? q.KS : 0) {
+            case 14: {
+              // the weight start as an opaque per-tile value: otherwise every
+              // unrolled step's descriptor is hoisted out of the tile loop
+              // and held in registers (spilled)
+              uint32_t bt;
+              asm volatile("mov.b32 %0, %1;" : "=r"(bt) : "r"(b_lo));
+              issue_tile_fixed<PREC, 14>(kt, at, bt, d, lo_delta, c, lk, look_ahead);
+            } break;
+            default: {  // the K-step loop over the table in shared memory
+          uint32_t kd_next = kt[0];
+          for (int ks = 0; ks < q.KS; ++ks) {
+            const uint32_t kd_cur = kd_next;
+            kd_next = kt[ks + 1];
+            if (lk && ks == q.KS - 1) look_ahead();
+            const uint32_t ah = at + kd_cur;
+            const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+            const uint32_t accum = (ks | c) ? 1u : 0u;
+            if constexpr (PREC == 0) {
+              ptx::mma_tf32(d, desc_hi | ah, bd, idesc1, accum);
+              ptx::mma_tf32(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
+            } else {
+              ptx::mma_f16(d, desc_hi | ah, bd, idesc1, accum);
+              ptx::mma_f16(d + 64, desc_hi | (ah + lo_delta), bd, idesc2, 1u);
+            }
+          }
+            } break;
+          }
+          if (last) ptx::tc_commit(bars + ACC_FULL + acc * U + t);
         }
       }
       ptx::tc_commit(bars + A_EMPTY + s);
+      if (!resident) ptx::tc_commit(bars + B_EMPTY + sb);
     }
-    ptx::tc_commit(bars + ACC_FULL + acc);
+    if constexpr (POOL) ptx::tc_commit(bars + ACC_FULL + acc);
   }
   return true;
 }
@@ -1406,9 +1423,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     }  // register-load producers
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
-    // The warp stays converged; every MMA burst and every commit is issued
-    // under elect.sync, which picks the same (lowest) lane each time, so each
-    // commit tracks all MMAs before it.
+    // Every MMA and commit comes from the same (lowest) lane -- elect.sync
+    // picks it each time -- so each commit tracks all MMAs before it.
     const uint32_t sbase = ptx::smem_u32(smem);
     // per-K-step A descriptor deltas, constant for the launch, kept in
     // registers (every index below is a compile-time constant)
@@ -1419,7 +1435,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 #pragma unroll
     for (int i = 0; i < 9; ++i) kcr[i] = SP ? ctl->kcls[i] : 0u;
     const uint32_t lo_delta = (uint32_t)((q.P * q.plane_bytes) >> 4);  // hi -> lo planes
-    const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile (pool)
+    const uint32_t tile_delta = (uint32_t)((q.R * q.RS * 16) >> 4);    // next M tile
     uint32_t g = 0, gb = 0, it = 0;
     // ring positions as counters (no integer division in the issue loop):
     // accumulator macc of phase mpar, stage ms of phase mph, weight slot msb
@@ -1433,27 +1449,25 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     bool pre_full = false, pre_acc = false;
     bool ok = true;
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
-    bool issued = false;  // the pooled units went through the single-thread loop
-    if constexpr (POOL && !SP) {
-      if (ok && q.b_resident) {
+    if constexpr (!SP) {
+      // every other entry: one thread issues all units
+      if (ok) {
         int r = 1;
-        if (ptx::elect_one()) r = issue_pool_units<PREC, U>(q, units, sbase, tmem, bars, ctl->kdelta,
-                                                            lo_delta, tile_delta, abort_flag, p.status)
-                                      ? 1 : 0;
+        if (ptx::elect_one())
+          r = issue_units<PREC, U, POOL, !CL>(q, units, sbase, tmem, bars, ctl->kdelta, lo_delta,
+                                              tile_delta, abort_flag, p.status) ? 1 : 0;
         __syncwarp();
         ok = __shfl_sync(0xffffffffu, r, 0) != 0;
-        issued = true;
       }
-    }
-    for (long u = blockIdx.x; ok && !issued && u < units; u += gridDim.x, ++it) {
+    } else {
+    // Parity-class pooled units (stride-2 transposed conv): the warp stays
+    // converged and issues under elect.sync.
+    for (long u = blockIdx.x; ok && u < units; u += gridDim.x, ++it) {
       const int cb = (int)fdiv((uint32_t)u, q.fd_cb);
       const int acc = macc;
       const uint32_t acc_par = mpar ^ 1;
       if (++macc == q.NACC) { macc = 0; mpar ^= 1; }
-      // One wait for the whole accumulator: the epilogue frees a unit's
-      // tiles in order (each warp arrives for tile t before tile t + 1), so
-      // the last tile's barrier implies the others.
-      if (!pre_acc && !wait_bar_warp(bars, ACC_EMPTY + (POOL ? acc : acc * U + U - 1), acc_par,
+      if (!pre_acc && !wait_bar_warp(bars, ACC_EMPTY + acc, acc_par,
                                      abort_flag, p.status, 0x21000000u | it))
         break;
       ptx::tc_fence_after();
@@ -1533,46 +1547,12 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         const uint32_t a_lo = ((sbase + (uint32_t)(s * q.a_stage_bytes)) >> 4) & 0x3FFFu;
         const uint32_t b_lo = ((bbase >> 4) & 0x3FFFu) | ((2048u >> 4) << 16);
         const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
-        const uint32_t first = c != 0;
-        if constexpr (POOL) {
-          // every tile per K step, K-step deltas from the shared-memory table
-          // (measured faster for the pooled chunks than tile by tile, and than
-          // the K loop unrolled: 1.49 against 1.53 ms on the pooled workload)
-          if constexpr (SP) {
-            if (q.KS == 5) issue_subpix<PREC, 0, 5>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
-            else issue_subpix<PREC, 0, 9>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
-          } else {
-            issue_chunk_loop<PREC, U>(ctl->kdelta, q.KS, a_lo, b_lo, dacc, lo_delta, tile_delta, first);
-          }
-        } else {
-          // Tile by tile, each committed to its own accumulator-full barrier:
-          // the epilogue starts on a tile once its last chunk's MMAs are done.
-          // (Both tiles per K step, committed together, measured slower:
-          // conv3d 0.565 -> 0.676 ms, conv2d 0.116 -> 0.127 ms.)
-#pragma unroll 1
-          for (int t = 0; t < U; ++t) {
-            const int ab = acc * U + t;
-            const uint32_t at = a_lo + (uint32_t)t * tile_delta, dt = dacc + (uint32_t)(t * 128);
-            switch (q.KS) {  // 3 x 3 kernels: 2D 5 or 9 K steps, 3D 14 or 27
-              case 5: issue_chunk<PREC, 1, 5>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
-              case 9: issue_chunk<PREC, 1, 9>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
-              case 14: issue_chunk<PREC, 1, 14>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
-              case 27: issue_chunk<PREC, 1, 27>(kdr, at, b_lo, dt, lo_delta, tile_delta, first); break;
-              default:  // other kernel sizes: K-step table in shared memory
-                issue_chunk_loop<PREC, 1>(ctl->kdelta, q.KS, at, b_lo, dt, lo_delta, tile_delta, first);
-                break;
-            }
-            if (c == q.NCH - 1) {
-              if (ptx::elect_one()) ptx::tc_commit(&acc_full[ab]);
-              __syncwarp();
-            }
-          }
-        }
+        if (q.KS == 5) issue_subpix<PREC, 0, 5>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
+        else issue_subpix<PREC, 0, 9>(kdr, kcr, a_lo, b_lo, dacc, lo_delta, c == 0);
         // look ahead while the MMAs just issued run
         pre_full = __all_sync(0xffffffffu, ptx::mbar_test_wait(&a_full[ms], mph));
         if (c == q.NCH - 1)
-          pre_acc = __all_sync(0xffffffffu, ptx::mbar_test_wait(
-                                                &acc_empty[POOL ? macc : macc * U + U - 1], mpar ^ 1));
+          pre_acc = __all_sync(0xffffffffu, ptx::mbar_test_wait(&acc_empty[macc], mpar ^ 1));
         if (ptx::elect_one()) {
           ptx::tc_commit(&a_empty[s]);
           if (!q.b_resident) ptx::tc_commit(&b_empty[sb]);
@@ -1584,11 +1564,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
       }
       if (!ok) break;
-      if constexpr (POOL) {
-        if (ptx::elect_one()) ptx::tc_commit(&acc_full[acc]);
-        __syncwarp();
-      }
+      if (ptx::elect_one()) ptx::tc_commit(&acc_full[acc]);
+      __syncwarp();
     }
+    }  // parity-class units
     // wait until every MMA this warp issued has completed
     if (ptx::elect_one()) ptx::tc_commit(drain);
     __syncwarp();
