@@ -52,11 +52,18 @@ namespace fc {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 32 channels each
-constexpr int kMmaWarp = 8;
-constexpr int kProdWarp0 = 9;
-constexpr int kProdWarps = 7;
-constexpr int kProdThreads = 32 * kProdWarps;
+// Warp roles of the 16 warps: kEpi epilogue warps (two per TMEM lane
+// quadrant, 32 channels each; with FEW_EPI one per quadrant taking all 64
+// channels -- the 2x2-pooled entry, whose epilogue is light and whose
+// stages want more loading warps), one MMA warp, the rest producers.
+template <bool FEW_EPI>
+struct Roles {
+  static constexpr int kEpi = FEW_EPI ? 4 : 8;
+  static constexpr int kMma = kEpi;
+  static constexpr int kProd0 = kEpi + 1;
+  static constexpr int kProd = 16 - kProd0;
+  static constexpr int kProdT = 32 * kProd;
+};
 constexpr int kBStep = 4096;                  // one K step of B: 2 slices x 128 rows x 16 B
 constexpr int kMaxSmem = 227 * 1024 - 1024;   // minus the 1 KB alignment slack
 constexpr uint64_t kWaitNs = 4000000000ull;
@@ -574,21 +581,23 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bars, int idx, uint32_t 
 // Weight-ring slot of chunk g.
 __device__ __forceinline__ int psb_tma_slot(uint32_t g, int SB) { return (int)(g % (uint32_t)SB); }
 
-// AND of a predicate over the 256 epilogue threads (named barrier 1).
+// AND of a predicate over the NT epilogue threads (named barrier 1).
+template <int NT>
 __device__ __forceinline__ bool epi_all(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "n"(NT)
       : "memory");
   return r != 0;
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
 struct UnitPos {
   int cb, n, od, rt, ct;
@@ -1047,6 +1056,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   static_assert(!GP || (POOL && !SP && !S2 && !CL), "general pool: stride-1 pooled entry");
   static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
   static_assert(!CL || (!POOL && !S2), "channels-last: stride-1 elementwise entries");
+  using RL = Roles<POOL && !SP && !GP>;
+  constexpr int kEpiWarps = RL::kEpi, kMmaWarp = RL::kMma, kProdWarp0 = RL::kProd0;
+  constexpr int kProdWarps = RL::kProd, kProdThreads = RL::kProdT;
+  constexpr int kEpiThreads = 32 * kEpiWarps;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1591,7 +1604,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     // Warp w reads TMEM lane quadrant w % 4 (one output pixel per lane) and
-    // channel half w / 4 (32 of the 64 channels).
+    // channel half w / 4 (32 of the 64 channels; all 64 with 4 warps).
     const int quad = warp & 3, half = warp >> 2;
     const int m = quad * 32 + lane;  // TMEM lane = M row = output pixel
     const int m_row = m / q.RS, m_col = m - m_row * q.RS;  // staged row / column of m
@@ -1606,7 +1619,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       if (++eacc == q.NACC) { eacc = 0; epar ^= 1; }
       if constexpr (POOL) {
         bool okw = wait_bar_warp(bars, ACC_FULL + acc, acc_par, abort_flag, p.status, 0x30000000u | it);
-        okw = epi_all(okw);
+        okw = epi_all<kEpiThreads>(okw);
         if (!okw) break;
         ptx::tc_fence_after();
       }
@@ -1769,7 +1782,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
-        epi_sync();
+        epi_sync<kEpiThreads>();
         // windows: thread (jq, ch) takes pooled columns jq, jq + 4, ... of
         // channel ch in increasing order; the bias is common to a window, so
         // it is added after the max (x -> x + b is monotone in fp32)
@@ -1786,7 +1799,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           sum += fminf(fmaxf(mxw + bias, p.ht_lo), p.ht_hi);
         }
         ctl->red[jq][ch] = sum;
-        epi_sync();
+        epi_sync<kEpiThreads>();
         if (et < 64) {
           const int T = q.n_rt * q.n_ct;
           const int t = up.rt * q.n_ct + up.ct;
@@ -1795,7 +1808,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             partial[((long)up.n * T + t) * p.CO + co] =
                 ((ctl->red[0][et] + ctl->red[1][et]) + ctl->red[2][et]) + ctl->red[3][et];
         }
-        epi_sync();
+        epi_sync<kEpiThreads>();
       } else if constexpr (SP) {
         // lane m = pooled pixel (rt R + m_row, ct WT + m_col); the 2x2 window
         // is the four class accumulators of that lane
@@ -1823,7 +1836,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&acc_empty[0]);
           bool okw = wait_bar_warp(bars, ACC_FULL + 1, acc_par, abort_flag, p.status, 0x30100000u | it);
-          okw = epi_all(okw);
+          okw = epi_all<kEpiThreads>(okw);
           if (!okw) break;
           ptx::tc_fence_after();
 #pragma unroll
@@ -1851,7 +1864,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&acc_empty[1]);
-          epi_sync();
+          epi_sync<kEpiThreads>();
           if (warp == 0) {
             const int T = q.n_rt * q.n_ct;
             const int t = up.rt * q.n_ct + up.ct;
@@ -1862,7 +1875,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                 dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
             }
           }
-          epi_sync();
+          epi_sync<kEpiThreads>();
           continue;
         }
 #pragma unroll 1
@@ -1898,7 +1911,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
-        epi_sync();
+        epi_sync<kEpiThreads>();
         if (warp == 0) {
           const int T = q.n_rt * q.n_ct;
           const int t = up.rt * q.n_ct + up.ct;
@@ -1909,14 +1922,15 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
           }
         }
-        epi_sync();
+        epi_sync<kEpiThreads>();
       } else {
         const int c = m;  // one output row per M tile
         const int ow = up.ct * q.WT + c;
         const bool valid = ((c & 1) == 0) && (c + 1 < q.WT) && (ow + 1 < p.Wo);
         const uint32_t col0 = (uint32_t)(acc * 256 + ch0);
+        constexpr int kWarpCh = 256 / kEpiWarps;  // channels of this warp: 64 (4 warps)
 #pragma unroll 1
-        for (int cc = 0; cc < 32; cc += 16) {
+        for (int cc = 0; cc < kWarpCh; cc += 16) {
           uint32_t h0[16], l0[16], h1[16], l1[16];
           ptx::tmem_ld16(tl + col0 + cc, h0);
           ptx::tmem_ld16(tl + col0 + 64 + cc, l0);
@@ -1947,7 +1961,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
-        epi_sync();
+        epi_sync<kEpiThreads>();
         if (warp == 0) {
           const int T = q.n_rt * q.n_ct;
           const int t = up.rt * q.n_ct + up.ct;
@@ -1958,7 +1972,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               dst[co] = ((ctl->red[0][j] + ctl->red[1][j]) + ctl->red[2][j]) + ctl->red[3][j];
           }
         }
-        epi_sync();
+        epi_sync<kEpiThreads>();
       }
     }
   }
