@@ -858,6 +858,41 @@ __device__ __forceinline__ void issue_tile_fixed(const volatile uint32_t *kt, ui
   }
 }
 
+// A pooled chunk of KS K steps, every one of the U tiles per step,
+// unrolled (same reads as issue_tile_fixed); `look` runs before the last
+// step.
+template <int PREC, int U, int KS, class F>
+__device__ __forceinline__ void issue_pool_fixed(const volatile uint32_t *kt, uint32_t a_lo,
+                                                 uint32_t b_lo, uint32_t dacc, uint32_t lo_delta,
+                                                 uint32_t tile_delta, int c, F &&look) {
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
+  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
+  uint32_t kd_next = kt[0];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t kd_cur = kd_next;
+    if (ks + 1 < KS) kd_next = kt[ks + 1];
+    if (ks == KS - 1) look();
+    const uint32_t ah = a_lo + kd_cur;
+    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+    const uint32_t accum = (ks | c) ? 1u : 0u;
+#pragma unroll
+    for (int t = 0; t < U; ++t) {
+      const uint32_t aht = ah + (uint32_t)t * tile_delta;
+      const uint32_t d = dacc + (uint32_t)(t * 128);
+      if constexpr (PREC == 0) {
+        ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
+        ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+      } else {
+        ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
+        ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
+      }
+    }
+  }
+}
+
 // Every MMA of a CTA's units issued by one thread (all entries but the
 // parity-class pooled one).  The tensor pipe runs at most about one MMA
 // ahead of the issuing thread (measured: a pause of n clocks between two
@@ -927,7 +962,11 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
           acc_ok = ptx::mbar_test_wait(bars + ACC_EMPTY + (POOL ? macc : macc * U + U - 1),
                                        mpar ^ 1);
       };
-      if constexpr (POOL) {
+      if (POOL && U == 2 && q.KS == 9) {
+        uint32_t bt;  // opaque: keeps the steps' descriptors from being hoisted
+        asm volatile("mov.b32 %0, %1;" : "=r"(bt) : "r"(b_lo));
+        issue_pool_fixed<PREC, U, 9>(kt, a_lo, bt, dacc, lo_delta, tile_delta, c, look_ahead);
+      } else if constexpr (POOL) {
         uint32_t kd_next = kt[0];
         for (int ks = 0; ks < q.KS; ++ks) {
           const uint32_t kd_cur = kd_next;
