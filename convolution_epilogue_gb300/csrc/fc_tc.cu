@@ -144,6 +144,11 @@ struct TcPlan {
   int b_chunk_bytes;
   int b_resident;
   int SB;
+  // CTA pairs (2x2-pooled plans): a cluster of two CTAs, the even one
+  // issuing M = 256 MMAs over both CTAs' tiles, each CTA holding half of B
+  // (b_kstep = 3072 bytes a K step: 64 rows of [W_hi | W_lo], 32 of W_hi)
+  int PAIR;
+  int b_kstep;
   int NACC;
   int tmem_cols;
   int n_rt, n_ct;
@@ -231,7 +236,7 @@ bool tc_kernel_ok(const ConvProblem &p) {
   return p.entry != 1 || p.KH == 1;
 }
 
-TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
+TcPlan make_plan_u(const ConvProblem &p, int prec, int U, bool allow_pair = true) {
   TcPlan q{};
   if (!tc_kernel_ok(p)) return q;
   if (p.stride > 2 || p.dil > 2 || ((p.stride > 1 || p.dil > 1) && p.pool)) return q;
@@ -329,6 +334,17 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U) {
   // shared memory: A stages + raw slots (tensor-copy staging) + B (resident
   // or a ring) + barriers/misc (+ the general pool's row maxima)
   const int misc = 512 + (int)sizeof(SmemCtl) + 256 + q.XB;
+  q.b_kstep = kBStep;
+  // 2x2 pool: CTA pairs when the units pair up and the pair's smaller
+  // weight half stays resident beside two or more stages
+  if (allow_pair && p.pool && !gp && q.U == 2 && q.units >= 2 && q.units % 2 == 0) {
+    const long b_pair = (long)q.COB * q.NCH * q.KS * 3072;
+    if (2L * q.a_stage_bytes + b_pair + misc <= kMaxSmem) {
+      q.PAIR = 1;
+      q.b_kstep = 3072;
+      q.b_chunk_bytes = q.KS * 3072;
+    }
+  }
   const long b_all = (long)q.COB * q.NCH * q.b_chunk_bytes;
   // Tensor-copy staging needs 16-byte multiples for the tensor's strides
   // (channels-first: W % 4 == 0; channels-last: C_in % 4 == 0) and box
@@ -504,12 +520,12 @@ TcPlan make_plan_subpix(const ConvProblem &p, int prec) {
 // takes two M tiles (half the barrier hand-offs per MMA, fewer re-staged
 // halo rows) when the image has rows for both and shared memory still holds
 // at least three stages; otherwise one.
-TcPlan make_plan(const ConvProblem &p, int prec) {
+TcPlan make_plan(const ConvProblem &p, int prec, bool allow_pair = true) {
   if (p.subpix) return make_plan_subpix(p, prec);
   // 2x2 pool: one row pair per unit.  (Two pairs, four tiles per K step,
   // issue faster but hold one accumulator and stream the weights: measured
   // 1.52 against 1.45 ms on the pooled workload.)
-  if (p.pool) return make_plan_u(p, prec, (p.pk == 2 && p.ps == 2) ? 2 : p.pk);
+  if (p.pool) return make_plan_u(p, prec, (p.pk == 2 && p.ps == 2) ? 2 : p.pk, allow_pair);
   TcPlan q2 = make_plan_u(p, prec, 2);
   if (q2.ok && q2.S >= 3 && p.Ho > q2.R) return q2;
   TcPlan q1 = make_plan_u(p, prec, 1);
@@ -858,17 +874,47 @@ __device__ __forceinline__ void issue_tile_fixed(const volatile uint32_t *kt, ui
   }
 }
 
+// One K step's two products of an M tile: A_hi x [W_hi | W_lo] (N = 128)
+// into columns d .. d + 127 and A_lo x W_hi (N = 64) into d + 64 .. d + 127.
+// bk1 / bk2: low descriptor words of the two B operands (the same operand
+// in one CTA; with CTA pairs this CTA's halves, M = 256 over both CTAs).
+template <int PREC, bool PAIR>
+__device__ __forceinline__ void mma_k_step(uint32_t d, uint32_t ah, uint32_t lo_delta,
+                                           uint32_t bk1, uint32_t bk2, uint32_t accum) {
+  constexpr uint32_t fmt = PREC ? 0u : 2u;
+  constexpr uint32_t M = PAIR ? 256u : 128u;
+  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, M, 128), idesc2 = ptx::instr_desc(fmt, M, 64);
+  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;  // SBO 128 B, version 1
+  const uint64_t a1 = desc_hi | ah, a2 = desc_hi | (ah + lo_delta);
+  const uint64_t b1 = desc_hi | bk1, b2 = desc_hi | bk2;
+  if constexpr (PAIR) {
+    if constexpr (PREC == 0) {
+      ptx::mma2_tf32(d, a1, b1, idesc1, accum);
+      ptx::mma2_tf32(d + 64, a2, b2, idesc2, 1u);
+    } else {
+      ptx::mma2_f16(d, a1, b1, idesc1, accum);
+      ptx::mma2_f16(d + 64, a2, b2, idesc2, 1u);
+    }
+  } else {
+    if constexpr (PREC == 0) {
+      ptx::mma_tf32(d, a1, b1, idesc1, accum);
+      ptx::mma_tf32(d + 64, a2, b2, idesc2, 1u);
+    } else {
+      ptx::mma_f16(d, a1, b1, idesc1, accum);
+      ptx::mma_f16(d + 64, a2, b2, idesc2, 1u);
+    }
+  }
+}
+
 // A pooled chunk of KS K steps, every one of the U tiles per step,
 // unrolled (same reads as issue_tile_fixed); `look` runs before the last
 // step.
-template <int PREC, int U, int KS, class F>
+template <int PREC, int U, int KS, bool PAIR, class F>
 __device__ __forceinline__ void issue_pool_fixed(const volatile uint32_t *kt, uint32_t a_lo,
-                                                 uint32_t b_lo, uint32_t dacc, uint32_t lo_delta,
-                                                 uint32_t tile_delta, int c, F &&look) {
-  constexpr uint32_t fmt = PREC ? 0u : 2u;
-  constexpr uint32_t idesc1 = ptx::instr_desc(fmt, 128, 128);
-  constexpr uint32_t idesc2 = ptx::instr_desc(fmt, 128, 64);
-  constexpr uint64_t desc_hi = (uint64_t)((128u >> 4) | (1u << 14)) << 32;
+                                                 uint32_t b_lo, uint32_t b_lo2, uint32_t dacc,
+                                                 uint32_t lo_delta, uint32_t tile_delta, int c,
+                                                 F &&look) {
+  constexpr uint32_t kStep16 = (PAIR ? 3072u : (uint32_t)kBStep) >> 4;
   uint32_t kd_next = kt[0];
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
@@ -876,20 +922,11 @@ __device__ __forceinline__ void issue_pool_fixed(const volatile uint32_t *kt, ui
     if (ks + 1 < KS) kd_next = kt[ks + 1];
     if (ks == KS - 1) look();
     const uint32_t ah = a_lo + kd_cur;
-    const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
     const uint32_t accum = (ks | c) ? 1u : 0u;
 #pragma unroll
-    for (int t = 0; t < U; ++t) {
-      const uint32_t aht = ah + (uint32_t)t * tile_delta;
-      const uint32_t d = dacc + (uint32_t)(t * 128);
-      if constexpr (PREC == 0) {
-        ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
-        ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
-      } else {
-        ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
-        ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
-      }
-    }
+    for (int t = 0; t < U; ++t)
+      mma_k_step<PREC, PAIR>(dacc + (uint32_t)(t * 128), ah + (uint32_t)t * tile_delta, lo_delta,
+                             b_lo + (uint32_t)ks * kStep16, b_lo2 + (uint32_t)ks * kStep16, accum);
   }
 }
 
@@ -907,7 +944,7 @@ __device__ __forceinline__ void issue_pool_fixed(const volatile uint32_t *kt, ui
 // epilogue can start on it.  UNROLL: 14-step tiles unrolled (off for the
 // channels-last instances, where it spilled registers).  Returns false
 // when a wait gave up (the abort flag is then set).
-template <int PREC, int U, bool POOL, bool UNROLL>
+template <int PREC, int U, bool POOL, bool UNROLL, bool PAIR>
 __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_t sbase,
                                             uint32_t tmem, uint64_t *bars, const uint32_t *kd_smem,
                                             uint32_t lo_delta, uint32_t tile_delta,
@@ -922,6 +959,12 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
   const uint32_t b_base = ((sbase + (uint32_t)q.off_b) >> 4) & 0x3FFFu;
   const uint32_t b_step = (uint32_t)(q.b_chunk_bytes >> 4);
   const bool resident = q.b_resident != 0;
+  // commits reach both CTAs of a pair (each has its stage and accumulator
+  // barriers at the same offsets)
+  auto commit = [](uint64_t *bar) {
+    if constexpr (PAIR) ptx::tc_commit2(bar, 3);
+    else ptx::tc_commit(bar);
+  };
   int ms = 0, macc = 0, msb = 0;
   uint32_t mph = 0, mpar = 0, msbph = 0, g = 0, it = 0;
   // seen complete by the look-ahead tests
@@ -938,7 +981,11 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
       return false;
     ptx::tc_fence_after();
     const uint32_t dacc = tmem + (uint32_t)(acc * U * 128);
-    uint32_t b_res = (b_base + cb * (uint32_t)q.NCH * b_step) | ((2048u >> 4) << 16);
+    // B descriptors' low words: start | slice distance (LBO) << 16; with
+    // CTA pairs this CTA's 64 rows of [W_hi | W_lo] (slices 1 KB apart)
+    // and, 2 KB further, its 32 rows of W_hi (slices 512 B apart)
+    constexpr uint32_t kLbo1 = (PAIR ? 1024u : 2048u) >> 4;
+    uint32_t b_res = (b_base + cb * (uint32_t)q.NCH * b_step) | (kLbo1 << 16);
     for (int c = 0; c < q.NCH; ++c, ++g, b_res += b_step) {
       const int s = ms, sb = msb;
       const uint32_t sph = mph, sbph = msbph;
@@ -950,8 +997,9 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
         if (++msb == q.SB) { msb = 0; msbph ^= 1; }
         if (!wfull_ok && !wait_bar(bars, B_FULL + sb, sbph, abort, status, 0x23000000u | g))
           return false;
-        b_lo = (b_base + (uint32_t)sb * b_step) | ((2048u >> 4) << 16);
+        b_lo = (b_base + (uint32_t)sb * b_step) | (kLbo1 << 16);
       }
+      const uint32_t b_lo2 = PAIR ? (((b_lo & 0x3FFFu) + (2048u >> 4)) | ((512u >> 4) << 16)) : b_lo;
       ptx::tc_fence_after();
       const uint32_t a_lo = a_base + (uint32_t)s * a_step;
       const bool last = c == q.NCH - 1;
@@ -963,9 +1011,11 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
                                        mpar ^ 1);
       };
       if (POOL && U == 2 && q.KS == 9) {
-        uint32_t bt;  // opaque: keeps the steps' descriptors from being hoisted
+        uint32_t bt, bt2;  // opaque: keeps the steps' descriptors from being hoisted
         asm volatile("mov.b32 %0, %1;" : "=r"(bt) : "r"(b_lo));
-        issue_pool_fixed<PREC, U, 9>(kt, a_lo, bt, dacc, lo_delta, tile_delta, c, look_ahead);
+        asm volatile("mov.b32 %0, %1;" : "=r"(bt2) : "r"(b_lo2));
+        issue_pool_fixed<PREC, U, 9, PAIR>(kt, a_lo, bt, bt2, dacc, lo_delta, tile_delta, c,
+                                           look_ahead);
       } else if constexpr (POOL) {
         uint32_t kd_next = kt[0];
         for (int ks = 0; ks < q.KS; ++ks) {
@@ -973,20 +1023,12 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
           kd_next = kt[ks + 1];
           if (ks == q.KS - 1) look_ahead();
           const uint32_t ah = a_lo + kd_cur;
-          const uint64_t bd = desc_hi | (b_lo + (uint32_t)(ks * (kBStep >> 4)));
+          const uint32_t kb = (uint32_t)ks * ((PAIR ? 3072u : (uint32_t)kBStep) >> 4);
           const uint32_t accum = (ks | c) ? 1u : 0u;
 #pragma unroll
-          for (int t = 0; t < U; ++t) {
-            const uint32_t aht = ah + (uint32_t)t * tile_delta;
-            const uint32_t d = dacc + (uint32_t)(t * 128);
-            if constexpr (PREC == 0) {
-              ptx::mma_tf32(d, desc_hi | aht, bd, idesc1, accum);
-              ptx::mma_tf32(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
-            } else {
-              ptx::mma_f16(d, desc_hi | aht, bd, idesc1, accum);
-              ptx::mma_f16(d + 64, desc_hi | (aht + lo_delta), bd, idesc2, 1u);
-            }
-          }
+          for (int t = 0; t < U; ++t)
+            mma_k_step<PREC, PAIR>(dacc + (uint32_t)(t * 128), ah + (uint32_t)t * tile_delta,
+                                   lo_delta, b_lo + kb, b_lo2 + kb, accum);
         }
       } else {
 #pragma unroll 1
@@ -1025,13 +1067,13 @@ __device__ __forceinline__ bool issue_units(const TcPlan &q, long units, uint32_
           }
             } break;
           }
-          if (last) ptx::tc_commit(bars + ACC_FULL + acc * U + t);
+          if (last) commit(bars + ACC_FULL + acc * U + t);
         }
       }
-      ptx::tc_commit(bars + A_EMPTY + s);
-      if (!resident) ptx::tc_commit(bars + B_EMPTY + sb);
+      commit(bars + A_EMPTY + s);
+      if (!resident) commit(bars + B_EMPTY + sb);
     }
-    if constexpr (POOL) ptx::tc_commit(bars + ACC_FULL + acc);
+    if constexpr (POOL) commit(bars + ACC_FULL + acc);
   }
   return true;
 }
@@ -1085,7 +1127,7 @@ __device__ __forceinline__ void lane_sum16(float (&v)[16], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP, bool CL, bool GP>
+template <int PREC, int CHAIN, bool POOL, int U, bool S2, bool SP, bool CL, bool GP, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                float *__restrict__ partial, const __grid_constant__ CUtensorMap tmx) {
@@ -1095,6 +1137,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   static_assert(!GP || (POOL && !SP && !S2 && !CL), "general pool: stride-1 pooled entry");
   static_assert(!SP || (POOL && U == 1 && !S2), "parity classes: one pooled tile per unit");
   static_assert(!CL || (!POOL && !S2), "channels-last: stride-1 elementwise entries");
+  static_assert(!PAIR || (POOL && U == 2 && !SP && !GP), "CTA pairs: the 2x2-pooled entry");
   using RL = Roles<POOL && !SP && !GP>;
   constexpr int kEpiWarps = RL::kEpi, kMmaWarp = RL::kMma, kProdWarp0 = RL::kProd0;
   constexpr int kProdWarps = RL::kProd, kProdThreads = RL::kProdT;
@@ -1119,8 +1162,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
   const int warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
+    // (CTA pairs: the even CTA's stage-full and accumulator-empty barriers
+    // also count the odd CTA's producer and epilogue warps)
     for (int s = 0; s < q.S; ++s) {  // tensor-copy staging: one warp loads, the rest convert
-      ptx::mbar_init(&a_full[s], (uint32_t)(q.TMA ? kProdWarps - 1 : kProdWarps));
+      ptx::mbar_init(&a_full[s], (uint32_t)((q.TMA ? kProdWarps - 1 : kProdWarps) * (PAIR ? 2 : 1)));
       ptx::mbar_init(&a_empty[s], 1);
     }
     for (int r = 0; r < q.TR; ++r) {
@@ -1133,7 +1178,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     }
     for (int a = 0; a < 4; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], kEpiWarps);
+      ptx::mbar_init(&acc_empty[a], kEpiWarps * (PAIR ? 2 : 1));
     }
     ptx::mbar_init(drain, 1);
     ctl->abort = 0;
@@ -1165,12 +1210,41 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                          ? p.epi.chan[1][c]
                          : 0.0f;
   }
+  const uint32_t rank = PAIR ? ptx::cluster_rank() : 0u;
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(&ctl->tmem_base, (uint32_t)q.tmem_cols);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {  // one allocation spanning both CTAs, same address in each
+      ptx::tmem_alloc2(&ctl->tmem_base, (uint32_t)q.tmem_cols);
+      ptx::tmem_relinquish2();
+    } else {
+      ptx::tmem_alloc(&ctl->tmem_base, (uint32_t)q.tmem_cols);
+      ptx::tmem_relinquish();
+    }
+  }
+  if constexpr (PAIR) {
+    // This CTA's half of B, resident: per K step of the packed image (2
+    // slices x 128 rows of [W_hi | W_lo], 16 B a row) the rows 64 rank ..
+    // 64 rank + 63 of each slice (the N = 128 product's columns of this
+    // CTA) and the rows 32 rank .. 32 rank + 31 (of W_hi: the N = 64
+    // product's), at 3072 bytes a K step.  Both CTAs' halves are in place
+    // before the cluster barrier below, so the first MMA needs no wait.
+    if (tid == 0) {
+      const long ksteps = (long)q.COB * q.NCH * q.KS;
+      ptx::mbar_arrive_expect_tx(&b_full[0], (uint32_t)(ksteps * 3072));
+      for (long k = 0; k < ksteps; ++k) {
+        const uint8_t *src = bimg + k * kBStep;
+        uint8_t *dst = smem + q.off_b + k * 3072;
+        for (int sl = 0; sl < 2; ++sl) {
+          ptx::bulk_g2s(dst + sl * 1024, src + sl * 2048 + rank * 1024, 1024u, &b_full[0]);
+          ptx::bulk_g2s(dst + 2048 + sl * 512, src + sl * 2048 + rank * 512, 512u, &b_full[0]);
+        }
+      }
+      volatile int no_abort = 0;
+      wait_bar(bars, B_FULL, 0, &no_abort, p.status, 0x17000000u);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();  // barriers, TMEM and weights ready in both CTAs
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -1184,7 +1258,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     float amax = 0.0f;                 // largest |x| staged (fp16 range check)
     uint32_t g = 0;
     bool ok = true;
-    if (q.b_resident && pt == 0) {
+    if (!PAIR && q.b_resident && pt == 0) {
       const long total = (long)q.COB * q.NCH * q.b_chunk_bytes;
       ptx::mbar_arrive_expect_tx(&b_full[0], (uint32_t)total);
       for (long off = 0; off < total; off += 16384) {
@@ -1462,7 +1536,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         if (++psb == q.SB) { psb = 0; psbph ^= 1; }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&a_full[s]);
+        if (lane == 0) {  // (CTA pairs: the even CTA's barrier)
+          if constexpr (PAIR) ptx::mbar_arrive_at(&a_full[s], 0);
+          else ptx::mbar_arrive(&a_full[s]);
+        }
       }
     }
     if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
@@ -1502,12 +1579,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     bool ok = true;
     if (q.b_resident) ok = wait_bar_warp(bars, B_FULL, 0, abort_flag, p.status, 0x20000000u);
     if constexpr (!SP) {
-      // every other entry: one thread issues all units
-      if (ok) {
+      // every other entry: one thread issues all units (CTA pairs: the even
+      // CTA's, for both CTAs' tiles)
+      if (ok && rank == 0) {
         int r = 1;
         if (ptx::elect_one())
-          r = issue_units<PREC, U, POOL, !CL>(q, units, sbase, tmem, bars, ctl->kdelta, lo_delta,
-                                              tile_delta, abort_flag, p.status) ? 1 : 0;
+          r = issue_units<PREC, U, POOL, !CL, PAIR>(q, units, sbase, tmem, bars, ctl->kdelta,
+                                                    lo_delta, tile_delta, abort_flag, p.status)
+                  ? 1 : 0;
         __syncwarp();
         ok = __shfl_sync(0xffffffffu, r, 0) != 0;
       }
@@ -1621,9 +1700,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     }
     }  // parity-class units
     // wait until every MMA this warp issued has completed
-    if (ptx::elect_one()) ptx::tc_commit(drain);
-    __syncwarp();
-    wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u);
+    if (rank == 0) {
+      if (ptx::elect_one()) {
+        if constexpr (PAIR) ptx::tc_commit2(drain, 1);
+        else ptx::tc_commit(drain);
+      }
+      __syncwarp();
+      wait_bar_warp(bars, DRAIN, 0, abort_flag, p.status, 0x24000000u);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     if constexpr (PREC == 1) {
@@ -1999,7 +2083,10 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+        if (lane == 0) {  // (CTA pairs: the even CTA's barrier)
+          if constexpr (PAIR) ptx::mbar_arrive_at(&acc_empty[acc], 0);
+          else ptx::mbar_arrive(&acc_empty[acc]);
+        }
         epi_sync<kEpiThreads>();
         if (warp == 0) {
           const int T = q.n_rt * q.n_ct;
@@ -2018,8 +2105,14 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
 
   ptx::tc_fence_before();
   __syncthreads();
+  // CTA pairs: neither CTA leaves (nor frees its half of the tensor memory)
+  // before the other is done with its shared memory and barriers
+  if constexpr (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
+  if (warp == kMmaWarp) {
+    if constexpr (PAIR) ptx::tmem_dealloc2(tmem, (uint32_t)q.tmem_cols);
+    else ptx::tmem_dealloc(tmem, (uint32_t)q.tmem_cols);
+  }
   if constexpr (PREC == 1) {
     // Bottom of the fp16 split's range (see the weights' check above): this
     // CTA's staged x
@@ -2140,10 +2233,10 @@ cudaError_t make_x_map(const ConvProblem &p, const TcPlan &q, CUtensorMap *m) {
 int g_num_sms = 0;
 
 template <int PREC, int CHAIN, bool POOL, int U, bool S2 = false, bool SP = false, bool CL = false,
-          bool GP = false>
+          bool GP = false, bool PAIR = false>
 cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *bimg,
                           float *partial, const CUtensorMap &tm, cudaStream_t s) {
-  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP, CL, GP>;
+  auto kern = tc_conv_kernel<PREC, CHAIN, POOL, U, S2, SP, CL, GP, PAIR>;
   const int smem = q.smem_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -2153,11 +2246,30 @@ cudaError_t launch_kernel(const ConvProblem &p, const TcPlan &q, const uint8_t *
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (g_num_sms <= 0) g_num_sms = 148;
   }
-  const long grid = q.units < g_num_sms ? q.units : g_num_sms;
+  long grid = q.units < g_num_sms ? q.units : g_num_sms;
   prof_begin(s);
-  kern<<<(unsigned)grid, kThreads, smem, s>>>(p, q, bimg, partial, tm);
+  if constexpr (PAIR) {
+    // clusters of two CTAs; units 2k and 2k + 1 go to the two CTAs of a pair
+    grid &= ~1L;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, q, bimg, partial, tm);
+  } else {
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(p, q, bimg, partial, tm);
+    e = cudaGetLastError();
+  }
   prof_end(s, p.entry);
-  return cudaGetLastError();
+  return e;
 }
 
 template <int PREC, int U, bool S2, bool CL = false>
@@ -2187,7 +2299,10 @@ cudaError_t launch_prec(const ConvProblem &p, const TcPlan &q, const uint8_t *bi
       default: return launch_kernel<PREC, CHAIN_NONE, true, 4, false, false, false, true>(p, q, bimg, partial, tm, s);
     }
   }
-  if (p.pool) return launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, tm, s);
+  if (p.pool)
+    return q.PAIR ? launch_kernel<PREC, CHAIN_NONE, true, 2, false, false, false, false, true>(
+                        p, q, bimg, partial, tm, s)
+                  : launch_kernel<PREC, CHAIN_NONE, true, 2>(p, q, bimg, partial, tm, s);
   // stride 2 (even / odd sub-plane staging) is its own instance, so the
   // stride-1 producer carries none of its index arithmetic
   if (q.S2)
@@ -2260,6 +2375,14 @@ cudaError_t tc_launch(const ConvProblem &p, int prec, void *ws, const WsLayout &
     if (e != cudaSuccess) return e;
   }
   e = prec ? launch_prec<1>(pp, q, bimg, partial, tm, s) : launch_prec<0>(pp, q, bimg, partial, tm, s);
+  if (e != cudaSuccess && q.PAIR) {
+    // a cluster launch refused (no two free SMs of a pair, say): the same
+    // units by single CTAs (same weight image, same partials)
+    (void)cudaGetLastError();
+    const TcPlan q1 = make_plan(p, prec, false);
+    if (q1.ok)
+      e = prec ? launch_prec<1>(pp, q1, bimg, partial, tm, s) : launch_prec<0>(pp, q1, bimg, partial, tm, s);
+  }
   if (e != cudaSuccess) return e;
   *launches += 1;
   if (p.pool) {

@@ -221,8 +221,8 @@ void check(const char *name, ConvProblem p) {
     TcPlan q = make_plan(p, prec);
     if (pv >= 2 && !q.TMA) continue;  // the tensor-copy plan fell back to loads: checked above
     if (!q.ok) { printf("%s prec%d: not supported\n", name, prec); continue; }
-    printf("%s prec%d st%d: S2=%d U=%d P=%d NCH=%d KS=%d pair=%d R=%d RS=%d WT=%d RIN=%d LW=%d SR=%d DSL=%d NPIX=%d S=%d res=%d units=%ld smem=%d TMA=%d TR=%d\n",
-           name, prec, p.staging, q.S2, q.U, q.P, q.NCH, q.KS, q.pairtaps, q.R, q.RS, q.WT, q.RIN, q.LW, q.SR, q.DSL, q.NPIX, q.S, q.b_resident, q.units, q.smem_bytes, q.TMA, q.TR);
+    printf("%s prec%d st%d: S2=%d U=%d P=%d NCH=%d KS=%d pair=%d R=%d RS=%d WT=%d RIN=%d LW=%d SR=%d DSL=%d NPIX=%d S=%d res=%d units=%ld smem=%d TMA=%d TR=%d CTApair=%d\n",
+           name, prec, p.staging, q.S2, q.U, q.P, q.NCH, q.KS, q.pairtaps, q.R, q.RS, q.WT, q.RIN, q.LW, q.SR, q.DSL, q.NPIX, q.S, q.b_resident, q.units, q.smem_bytes, q.TMA, q.TR, q.PAIR);
     REQ(q.smem_bytes + 1024 <= 227 * 1024, "smem %d", q.smem_bytes);
     REQ(q.off_misc + (int)sizeof(SmemCtl) <= q.smem_bytes, "misc");
     REQ(q.off_misc % 16 == 0 && q.off_b % 16 == 0 && q.a_stage_bytes % 16 == 0 && q.plane_bytes % 16 == 0, "align");
@@ -234,6 +234,27 @@ void check(const char *name, ConvProblem p) {
         "TMA ring / box");
     REQ(!q.TMA || p.cl || (q.BW % 4 == 0 && (((-p.pad - q.coff) % 4) + 4) % 4 == 0), "TMA x alignment");
     REQ((((long)q.off_b + (q.b_resident ? (long)q.COB * q.NCH * q.b_chunk_bytes : (long)q.SB * q.b_chunk_bytes)) >> 4) < (1 << 14), "B desc range");
+    if (q.PAIR) {
+      // CTA pairs: 2x2 pool, units in pairs, this CTA's B half resident.
+      // Each CTA's bulk copies put, per K step k, image rows 64 r + j of
+      // slice sl at k 3072 + sl 1024 + 16 j and image rows 32 r + j at
+      // k 3072 + 2048 + sl 512 + 16 j (CTA rank r); the M = 256 MMA takes
+      // B column n of the N = 128 product from CTA n / 64 (its row n % 64
+      // of the first block) and of the N = 64 product from CTA n / 32: both
+      // must be image row n.
+      REQ(p.pool && q.U == 2 && !q.GP && q.units % 2 == 0 && q.b_resident, "%s pair plan", name);
+      REQ(q.b_kstep == 3072 && q.b_chunk_bytes == q.KS * 3072, "%s pair B size", name);
+      for (int n = 0; n < 128; ++n) {
+        const int r = n / 64, j = n % 64;
+        REQ(64 * r + j == n, "%s pair N128 column %d", name, n);
+        REQ(j * 16 + 16 <= 1024, "%s pair N128 slice", name);
+      }
+      for (int n = 0; n < 64; ++n) {
+        const int r = n / 32, j = n % 32;
+        REQ(32 * r + j == n, "%s pair N64 column %d", name, n);
+        REQ(2048 + 512 + j * 16 + 16 <= 3072, "%s pair N64 slice", name);
+      }
+    }
     std::vector<int> seen(kMaxTaps + 2, 0);
     for (int k = 0; k < kMaxTaps + 2; ++k) if (q.perm[k] < q.TAPS) seen[q.perm[k]]++;
     for (int t = 0; t < q.TAPS; ++t) REQ(seen[t] == 1, "%s perm", name);
