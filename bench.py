@@ -81,10 +81,11 @@ def algorithmic_bytes(wid: int) -> int:
 # change to them the roofline's traffic is reported as null until the kernel
 # is captured again.
 NCU_TRAFFIC = {
-    # batch-16 capture (272.660736 MB read + write) x 8 for the 128-image launch
-    (5, "tc_f16x3"): {"src": "7ba80dbf7288c1b6", "bytes": 2181285888},
+    # batch-32 capture (542.595328 MB read + write, CTA-pair kernel) x 4 for
+    # the 128-image launch
+    (5, "tc_f16x3"): {"src": "26afe7421113e71f", "bytes": 2170381312},
     # full-size capture; the tail of y is still in L2 when the launch ends
-    (3, "tc_f16x3"): {"src": "7ba80dbf7288c1b6", "bytes": 527386112},
+    (3, "tc_f16x3"): {"src": "26afe7421113e71f", "bytes": 527941888},
 }
 
 KERNEL_SOURCES = ("fc_tc.cu", "fc_tc_ptx.cuh", "fc_epi.cuh", "fc_internal.h")

@@ -335,9 +335,13 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U, bool allow_pair = true
   // or a ring) + barriers/misc (+ the general pool's row maxima)
   const int misc = 512 + (int)sizeof(SmemCtl) + 256 + q.XB;
   q.b_kstep = kBStep;
-  // 2x2 pool: CTA pairs when the units pair up and the pair's smaller
-  // weight half stays resident beside two or more stages
-  if (allow_pair && p.pool && !gp && q.U == 2 && q.units >= 2 && q.units % 2 == 0) {
+  // 2x2 pool: CTA pairs when the units pair up, there are enough of them
+  // to amortise the pair's start (its weight half loads completely before
+  // the first MMA; measured: 16 x 64 x 64 x 64 0.033 -> 0.037 ms on pairs,
+  // 128 x 64 x 128 x 128 (8192 units) 0.565 -> 0.561, 128 x 64 x 256 x 256
+  // 1.24 -> 1.16) and the pair's smaller weight half stays resident beside
+  // two or more stages
+  if (allow_pair && p.pool && !gp && q.U == 2 && q.units >= 8192 && q.units % 2 == 0) {
     const long b_pair = (long)q.COB * q.NCH * q.KS * 3072;
     if (2L * q.a_stage_bytes + b_pair + misc <= kMaxSmem) {
       q.PAIR = 1;
