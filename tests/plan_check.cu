@@ -305,6 +305,14 @@ int main() {
   check("r3d-b", conv3d(2, 8, 4, 12, 66, 64, 1));
   check("cfg2", convT(2, 64, 32, 32, 64));
   check("cfg5", convT(128, 64, 256, 256, 64));
+  // the pooled workload at full size runs on CTA pairs (fp16 split); a
+  // batch below 8192 units, an odd unit count and the tf32 split do not
+  REQ(make_plan(convT(128, 64, 256, 256, 64), 1).PAIR == 1, "cfg5 fp16 on CTA pairs");
+  REQ(make_plan(convT(128, 64, 256, 256, 64), 0).PAIR == 0, "cfg5 tf32 single CTAs");
+  REQ(make_plan(convT(16, 64, 256, 256, 64), 1).PAIR == 0, "4096 units single CTAs");
+  REQ(make_plan(convT(32, 64, 256, 200, 64), 1).PAIR == 1, "8192 units on pairs");
+  REQ(make_plan(convT(32, 64, 256, 200, 64), 1, false).PAIR == 0, "pairs refused -> single CTAs");
+  check("pair-ragged", convT(32, 64, 256, 200, 64));
   check("rT-d", convT(1, 9, 33, 31, 65));
   check("s2-cfg3", conv2d(128, 8, 128, 128, 64, 0, 2));
   check("s2-a", conv2d(2, 8, 33, 37, 70, 0, 2));

@@ -841,6 +841,32 @@ def test_pooled_batch_1024_beyond_2_31_elements():
     _check(y8[:128], _full_ref(5), "batch 1024 vs the oracle")
 
 
+def test_pooled_cta_pairs_ragged_strips():
+    """x [32,64,256,200]: 8192 pooled units, so the fp16 split runs on CTA
+    pairs, with a ragged second column strip (72 of 128 columns).  Sampled
+    (n, c) outputs against the oracle, and the first 16 images bitwise
+    against a 16-image call (4096 units: single CTAs)."""
+    inp = _full_inputs(5)
+    x = np.ascontiguousarray(inp["x"][:32, :, :, :200])
+    w, b = inp["w"], inp["b"]
+    m = fc()
+    m.set_variant("tc_f16x3")
+    try:
+        y32 = m.fc_convT2d_pool_mean(_dev(x), _dev(w), _dev(b)).cpu().numpy().reshape(32, 64)
+        assert m.get_last_device_error() == 0
+        y16 = m.fc_convT2d_pool_mean(_dev(x[:16]), _dev(w), _dev(b)).cpu().numpy().reshape(16, 64)
+        assert m.get_last_device_error() == 0
+    finally:
+        m.set_variant("auto")
+    np.testing.assert_array_equal(y32[:16], y16)
+    rng = np.random.default_rng(11)
+    pairs = [(0, 0), (31, 63), (17, 5)] + [(int(rng.integers(32)), int(rng.integers(64)))
+                                           for _ in range(13)]
+    ref = oracle.convT_pool_mean_points(x, w, b, pairs)
+    got = np.array([y32[n, c] for n, c in pairs])
+    _check(got, ref, "CTA pairs, ragged strips")
+
+
 @pytest.mark.parametrize("variant", ["auto", "tc_tf32x3", "tc_f16x3"])
 def test_convT_stride2_full_size_sampled(variant):
     """x [128,64,128,128] -> transposed conv 256 x 256 (stride 2, output
