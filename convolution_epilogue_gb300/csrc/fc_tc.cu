@@ -1450,12 +1450,118 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
       }
     }
     if (!tma_done) {
+    // 2x2-pooled stages of one job a warp at most (rows of 128..159 staged
+    // columns, weights resident): each warp issues the loads of its job of
+    // the NEXT stage before it waits for and fills the current one, so a
+    // stage's loads are in flight for a whole stage period instead of being
+    // waited for after the stage is free (two register buffers of 4 column
+    // groups x E channels).  Jobs and their rotation as below.
+    uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
+    bool db_done = false;
+    if constexpr (POOL && !SP && !GP && !S2 && !CL) {
+      if (q.b_resident && njobs <= kProdWarps && G == 4 && parts == 1 && blockIdx.x < units) {
+        db_done = true;
+        auto stage_src = [&](long uu, int cc) {
+          const UnitPos up = decode_unit(uu, q);
+          StageSrc r;
+          r.id0 = up.od * p.stride - p.pad_d;
+          r.ih0 = up.rt * q.ROWSTEP * p.stride - p.pad;
+          r.iw0 = up.ct * q.COLSTEP * p.stride - p.pad;
+          r.xn = (long)up.n * p.C * p.D * HW;
+          r.ci0 = cc * q.chunk_ci;
+          return r;
+        };
+        // job J of the stage at `src` into v: a main job (row J, the row's 4
+        // column groups) or a tail job (lane -> one of the rows' last
+        // LW - 128 pixels); `dst` gets the byte offset of each loaded slice
+        // in the hi planes (or ~0u: nothing to store)
+        auto load_job = [&](int J, const StageSrc &src, float (&v)[4][E], uint32_t (&dst)[4]) {
+          if (J < mjobs) {
+            const RowJob jb = row_job(J, src, q, p, nrows, E, false);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              load_pixel<E, false>(p.x, jb, lane + 32 * k, cstride, src.iw0, p.W, p.C, v[k]);
+              dst[k] = jb.dst + (uint32_t)(lane + 32 * k) * 16u;
+            }
+          } else {
+            const int l = (J - mjobs) * 32 + lane;
+            const int job = l / tail;
+            const int cc = 32 * G + (l - job * tail);
+#pragma unroll
+            for (int k = 1; k < 4; ++k) dst[k] = ~0u;
+            dst[0] = ~0u;
+            if (job < jobs) {
+              const RowJob jb = row_job(job, src, q, p, nrows, E, false);
+              load_pixel<E, false>(p.x, jb, cc, cstride, src.iw0, p.W, p.C, v[0]);
+              dst[0] = jb.dst + (uint32_t)cc * 16u;
+            }
+          }
+        };
+        const int lo_off = q.P * q.plane_bytes;
+        long u = blockIdx.x;
+        int c = 0, ps = 0, rot = 0;
+        uint32_t pph = 0;
+        StageSrc ss = stage_src(u, 0);
+        float va[4][E], vb[4][E];
+        uint32_t da[4], db[4];
+        int JA = pw;  // rot = 0
+        if (JA < njobs) load_job(JA, ss, va, da);
+        for (;;) {
+          long un = u;
+          int cn = c + 1;
+          if (cn == q.NCH) { cn = 0; un = u + gridDim.x; }
+          int rotn = rot + njobs % kProdWarps;
+          if (rotn >= kProdWarps) rotn -= kProdWarps;
+          int JB = pw - rotn;
+          if (JB < 0) JB += kProdWarps;
+          StageSrc sn = ss;
+          if (un < units) {
+            if (un != u) sn = stage_src(un, 0);
+            else sn.ci0 = cn * q.chunk_ci;
+            if (JB < njobs) load_job(JB, sn, vb, db);
+          }
+          // the current stage: free once the MMAs that read it S chunks ago
+          // are done; then the slices loaded one stage ago go in
+          const int s = ps;
+          if (!wait_bar_warp(bars, A_EMPTY + s, pph ^ 1, abort_flag, p.status, 0x10000000u | g)) {
+            ok = false;
+            break;
+          }
+          uint8_t *stage = smem + (long)s * q.a_stage_bytes;
+          if (JA < njobs) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (da[k] != ~0u) store_slice<PREC, E>(stage + da[k], stage + lo_off + da[k], va[k], amax);
+          }
+          if (++ps == q.S) { ps = 0; pph ^= 1; }
+          ++g;
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {  // (CTA pairs: the even CTA's barrier)
+            if constexpr (PAIR) ptx::mbar_arrive_at(&a_full[s], 0);
+            else ptx::mbar_arrive(&a_full[s]);
+          }
+          if (un >= units) break;
+          u = un;
+          c = cn;
+          ss = sn;
+          rot = rotn;
+          JA = JB;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            da[k] = db[k];
+#pragma unroll
+            for (int e = 0; e < E; ++e) va[k][e] = vb[k][e];
+          }
+        }
+      }
+    }
+    if (!db_done) {
     // Job J of a stage goes to producer warp (rot + J) % kProdWarps, where
     // rot counts the jobs of all earlier stages: the remainder of
     // njobs / kProdWarps moves round the warps instead of always landing on
     // the first ones.
     int rot = 0;
-    uint32_t last_b = 0xffffffffu;  // last chunk whose weights this warp streamed
     // ring positions kept as counters (no integer division in the loop):
     // stage ps of phase pph; weight slot psb of phase psbph
     int ps = 0, psb = 0;
@@ -1546,6 +1652,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         }
       }
     }
+    }  // !db_done
     if (amax >= 65520.0f) atomicOr(p.status, ST_RANGE);  // some hi part overflowed
     atomicMax(&ctl->amax_bits, __float_as_uint(amax));    // |x| >= 0: bits order as values
     // drain outstanding weight copies before the CTA can exit
