@@ -1297,16 +1297,19 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
     bool tma_done = false;
     if constexpr (!S2 && !SP && !POOL) {  // the pooled instances keep the smaller code
       if (q.TMA) {
-        // ---- tensor-copy staging.  Warp kProdWarp0 (its first lane) issues
+        // ---- tensor-copy staging.  One producer warp (its first lane) issues
         // one tiled tensor copy per (chunk, depth slice) into the raw ring and
-        // streams the weights; warps kProdWarp0+1.. split each raw slice into
-        // the stage's hi / lo slices (zeros outside the image come from the
-        // copy itself).
+        // streams the weights; the others split each raw slice into the
+        // stage's hi / lo slices (zeros outside the image come from the copy
+        // itself).  The loader is the producer warp on the MMA warp's
+        // scheduler (warp w issues on scheduler w % 4): its light work there
+        // instead of a converter's.
+        constexpr int kLoaderPw = ((kMmaWarp & 3) - (kProdWarp0 & 3) + 4) & 3;
         uint8_t *raw0 = smem + q.off_raw;
         int rs = 0;
         uint32_t rph = 0;
         const int iw_adj = CL ? 0 : q.coff;
-        if (pw == 0) {
+        if (pw == kLoaderPw) {
           ptx::tma_prefetch_desc(&tmx);
           int last_rs = -1;
           uint32_t last_par = 0;  // bit r: phase parity of the last copy into slot r
@@ -1381,7 +1384,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
               wait_bar(bars, RAW_FULL + r, (last_par >> r) & 1u, &no_abort, p.status,
                        0x15000000u | r);
           }
-          if (pt == 0 && q.b_resident)
+          if (lane == 0 && q.b_resident)  // the resident weights' copy (issued by pt 0)
             wait_bar(bars, B_FULL, 0, abort_flag, p.status, 0x12000000u);
           if (lane == 0 && !q.b_resident && g > 0) {
             const uint32_t lb = g - 1;
@@ -1389,7 +1392,8 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
                      0x13000000u | lb);
           }
         } else {
-          const int ct = pt - 32;  // converter thread, 0 .. 32 (kProdWarps - 1) - 1
+          // converter thread, 0 .. 32 (kProdWarps - 1) - 1
+          const int ct = (pw < kLoaderPw ? pw : pw - 1) * 32 + lane;
           constexpr int kConv = 32 * (kProdWarps - 1);
           const int lo_off = q.P * q.plane_bytes;
           const int items = q.P * q.RIN * q.LW;  // (plane, row, column) per depth slice
