@@ -138,7 +138,7 @@ def pipe_peak_tflops(variant: str, peaks, basis: str = "burst") -> tuple[float, 
             "fp32 FFMA: 152 SMs x 128 lanes x 2 x max SM clock")
 
 
-# HBM bandwidth the survey's roofline names ("~8 TB/s"), reported beside the
+# nominal HBM3e bandwidth of a GB300 (~8 TB/s), reported beside the
 # measured copy bandwidth
 NOMINAL_HBM_GBS = 8000.0
 

@@ -139,7 +139,7 @@ typedef enum {
  * the tensor-core variants the square odd kernels at stride / dilation
  * 1-2 whose plan fits (they stage stride 2 as even/odd row x column
  * sub-planes).  N = 0 is a valid empty call (nothing is launched).
- * Argument order: the survey's boundary lists (..., stride, pad, epi, ...);
+ * Argument order: the boundary's base form is (..., stride, pad, epi, ...);
  * `dilation` is inserted after `pad` (every variant takes it). */
 FC_API fc_status fc_conv2d_epi(const float *x, int N, int C_in, int H, int W,
                         const float *w, int C_out, int kH, int kW, int stride,
