@@ -218,3 +218,42 @@ def test_cpu_sample_counts_the_macs_it_runs():
     per5 = 256 * 256 * 64 * 9
     assert macs == per3 + per4 + 16 * per5
     assert "1 image(s)" in desc and "16 (n, c_out)" in desc
+
+
+def _run_bench(args, env_extra=None):
+    import subprocess
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                          env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the CPU oracle on a bounded sample and
+    prints one JSON line with the contract's keys (no GPU needed)."""
+    import json
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-scale", "1"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["warmup"] >= 3 and d["steps"] == 1 and d["value"] > 0
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    _run, macs, desc = bench.cpu_sample(1)
+    assert d["value"] == pytest.approx(2.0 * macs / (d["ms_per_step"] * 1e-3) / 1e9, rel=1e-9)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["sample"] == desc == d["config"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-scale", "1"],
+                   {"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
