@@ -619,7 +619,8 @@ def widened_convT_s2(fc, d5, flush, stream, peaks, reps=20):
 def widened_general_pool(fc, d5, flush, stream, peaks, reps=10):
     """Transposed conv (stride 1) on 16 images of the pooled workload's input
     [16,64,256,256] -> 3x3 max pool, stride 2 (overlapping, floor extent
-    127 x 127) -> hardtanh -> mean -> tanh, fused on the CUDA-core kernel.
+    127 x 127) -> hardtanh -> mean -> tanh, fused in the variant the library
+    picks (the tensor cores' general-pool units).
     Useful FLOPs = 2 x conv MACs (each conv output counted once; the kernel
     recomputes the outputs shared by overlapping windows, 2.25x here)."""
     import torch
