@@ -886,6 +886,9 @@ def run_profile_case(args):
     nb = args.profile_batch or spec["x"][0]
     inp = synth.make_inputs(wid, first_images=nb)
     d = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
+    pool = tuple(int(v) for v in args.profile_pool.split(","))
+    if len(pool) != 2 or not all(1 <= v <= 4 for v in pool):
+        raise ValueError("--profile-pool takes K,S with 1 <= K, S <= 4")
     fc.set_variant(args.variant)
     fc.set_staging(args.staging)
     for _ in range(args.profile_reps):
@@ -896,12 +899,12 @@ def run_profile_case(args):
                    ("gelu_erf",))
             y = fc.fc_conv3d_epi(d["x"], d["w"], d["b"], ops)
         else:
-            y = fc.fc_convT2d_pool_mean(d["x"], d["w"], d["b"])
+            y = fc.fc_convT2d_pool_mean(d["x"], d["w"], d["b"], pool=pool)
     torch.cuda.synchronize()
     if fc.get_last_device_error() != 0:
         raise RuntimeError("device status word set")
     print(f"profile case: workload {wid} batch {nb} variant {fc.last_variant()} "
-          f"out {tuple(y.shape)}")
+          f"pool {pool} out {tuple(y.shape)}")
     return 0
 
 
@@ -926,6 +929,8 @@ def main():
                     help="run only this workload (1..5) --profile-reps times, for profilers")
     ap.add_argument("--profile-batch", type=int, default=0)
     ap.add_argument("--profile-reps", type=int, default=2)
+    ap.add_argument("--profile-pool", default="2,2",
+                    help="max-pool window,stride of the pooled workload's profile case")
     args = ap.parse_args()
     if args.profile_workload:
         return run_profile_case(args)
