@@ -179,6 +179,11 @@ struct TcPlan {
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kMaxCoTc = 512;  // output channels the tensor-core path stages in smem
+// General max pool: channel rows of the row-maxima buffer are 129 floats
+// apart, so the 32 channels a warp reads at one column fall in 32 banks
+// (at 128 they all fell in one: 51 M conflicted loads in a 3x3/2 pool of
+// 16x64x256x256).
+constexpr int kXbPitch = 129;
 
 struct SmemCtl {
   uint32_t tmem_base;
@@ -282,7 +287,7 @@ TcPlan make_plan_u(const ConvProblem &p, int prec, int U, bool allow_pair = true
     q.COLSTEP = q.PJ * p.ps;
     q.n_ct = cdiv(Wp, q.PJ);
     q.ROWSTEP = p.ps;
-    q.XB = 64 * 128 * 4;  // row maxima of 64 channels x 128 columns
+    q.XB = 64 * kXbPitch * 4;  // row maxima of 64 channels x 128 columns
   }
   if (!q.S2) {  // output rows u read input rows u + kh DIL: UR + (KH - 1) DIL rows
     q.RIN = q.U * q.R + spanh;
@@ -1997,7 +2002,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         // maximum over the unit's U conv rows (the pooled row's window rows)
         // goes to shared memory, the accumulator is released, and the 256
         // epilogue threads take the windows across columns there.
-        float *xb = reinterpret_cast<float *>(smem + q.off_xb);  // [64 channels][128 columns]
+        float *xb = reinterpret_cast<float *>(smem + q.off_xb);  // [64 channels][kXbPitch]
 #pragma unroll 1
         for (int cc = 0; cc < 32; cc += 16) {
           float mx[16];
@@ -2015,7 +2020,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
             }
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) xb[(ch0 + cc + j) * 128 + m] = mx[j];
+          for (int j = 0; j < 16; ++j) xb[(ch0 + cc + j) * kXbPitch + m] = mx[j];
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -2031,7 +2036,7 @@ tc_conv_kernel(ConvProblem p, TcPlan q, const uint8_t *__restrict__ bimg,
         float sum = 0.0f;
         for (int j = jq; j < q.PJ; j += 4) {
           if (up.ct * q.PJ + j >= Wp) break;
-          const float *w = xb + ch * 128 + j * p.ps;
+          const float *w = xb + ch * kXbPitch + j * p.ps;
           float mxw = w[0];
           for (int a = 1; a < p.pk; ++a) mxw = fmaxf(mxw, w[a]);
           sum += fminf(fmaxf(mxw + bias, p.ht_lo), p.ht_hi);
