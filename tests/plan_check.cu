@@ -255,6 +255,23 @@ void check(const char *name, ConvProblem p) {
         REQ(2048 + 512 + j * 16 + 16 <= 3072, "%s pair N64 slice", name);
       }
     }
+    if (q.GP) {
+      // General max pool: the row maxima buffer [64 channels][kXbPitch]
+      // lies inside the plan's shared memory; every window reads columns
+      // below 128 of its channel row; and the 32 channels one warp's window
+      // threads read at a column (thread e of the epilogue takes channel
+      // e % 64) fall in 32 distinct banks.
+      REQ(q.XB == 64 * kXbPitch * 4 && kXbPitch >= 128, "%s row-maxima buffer size", name);
+      REQ(q.off_xb >= q.off_misc + (int)sizeof(SmemCtl) && q.off_xb + q.XB <= q.smem_bytes,
+          "%s row-maxima buffer inside shared memory", name);
+      REQ(q.PJ >= 1 && (q.PJ - 1) * p.ps + p.pk <= 128, "%s windows inside the strip", name);
+      for (int c0 = 0; c0 < 64; c0 += 32)
+        for (int col = 0; col < 128; ++col) {
+          uint32_t banks = 0;
+          for (int l = 0; l < 32; ++l) banks |= 1u << (((c0 + l) * kXbPitch + col) % 32);
+          REQ(banks == 0xffffffffu, "%s window loads of a warp share banks (col %d)", name, col);
+        }
+    }
     std::vector<int> seen(kMaxTaps + 2, 0);
     for (int k = 0; k < kMaxTaps + 2; ++k) if (q.perm[k] < q.TAPS) seen[q.perm[k]]++;
     for (int t = 0; t < q.TAPS; ++t) REQ(seen[t] == 1, "%s perm", name);
