@@ -874,6 +874,17 @@ def variant_table_header(tab) -> str:
     return "\n".join(lines) + "\n"
 
 
+def parse_pool(text: str) -> tuple[int, int]:
+    """`K,S` of --profile-pool: max-pool window and stride, each 1..4."""
+    try:
+        pool = tuple(int(v) for v in text.split(","))
+    except ValueError:
+        pool = ()
+    if len(pool) != 2 or not all(1 <= v <= 4 for v in pool):
+        raise ValueError(f"--profile-pool takes K,S with 1 <= K, S <= 4, not {text!r}")
+    return pool
+
+
 def run_profile_case(args):
     """Run one workload (optionally at a smaller batch) `--profile-reps`
     times through the public API and exit: the command profilers wrap."""
@@ -886,9 +897,7 @@ def run_profile_case(args):
     nb = args.profile_batch or spec["x"][0]
     inp = synth.make_inputs(wid, first_images=nb)
     d = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
-    pool = tuple(int(v) for v in args.profile_pool.split(","))
-    if len(pool) != 2 or not all(1 <= v <= 4 for v in pool):
-        raise ValueError("--profile-pool takes K,S with 1 <= K, S <= 4")
+    pool = parse_pool(args.profile_pool)
     fc.set_variant(args.variant)
     fc.set_staging(args.staging)
     for _ in range(args.profile_reps):
@@ -932,6 +941,7 @@ def main():
     ap.add_argument("--profile-pool", default="2,2",
                     help="max-pool window,stride of the pooled workload's profile case")
     args = ap.parse_args()
+    parse_pool(args.profile_pool)  # refuse a bad window before any build or device work
     if args.profile_workload:
         return run_profile_case(args)
     if args.variant_table:

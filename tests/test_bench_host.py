@@ -257,3 +257,12 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-scale", "1"],
                    {"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_profile_pool_parsing():
+    assert bench.parse_pool("3,2") == (3, 2) and bench.parse_pool("2,2") == (2, 2)
+    for bad in ("3", "0,2", "5,1", "3,2,1", "a,b", ""):
+        with pytest.raises(ValueError):
+            bench.parse_pool(bad)
+    r = _run_bench(["--profile-workload", "5", "--profile-pool", "9,9"])
+    assert r.returncode != 0 and "--profile-pool" in r.stderr
