@@ -874,6 +874,31 @@ def variant_table_header(tab) -> str:
     return "\n".join(lines) + "\n"
 
 
+def install_variant_table(src_json: str, csrc: str | None = None) -> int:
+    """Copy a table measured by --variant-table into the library's sources:
+    the JSON beside the header, and the header's rows and GPU name.  The
+    rest of fc_variant_table.h (row type, lookup) is kept.  Returns the
+    number of rows."""
+    import re
+    csrc = csrc or os.path.join(ROOT, "convolution_epilogue_gb300", "csrc")
+    with open(src_json) as f:
+        tab = json.load(f)
+    with open(os.path.join(csrc, "fc_variant_table.json"), "w") as f:
+        json.dump(tab, f, indent=1)
+    hp = os.path.join(csrc, "fc_variant_table.h")
+    with open(hp) as f:
+        h = f.read()
+    head = "static const VariantRow kVariantTable[] = {\n"
+    a = h.index(head) + len(head)
+    b = h.index("};\nstatic const char kVariantTableSource[]")
+    h = h[:a] + variant_table_header(tab) + h[b:]
+    h = re.sub(r"// Measured on .* \(fc_variant_table.json",
+               lambda m: f"// Measured on {tab['gpu']} (fc_variant_table.json", h)
+    with open(hp, "w") as f:
+        f.write(h)
+    return len(tab["rows"])
+
+
 def parse_pool(text: str) -> tuple[int, int]:
     """`K,S` of --profile-pool: max-pool window and stride, each 1..4."""
     try:
@@ -934,6 +959,8 @@ def main():
     ap.add_argument("--variant-table", default="",
                     help="time every variant / staging on the table's shapes; write JSON and .h here")
     ap.add_argument("--table-reps", type=int, default=7)
+    ap.add_argument("--install-variant-table", default="",
+                    help="copy a table measured by --variant-table into the library's sources")
     ap.add_argument("--profile-workload", type=int, default=0,
                     help="run only this workload (1..5) --profile-reps times, for profilers")
     ap.add_argument("--profile-batch", type=int, default=0)
@@ -942,6 +969,9 @@ def main():
                     help="max-pool window,stride of the pooled workload's profile case")
     args = ap.parse_args()
     parse_pool(args.profile_pool)  # refuse a bad window before any build or device work
+    if args.install_variant_table:
+        print(f"installed {install_variant_table(args.install_variant_table)} rows")
+        return 0
     if args.profile_workload:
         return run_profile_case(args)
     if args.variant_table:

@@ -266,3 +266,27 @@ def test_profile_pool_parsing():
             bench.parse_pool(bad)
     r = _run_bench(["--profile-workload", "5", "--profile-pool", "9,9"])
     assert r.returncode != 0 and "--profile-pool" in r.stderr
+
+
+def test_install_variant_table_reproduces_the_committed_header(tmp_path):
+    """Installing the committed measurements into copies of the library's
+    table files gives the committed files back, byte for byte; a changed
+    measurement reaches the header's row."""
+    import json
+    csrc = os.path.join(ROOT, "convolution_epilogue_gb300", "csrc")
+    for f in ("fc_variant_table.h", "fc_variant_table.json"):
+        shutil.copy(os.path.join(csrc, f), tmp_path / f)
+    src = tmp_path / "measured.json"
+    shutil.copy(os.path.join(csrc, "fc_variant_table.json"), src)
+    n = bench.install_variant_table(str(src), str(tmp_path))
+    for f in ("fc_variant_table.h", "fc_variant_table.json"):
+        with open(os.path.join(csrc, f), "rb") as a:
+            assert (tmp_path / f).read_bytes() == a.read(), f
+    tab = json.loads(src.read_text())
+    assert n == len(tab["rows"])
+    tab["rows"][0]["ms"][0] = 9.87654
+    tab["gpu"] = "TEST GPU"
+    src.write_text(json.dumps(tab))
+    bench.install_variant_table(str(src), str(tmp_path))
+    h = (tmp_path / "fc_variant_table.h").read_text()
+    assert "{9.87654f," in h and "// Measured on TEST GPU (fc_variant_table.json" in h

@@ -1,8 +1,9 @@
 """The automatic choice against the measured table it compiles in (no GPU).
 
-`python bench.py --variant-table ...` times every (variant, input staging)
-pair on a grid of shapes on a GB300 and writes the measurements
-(convolution_epilogue_gb300/csrc/fc_variant_table.json) and the C rows the
+`python bench.py --variant-table T.json` times every (variant, input
+staging) pair on a grid of shapes on a GB300 and writes the measurements;
+`python bench.py --install-variant-table T.json` copies them into
+convolution_epilogue_gb300/csrc/fc_variant_table.json and the C rows the
 library compiles in (fc_variant_table.h).  These tests check that the
 compiled rows are those measurements, and that for every measured shape the
 library's selection (fc_select_variant, which runs no kernel) is the
